@@ -1,0 +1,19 @@
+"""CPU oracle of the MoE layer forward pass (test infrastructure, not product code).
+
+Only the tests, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline and
+reference legs may import this package.  It shares no code with the CUDA library.
+"""
+
+from .moe_oracle import (  # noqa: F401
+    combine,
+    gate_drop,
+    grouped_ffn,
+    moe_layer,
+    moe_layer_tokens,
+    permute,
+    route,
+    router_logits,
+    silu,
+    swiglu_ffn,
+    topk_softmax,
+)
