@@ -1,0 +1,412 @@
+"""Benchmark of the MoE layer forward pass on GB300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config mixtral|qwen_prefill|qwen_decode|deepseek|toy] [--tokens T]
+
+A step is one moe_layer_forward over one batch of synthetic tokens (router, top-k,
+gate drop, permutation, grouped SwiGLU FFN, shared expert, combine).  Timing: CUDA
+events on the launching stream around each step, with an L2 flush (a 512 MiB write)
+between steps outside the events; W untimed warm-up steps; max over ranks.  With
+N > 1 (torchrun) every rank runs an independent replica on its own GPU (the layer has
+no exchange step on one GPU): weak scaling, value = all tokens / slowest rank's time.
+
+Extra keys: "roofline" for the dominant kernel (the grouped gate/up GEMM, timed alone
+through moe_expert_gate_up), "cpu_baseline" (the CPU oracle on a bounded token sample),
+"e2e" (the same metric with host buffers: H2D of x and D2H of y inside the timed
+region), "stages_us" (route / permute / gate_up / down / shared / combine, timed one by
+one), "clocks" (nvidia-smi samples taken during the timed region).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+FLUSH_BYTES = 512 << 20
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="mixtral", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--tokens", type=int, default=None, help="token count (decode sweeps)")
+    ap.add_argument("--cpu-sample", type=int, default=None, help="tokens in the CPU-oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    if os.path.exists(PEAKS_FILE):
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_launches_per_step(shape, T):
+    """Kernels this library launches for one moe_layer_forward (the count is exact: it
+    mirrors the launch sequence of the C ABI for this config)."""
+    if T == 0:
+        return 0
+    n = 0
+    tc_router = shape.dtype == "bf16" and T >= 256 and shape.E >= 32 and shape.E % 16 == 0
+    n += 2 if tc_router else 1            # router GEMM + top-k, or the fused SIMT router
+    n += 3                                # rank, scan, scatter-gather
+    n += 2                                # grouped gate/up, grouped down
+    if shape.I_shared:
+        n += 2
+    n += 1                                # combine
+    return n
+
+
+def algorithmic(shape, T, counts):
+    """FLOPs and bytes the layer must do (not the dense work it avoids)."""
+    M = int(counts.sum())
+    touched = int((counts > 0).sum())
+    b = 2 if shape.dtype == "bf16" else 4
+    H, E, I, Is = shape.H, shape.E, shape.I, shape.I_shared
+    flops = 2 * T * E * H + 6 * H * I * M + 6 * H * Is * T
+    byts = T * H * b + E * H * b + 3 * H * I * b * touched + 3 * H * Is * b + T * H * b
+    gate_up_flops = 4 * H * I * M
+    gate_up_bytes = M * H * b + 2 * I * H * b * touched + M * I * b
+    return dict(M=M, touched=touched, flops=flops, bytes=byts, gate_up_flops=gate_up_flops,
+                gate_up_bytes=gate_up_bytes)
+
+
+def run_ours(args, rank, world, local):
+    import mixture_experts_layer_04_gb300 as moe
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    moe.load()
+    shape = synth.WORKLOADS[args.config]
+    T = args.tokens if args.tokens is not None else shape.T
+    inp = synth.make_inputs(shape.with_(seed=shape.seed + rank), device=dev, T=T)
+    dt = moe.BF16 if shape.dtype == "bf16" else moe.F32
+    cfg = moe.MoEConfig.make(T, shape.H, shape.E, shape.K, shape.I, shape.I_shared, shape.theta, dt)
+    ws = torch.empty(moe.workspace_size(cfg), dtype=torch.uint8, device=dev)
+    y = torch.empty(T, shape.H, dtype=shape.torch_dtype, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        moe.layer_forward(cfg, inp["x"], inp["w_router"], inp["router_bias"], inp["w_gate_up"],
+                          inp["w_down"], inp.get("w_shared_gate_up"), inp.get("w_shared_down"),
+                          y, None, ws, stream=stream)
+
+    def timed(fn, n):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        return [a.elapsed_time(b) for a, b in evs]
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    moe.sync_check(stream)
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t_wall0 = time.perf_counter()
+        times = timed(step, args.steps)
+        t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        torch.distributed.barrier()
+    moe.sync_check(stream)
+    ms = statistics.mean(times)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # routing statistics of this batch (counts come from the layer's own workspace)
+    views = moe.workspace_views(cfg, ws)
+    off = views["counts"] - ws.data_ptr()
+    counts = ws[off:off + 4 * shape.E].view(torch.int32).cpu().numpy()
+    alg = algorithmic(shape, T, counts)
+
+    # per-stage times (M1: route, permute, expert GEMMs and combine measured separately)
+    stages = {}
+    E, K, H_ = shape.E, shape.K, shape.H
+    logits = torch.empty(T, E, dtype=torch.float32, device=dev)
+    ids = torch.empty(T, K, dtype=torch.int32, device=dev)
+    w = torch.empty(T, K, dtype=torch.float32, device=dev)
+    counts_t = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(T * K, dtype=torch.int32, device=dev)
+    inv = torch.empty(T * K, dtype=torch.int32, device=dev)
+    x_perm = torch.empty(T * K, H_, dtype=shape.torch_dtype, device=dev)
+    h = torch.empty(T * K, shape.I, dtype=shape.torch_dtype, device=dev)
+    out_perm = torch.empty(T * K, H_, dtype=torch.float32, device=dev)
+    nst = max(3, min(args.steps, 10))
+    stages["route"] = timed(lambda: moe.route(cfg, inp["x"], inp["w_router"], inp["router_bias"],
+                                              logits, ids, w, stream=stream), nst)
+    stages["permute"] = timed(lambda: moe.permute(cfg, inp["x"], ids, counts_t, offsets, perm, inv,
+                                                  x_perm, ws, stream=stream), nst)
+    gate_up_times = timed(lambda: moe.expert_gate_up(cfg, x_perm, offsets, inp["w_gate_up"], h, ws,
+                                                     stream=stream), max(args.steps, 5))
+    stages["gate_up"] = gate_up_times
+    stages["down"] = timed(lambda: moe.expert_down(cfg, h, offsets, inp["w_down"], out_perm, ws,
+                                                   stream=stream), nst)
+    shared_out = None
+    if shape.I_shared:
+        one = moe.MoEConfig.make(T, H_, 1, 1, shape.I_shared, 0, 0.0, dt)
+        ws1 = torch.empty(moe.workspace_size(one), dtype=torch.uint8, device=dev)
+        one_off = torch.tensor([0, T], dtype=torch.int32, device=dev)
+        hs = torch.empty(T, shape.I_shared, dtype=shape.torch_dtype, device=dev)
+        shared_out = torch.empty(T, H_, dtype=torch.float32, device=dev)
+        stages["shared"] = timed(lambda: (
+            moe.expert_gate_up(one, inp["x"], one_off, inp["w_shared_gate_up"].unsqueeze(0), hs, ws1,
+                               stream=stream),
+            moe.expert_down(one, hs, one_off, inp["w_shared_down"].unsqueeze(0), shared_out, ws1,
+                            stream=stream)), nst)
+    stages["combine"] = timed(lambda: moe.combine(cfg, out_perm, inv, w, shared_out, y, None,
+                                                  stream=stream), nst)
+    moe.sync_check(stream)
+    stages_us = {k: round(1e3 * statistics.mean(v), 2) for k, v in stages.items()}
+
+    # roofline of the dominant kernel (grouped gate/up GEMM, timed alone)
+    peaks, peak_kind = load_peaks()
+    gu_s = statistics.mean(gate_up_times) / 1e3
+    decode = T <= 256
+    if decode:
+        achieved = alg["gate_up_bytes"] / gu_s / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
+    else:
+        achieved = alg["gate_up_flops"] / gu_s / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4)}
+    roof["traffic"] = None
+    roof["kernel"] = "tc_grouped_gemm_kernel<256,SwiGLU> (moe_expert_gate_up)"
+    roof["peak_source"] = peak_kind
+
+    # whole-layer roofline: the slower of FLOPs at the bf16 peak and bytes at HBM speed
+    t_roof = max(alg["flops"] / (peaks["bf16_tflops"] * 1e12), alg["bytes"] / (peaks["hbm_gbs"] * 1e9))
+    layer_frac = t_roof / (ms / 1e3)
+
+    # end to end through the public API with host buffers (x in, y out, pinned)
+    x_host = inp["x"].cpu().pin_memory()
+    y_host = torch.empty(T, H_, dtype=shape.torch_dtype).pin_memory()
+    x_dev = torch.empty_like(inp["x"])
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.layer_forward(cfg, x_dev, inp["w_router"], inp["router_bias"], inp["w_gate_up"],
+                          inp["w_down"], inp.get("w_shared_gate_up"), inp.get("w_shared_down"),
+                          y, None, ws, stream=stream)
+        y_host.copy_(y, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    e2e_times = timed(e2e_step, args.steps)
+    e2e_ms = statistics.mean(e2e_times)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    moe.sync_check(stream)
+
+    res = {
+        "metric": "MoE-layer tokens/s (prefill) & us/layer (decode), % of TC/HBM roofline",
+        "value": round(T * world / (ms / 1e3), 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "us_per_layer": round(ms * 1e3, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": shape.dtype,
+        "data": "synthetic (seeded; x~N(0,1), W_r~N(0,1/H), expert W~N(0,0.02))",
+        "config": {"workload": args.config, "T": T, "H": shape.H, "E": shape.E, "K": shape.K,
+                   "I": shape.I, "I_shared": shape.I_shared, "theta": shape.theta,
+                   "router_bias": shape.bias, "l2": "flushed between steps (512 MiB write)",
+                   "parallelism": "replicas" if world > 1 else "single-gpu",
+                   "kept_assignments": alg["M"], "experts_touched": alg["touched"],
+                   "group_rows_max": int(counts.max()), "empty_experts": int((counts == 0).sum())},
+        "roofline": roof,
+        "layer_roofline": {"t_roofline_us": round(t_roof * 1e6, 2), "frac": round(layer_frac, 4),
+                           "flops": alg["flops"], "bytes": alg["bytes"], "peaks": peak_kind},
+        "stages_us": stages_us,
+        "e2e": {"value": round(T * world / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                "ms_per_step": round(e2e_ms, 4),
+                "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
+                "d2h_bytes_per_step": y_host.numel() * y_host.element_size()},
+        "gpu_launches": kernel_launches_per_step(shape, T) * args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": round(t_wall, 3),
+    }
+    return res, shape, T, inp
+
+
+def oracle_sample(shape, T, inp, n_tokens, seed=0):
+    """Run the CPU oracle on a bounded token sample; returns (seconds, tokens)."""
+    import oracle
+    from synth import to_numpy_f64 as f64
+
+    class Lazy:
+        def __init__(self, w):
+            self.w = w
+
+        def __getitem__(self, e):
+            return f64(self.w[int(e)])
+
+    rng = np.random.default_rng(seed)
+    toks = np.sort(rng.choice(T, size=min(T, n_tokens), replace=False))
+    x = f64(inp["x"][torch.from_numpy(toks).to(inp["x"].device)])
+    bias = inp["router_bias"].cpu().numpy() if inp["router_bias"] is not None else None
+    sh = {}
+    if shape.I_shared:
+        sh = dict(w_shared_gate_up=f64(inp["w_shared_gate_up"]), w_shared_down=f64(inp["w_shared_down"]))
+    t0 = time.perf_counter()
+    oracle.moe_layer_tokens(x, f64(inp["w_router"]), Lazy(inp["w_gate_up"]), Lazy(inp["w_down"]),
+                            shape.K, shape.theta, bias, **sh)
+    return time.perf_counter() - t0, len(toks)
+
+
+def default_sample(shape, T):
+    return min(T, {"toy": 256, "mixtral": 16, "qwen_prefill": 256, "qwen_decode": 64,
+                   "deepseek": 8}.get(shape.name, 32))
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.distributed.init_process_group(backend="nccl" if args.impl == "ours" else "gloo")
+    if args.impl == "reference":
+        # The reference arm is the CPU oracle as it stands (rank 0 only).
+        if rank != 0:
+            return
+        shape = synth.WORKLOADS[args.config]
+        T = args.tokens if args.tokens is not None else shape.T
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        inp = synth.make_inputs(shape, device=dev, T=T)
+        n = args.cpu_sample or default_sample(shape, T)
+        for _ in range(args.warmup):
+            oracle_sample(shape, T, inp, max(1, n // 4), seed=99)
+        secs = [oracle_sample(shape, T, inp, n, seed=s)[0] for s in range(args.steps)]
+        rate = n / statistics.mean(secs)
+        res = {"impl": "reference",
+               "metric": "MoE-layer tokens/s (prefill) & us/layer (decode), % of TC/HBM roofline",
+               "value": round(rate, 3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+               "warmup": args.warmup, "ms_per_step": round(1e3 * statistics.mean(secs), 2),
+               "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+               "dtype": "f64", "data": "synthetic",
+               "config": {"workload": args.config, "T": T},
+               "cpu_baseline": {"value": round(rate, 3), "unit": "tokens/s",
+                                "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": f"{n} random tokens of the {T}-token batch per step"},
+               "e2e": {"value": round(rate, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                       "d2h_bytes_per_step": 0}}
+        print(json.dumps(res))
+        return
+    res, shape, T, inp = run_ours(args, rank, world, local)
+    if rank == 0 and not args.no_cpu_baseline:
+        n = args.cpu_sample or default_sample(shape, T)
+        secs, nt = oracle_sample(shape, T, inp, n)
+        res["cpu_baseline"] = {"value": round(nt / secs, 3), "unit": "tokens/s",
+                               "cores": os.cpu_count(), "kind": "oracle",
+                               "sample": f"{nt} random tokens of the {T}-token batch, float64 numpy"}
+    if rank == 0:
+        print(json.dumps(res))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,210 @@
+/*
+ * moe.h -- C ABI of a single-GPU Mixture-of-Experts feed-forward layer (forward pass)
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The layer follows the pipeline that the page opening
+ * "MoE通过稀疏激活降低每个token的计算量但增加了服务系统的复杂度" describes in its section
+ * "单机MoE执行流水线": the router scores every expert, top-k keeps the chosen expert ids
+ * and weights, a permutation writes the token rows in expert order and records an
+ * inverse map, a grouped GEMM runs every expert's ragged row block in one launch, each
+ * expert applies its activation and output projection, and an un-permute restores token
+ * order, applies the route weights and sums the contributions of each token.  The
+ * routing rule (softmax over the top-k logits, then drop gates below a threshold and
+ * renormalise) is section 2.2 of the page "MoE大模型的智能调度：从1.8万亿参数到每token仅激活
+ * 2%的工程真相".
+ *
+ * Notation: T tokens, H hidden size, E routed experts, K experts per token, I expert
+ * intermediate size, I_shared intermediate size of the always-on shared expert (0 =
+ * none), theta the gate-drop threshold (0 = off), M the number of kept assignments
+ * (M = T*K when theta = 0).
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ *  - Every tensor pointer is DEVICE memory owned by the caller, row-major and
+ *    contiguous, 16-byte aligned.  "act" below means the configured activation/weight
+ *    type: bfloat16 when cfg->dtype == MOE_BF16, float when cfg->dtype == MOE_F32.
+ *  - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL = legacy default
+ *    stream) and the call returns without synchronising.  The library never allocates
+ *    or frees device memory on these paths and never synchronises the device.
+ *  - Arguments are validated on the host before any launch; on any error nothing is
+ *    launched and the outputs are untouched.  No C++ exception crosses this boundary.
+ *  - T == 0 is a valid no-op: the call returns MOE_OK after checking `cfg` only (the
+ *    pointers of an empty batch may be NULL).
+ *  - Supported shapes: 1 <= K <= min(E, 16), E <= 1024, H and I multiples of 64,
+ *    0 <= theta < 1, H <= 65536, I <= 65536, T*K < 2^31.
+ *  - Asynchronous device errors (a bounded wait that timed out inside a kernel) are
+ *    recorded in a device error word and reported by moe_sync_check().
+ *  - Calls are deterministic: the same inputs give bitwise-identical outputs.
+ *  - Calls with separate workspaces may run concurrently on different streams.
+ */
+#ifndef MOE_GB300_MOE_H
+#define MOE_GB300_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* null pointer, bad shape, bad threshold */
+  MOE_ERR_UNSUPPORTED = 2,   /* shape/type outside the supported set, or no sm_103a device */
+  MOE_ERR_WORKSPACE = 3,     /* workspace missing or smaller than moe_workspace_size() */
+  MOE_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed (launch error, ...) */
+  MOE_ERR_TIMEOUT = 5,       /* a bounded device-side wait gave up (see moe_sync_check) */
+  MOE_ERR_INTERNAL = 6,      /* an internal consistency check failed */
+  MOE_ERR_MISALIGNED = 7     /* a pointer is not 16-byte aligned */
+} moe_status_t;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
+
+typedef struct {
+  int32_t T;               /* tokens */
+  int32_t H;               /* hidden size */
+  int32_t E;               /* routed experts */
+  int32_t K;               /* experts per token (top-k) */
+  int32_t I;               /* routed expert intermediate size */
+  int32_t I_shared;        /* shared expert intermediate size, 0 = no shared expert */
+  float gate_threshold;    /* theta: drop kept gates below it (slot 0 never), 0 = off */
+  int32_t dtype;           /* moe_dtype_t of activations and weights */
+  uint32_t flags;          /* reserved, must be 0 */
+} moe_config_t;
+
+typedef void* moe_stream_t; /* a cudaStream_t */
+
+/* Bytes of device workspace that moe_layer_forward, moe_permute and moe_grouped_ffn
+ * need for `cfg` (the largest of the three).  The workspace is scratch: its contents
+ * are undefined between calls, and it must not be shared by calls that may run
+ * concurrently.  Returns MOE_ERR_INVALID_ARG for an unsupported config. */
+moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes);
+
+/* Router scores and routing.
+ * Defined by: "MoE大模型的智能调度…" §2.2 routing steps 1-3 (logits per expert, softmax
+ * over the top-k logits, drop gates below the threshold and renormalise) and the
+ * page section "单机MoE执行流水线" (the router scores every candidate expert; top-k keeps
+ * the chosen ids and weights).
+ *   x           [T,H] act, or NULL: then `logits` is an INPUT [T,E] float that is read
+ *               (router_bias is then ignored).
+ *   w_router    [E,H] act (ignored when x == NULL).
+ *   router_bias [E] float added to every token's logits, or NULL for none.
+ *   logits      [T,E] float: written with x*W_r^T + bias (fp32 accumulation) when x != NULL.
+ *   topk_ids    [T,K] int32 out: slot 0 = largest logit, descending, ties to the lower
+ *               expert id; a dropped slot holds -1 (dropped slots form a suffix).
+ *   topk_w      [T,K] float out: softmax over the K kept logits, after the drop the
+ *               survivors renormalised to sum 1; dropped slots hold 0.
+ * The selection is taken on float32 logits. */
+moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* w_router,
+                       const float* router_bias, float* logits, int32_t* topk_ids,
+                       float* topk_w, moe_stream_t stream);
+
+/* Dispatch: group the assignments by expert (a stable permutation) and gather rows.
+ * Defined by: page section "一个批次如何变成各专家专属的矩阵" (assignments grouped by
+ * expert into matrices, the source token id kept beside each row) and section
+ * "单机MoE执行流水线" (the permutation writes token rows in expert order and records an
+ * inverse map for the combine).
+ *   x         [T,H] act in.
+ *   topk_ids  [T,K] int32 in (from moe_route; -1 = dropped, not dispatched).
+ *   counts    [E] int32 out: rows per expert.
+ *   offsets   [E+1] int32 out: exclusive prefix sum of counts; offsets[E] = M.
+ *   perm      [T*K] int32 out: perm[r] = source token of row r, rows ordered by
+ *             (expert ascending, token ascending); entries r >= M are untouched.
+ *   inv       [T*K] int32 out: inv[t*K+k] = row of assignment (t,k), -1 if dropped.
+ *   x_perm    [T*K,H] act out: x_perm[r] = x[perm[r]]; rows r >= M untouched.
+ *   ws        workspace of at least moe_workspace_size() bytes. */
+moe_status_t moe_permute(const moe_config_t* cfg, const void* x, const int32_t* topk_ids,
+                         int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                         void* x_perm, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Grouped expert FFN over ragged row groups (one launch per GEMM for all experts).
+ * Defined by: page section "单机MoE执行流水线" (a grouped GEMM runs several experts'
+ * matrices of different row counts in one launch, then each expert applies its
+ * activation and output projection) and "MoE大模型的智能调度…" §2.2 expert layer (every
+ * expert is a two-layer FFN of the same shape with its own weights).  Activation:
+ * SwiGLU, out = (silu(x W_g^T) * (x W_u^T)) W_d^T; the intermediate h is rounded to
+ * `act` between the two GEMMs; accumulation is fp32.
+ *   x_perm    [T*K,H] act in; rows offsets[e]..offsets[e+1]-1 belong to expert e.
+ *   offsets   [E+1] int32 in (device).
+ *   w_gate_up [E,2I,H] act: rows 0..I-1 of expert e = W_g, rows I..2I-1 = W_u.
+ *   w_down    [E,H,I] act.
+ *   out_perm  [T*K,H] float out; rows r >= offsets[E] untouched.
+ *   ws        workspace of at least moe_workspace_size() bytes. */
+moe_status_t moe_grouped_ffn(const moe_config_t* cfg, const void* x_perm, const int32_t* offsets,
+                             const void* w_gate_up, const void* w_down, float* out_perm,
+                             void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* The first GEMM of the grouped FFN alone: gate/up projection with SwiGLU.
+ * Defined by: page section "单机MoE执行流水线" (grouped GEMM over ragged expert row
+ * groups; each expert applies its activation).  For every row r of group e:
+ *   h[r] = silu(x_perm[r] W_g[e]^T) * (x_perm[r] W_u[e]^T), fp32 accumulation, rounded
+ *   once to `act`.
+ *   x_perm [T*K,H] act in; offsets [E+1] int32 in; w_gate_up [E,2I,H] act;
+ *   h [T*K,I] act out (rows >= offsets[E] untouched); ws as for moe_grouped_ffn. */
+moe_status_t moe_expert_gate_up(const moe_config_t* cfg, const void* x_perm,
+                                const int32_t* offsets, const void* w_gate_up, void* h, void* ws,
+                                size_t ws_bytes, moe_stream_t stream);
+
+/* The second GEMM of the grouped FFN alone: the output projection.
+ * Defined by: page section "单机MoE执行流水线" (each expert applies its output
+ * projection).  For every row r of group e: out_perm[r] = h[r] W_d[e]^T (fp32).
+ *   h [T*K,I] act in; offsets [E+1] int32 in; w_down [E,H,I] act;
+ *   out_perm [T*K,H] float out (rows >= offsets[E] untouched); ws as above. */
+moe_status_t moe_expert_down(const moe_config_t* cfg, const void* h, const int32_t* offsets,
+                             const void* w_down, float* out_perm, void* ws, size_t ws_bytes,
+                             moe_stream_t stream);
+
+/* Un-permute and gated weighted sum back to token order.
+ * Defined by: "MoE大模型的智能调度…" §2.2 fusion layer (output = sum of gate_i *
+ * Expert_i(h)) and page sections "MoE层的结构与token路由" (y = sum over the selected
+ * experts S(x) of w_e(x) E_e(x)) and "单机MoE执行流水线" (restore token order with the
+ * inverse map, apply the route weights, add contributions of the same token id).
+ *   y[t] = sum_{k=0..K-1, inv[t,k] >= 0} topk_w[t,k] * out_perm[inv[t,k]]  (+ shared_out[t])
+ * summed in fp32 in slot order, then rounded once to `act`.
+ *   out_perm   [T*K,H] float in;  inv [T*K] int32 in;  topk_w [T*K] float in.
+ *   shared_out [T,H] float in or NULL.
+ *   y          [T,H] act out.
+ *   y_f32      [T,H] float out (the fp32 sum before rounding) or NULL. */
+moe_status_t moe_combine(const moe_config_t* cfg, const float* out_perm, const int32_t* inv,
+                         const float* topk_w, const float* shared_out, void* y, float* y_f32,
+                         moe_stream_t stream);
+
+/* The whole layer: moe_route -> moe_permute -> moe_grouped_ffn -> (shared expert) ->
+ * moe_combine, on one stream, with every intermediate in `ws`.
+ * The shared expert (page section "MoE层的结构与token路由": not scored by the router, run
+ * for every token) is a SwiGLU FFN of size I_shared added with weight 1.
+ *   x [T,H] act; w_router [E,H] act; router_bias [E] float or NULL;
+ *   w_gate_up [E,2I,H] act; w_down [E,H,I] act;
+ *   w_shared_gate_up [2*I_shared,H] act and w_shared_down [H,I_shared] act, both NULL
+ *   when I_shared == 0;
+ *   y [T,H] act out; y_f32 [T,H] float out or NULL;
+ *   ws workspace of at least moe_workspace_size() bytes. */
+moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const void* w_router,
+                               const float* router_bias, const void* w_gate_up,
+                               const void* w_down, const void* w_shared_gate_up,
+                               const void* w_shared_down, void* y, float* y_f32, void* ws,
+                               size_t ws_bytes, moe_stream_t stream);
+
+/* Intermediates of the last moe_layer_forward that used `ws` (views into ws; valid
+ * until ws is reused).  Any output pointer may be NULL.  Useful to check every stage. */
+moe_status_t moe_workspace_views(const moe_config_t* cfg, void* ws, float** logits,
+                                 int32_t** topk_ids, float** topk_w, int32_t** counts,
+                                 int32_t** offsets, int32_t** perm, int32_t** inv,
+                                 void** x_perm, float** out_perm, float** shared_out);
+
+/* Synchronise `stream` and report (then clear) the device error word of the current
+ * device: MOE_ERR_TIMEOUT if a bounded device-side wait gave up since the last check,
+ * MOE_ERR_CUDA if the stream reports a CUDA error, MOE_OK otherwise. */
+moe_status_t moe_sync_check(moe_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* moe_status_string(moe_status_t status);
+
+/* Library version string ("moe_gb300 <major>.<minor> sm_103a"). */
+const char* moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_MOE_H */

@@ -1,0 +1,195 @@
+"""Thin Python binding of libmoe_gb300 (the C ABI declared in include/moe.h).
+
+Argument marshalling only: every step of the MoE layer runs in the library's CUDA
+kernels.  PyTorch supplies device memory (tensors), streams and the current device.
+Functions take torch CUDA tensors (or raw device addresses as ints, or None for NULL)
+and raise ``MoEError`` when the library returns a status other than MOE_OK.
+
+There is no fallback: if the shared library has not been built, or cannot be
+loaded, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+__all__ = [
+    "MoEConfig", "MoEError", "F32", "BF16", "library_path", "load", "workspace_size",
+    "route", "permute", "grouped_ffn", "expert_gate_up", "expert_down", "combine", "layer_forward", "workspace_views",
+    "sync_check", "status_string", "version",
+]
+
+F32 = 0
+BF16 = 1
+
+_STATUS = {
+    0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
+    4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_INTERNAL", 7: "MOE_ERR_MISALIGNED",
+}
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {_STATUS.get(status, status)}")
+
+
+class MoEConfig(ctypes.Structure):
+    """moe_config_t: T, H, E, K, I, I_shared, gate_threshold, dtype, flags."""
+
+    _fields_ = [
+        ("T", ctypes.c_int32), ("H", ctypes.c_int32), ("E", ctypes.c_int32),
+        ("K", ctypes.c_int32), ("I", ctypes.c_int32), ("I_shared", ctypes.c_int32),
+        ("gate_threshold", ctypes.c_float), ("dtype", ctypes.c_int32), ("flags", ctypes.c_uint32),
+    ]
+
+    @classmethod
+    def make(cls, T, H, E, K, I, I_shared=0, gate_threshold=0.0, dtype=BF16, flags=0):
+        return cls(T, H, E, K, I, I_shared, gate_threshold, dtype, flags)
+
+    def __repr__(self):
+        return (f"MoEConfig(T={self.T}, H={self.H}, E={self.E}, K={self.K}, I={self.I}, "
+                f"I_shared={self.I_shared}, theta={self.gate_threshold}, dtype={self.dtype})")
+
+
+def library_path() -> str:
+    return os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libmoe_gb300.so")
+
+
+_LIB: Optional[ctypes.CDLL] = None
+
+_P = ctypes.c_void_p
+_CFG = ctypes.POINTER(MoEConfig)
+_SIGS = {
+    "moe_workspace_size": [_CFG, ctypes.POINTER(ctypes.c_size_t)],
+    "moe_route": [_CFG, _P, _P, _P, _P, _P, _P, _P],
+    "moe_permute": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+    "moe_grouped_ffn": [_CFG, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+    "moe_expert_gate_up": [_CFG, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+    "moe_expert_down": [_CFG, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+    "moe_combine": [_CFG, _P, _P, _P, _P, _P, _P, _P],
+    "moe_layer_forward": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+    "moe_workspace_views": [_CFG, _P] + [ctypes.POINTER(_P)] * 10,
+    "moe_sync_check": [_P],
+    "moe_status_string": [ctypes.c_int],
+    "moe_version": [],
+}
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libmoe_gb300.so (built by ``build.py``); raises if it is missing."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = path or library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libmoe_gb300.so not built ({path}); run "
+                           "`python -c 'import __graft_entry__ as g; g.build()'` first")
+    lib = ctypes.CDLL(path)
+    for name, args in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_char_p if name in ("moe_status_string", "moe_version") else ctypes.c_int
+    _LIB = lib
+    return lib
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise MoEError(status, where)
+
+
+def status_string(status: int) -> str:
+    return load().moe_status_string(status).decode()
+
+
+def version() -> str:
+    return load().moe_version().decode()
+
+
+def workspace_size(cfg: MoEConfig) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)), "moe_workspace_size")
+    return n.value
+
+
+def route(cfg, x, w_router, router_bias, logits, topk_ids, topk_w, stream=None):
+    _check(load().moe_route(ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(router_bias),
+                            _ptr(logits), _ptr(topk_ids), _ptr(topk_w), _stream(stream)),
+           "moe_route")
+
+
+def permute(cfg, x, topk_ids, counts, offsets, perm, inv, x_perm, ws, ws_bytes=None, stream=None):
+    nb = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check(load().moe_permute(ctypes.byref(cfg), _ptr(x), _ptr(topk_ids), _ptr(counts),
+                              _ptr(offsets), _ptr(perm), _ptr(inv), _ptr(x_perm), _ptr(ws), nb,
+                              _stream(stream)), "moe_permute")
+
+
+def grouped_ffn(cfg, x_perm, offsets, w_gate_up, w_down, out_perm, ws, ws_bytes=None, stream=None):
+    nb = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check(load().moe_grouped_ffn(ctypes.byref(cfg), _ptr(x_perm), _ptr(offsets), _ptr(w_gate_up),
+                                  _ptr(w_down), _ptr(out_perm), _ptr(ws), nb, _stream(stream)),
+           "moe_grouped_ffn")
+
+
+def expert_gate_up(cfg, x_perm, offsets, w_gate_up, h, ws, ws_bytes=None, stream=None):
+    nb = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check(load().moe_expert_gate_up(ctypes.byref(cfg), _ptr(x_perm), _ptr(offsets),
+                                     _ptr(w_gate_up), _ptr(h), _ptr(ws), nb, _stream(stream)),
+           "moe_expert_gate_up")
+
+
+def expert_down(cfg, h, offsets, w_down, out_perm, ws, ws_bytes=None, stream=None):
+    nb = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check(load().moe_expert_down(ctypes.byref(cfg), _ptr(h), _ptr(offsets), _ptr(w_down),
+                                  _ptr(out_perm), _ptr(ws), nb, _stream(stream)),
+           "moe_expert_down")
+
+
+def combine(cfg, out_perm, inv, topk_w, shared_out, y, y_f32=None, stream=None):
+    _check(load().moe_combine(ctypes.byref(cfg), _ptr(out_perm), _ptr(inv), _ptr(topk_w),
+                              _ptr(shared_out), _ptr(y), _ptr(y_f32), _stream(stream)),
+           "moe_combine")
+
+
+def layer_forward(cfg, x, w_router, router_bias, w_gate_up, w_down, w_shared_gate_up,
+                  w_shared_down, y, y_f32, ws, ws_bytes=None, stream=None):
+    nb = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check(load().moe_layer_forward(ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(router_bias),
+                                    _ptr(w_gate_up), _ptr(w_down), _ptr(w_shared_gate_up),
+                                    _ptr(w_shared_down), _ptr(y), _ptr(y_f32), _ptr(ws), nb,
+                                    _stream(stream)), "moe_layer_forward")
+
+
+def workspace_views(cfg, ws) -> dict:
+    """Device addresses (ints) of the intermediates a moe_layer_forward left in `ws`."""
+    names = ["logits", "topk_ids", "topk_w", "counts", "offsets", "perm", "inv", "x_perm",
+             "out_perm", "shared_out"]
+    outs = [_P() for _ in names]
+    _check(load().moe_workspace_views(ctypes.byref(cfg), _ptr(ws), *[ctypes.byref(o) for o in outs]),
+           "moe_workspace_views")
+    return {n: o.value for n, o in zip(names, outs)}
+
+
+def sync_check(stream=None):
+    _check(load().moe_sync_check(_stream(stream)), "moe_sync_check")

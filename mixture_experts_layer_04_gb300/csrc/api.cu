@@ -1,0 +1,509 @@
+// C ABI of the MoE layer (include/moe.h): argument validation, the workspace plan and
+// the order of launches.  Every check happens on the host before the first launch; the
+// library never allocates, frees or synchronises on the compute paths.
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <initializer_list>
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+// Device error word (bits MOE_DEVERR_*), one per device that loads the library.
+__device__ unsigned g_error_word;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  bool supported = false;
+  int num_sms = 0;
+  unsigned* err = nullptr;
+};
+
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+// Per-device setup on first use: checks for an sm_103 device and looks up the device
+// address of the error word (the host-side symbol is not a device address).
+const DeviceInfo* device_info() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return nullptr;
+    d.supported = (prop.major == 10 && prop.minor == 3);
+    d.num_sms = prop.multiProcessorCount;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    d.err = static_cast<unsigned*>(p);
+    d.ready = true;
+  }
+  return &d;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status_t check_config(const moe_config_t* c) {
+  if (c == nullptr) return MOE_ERR_INVALID_ARG;
+  if (c->flags != 0u) return MOE_ERR_INVALID_ARG;
+  if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (c->T < 0 || c->H <= 0 || c->E <= 0 || c->K <= 0 || c->I <= 0 || c->I_shared < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (c->K > c->E || c->K > 16 || c->E > 1024) return MOE_ERR_INVALID_ARG;
+  if (c->H % 64 != 0 || c->I % 64 != 0 || c->I_shared % 64 != 0) return MOE_ERR_INVALID_ARG;
+  if (c->H > 65536 || c->I > 65536 || c->I_shared > 65536) return MOE_ERR_INVALID_ARG;
+  if (!(c->gate_threshold >= 0.0f && c->gate_threshold < 1.0f)) return MOE_ERR_INVALID_ARG;
+  if (static_cast<long long>(c->T) * c->K >= (1ll << 31)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+// Workspace plan: every region 256-byte aligned.
+struct Plan {
+  size_t logits, ids, w, counts, offsets, perm, inv, perm_ws, table, num_mt, x_perm, h, out_perm,
+      shared_h, shared_out, total;
+};
+
+inline size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+Plan make_plan(const moe_config_t* c) {
+  const size_t T = c->T, H = c->H, E = c->E, K = c->K, I = c->I, Is = c->I_shared;
+  const size_t ab = act_bytes(c->dtype);
+  const int bm = c->dtype == MOE_BF16 ? kTcBM : kSimtBM;
+  Plan p;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o += up256(bytes);
+    return at;
+  };
+  p.logits = take(T * E * 4);
+  p.ids = take(T * K * 4);
+  p.w = take(T * K * 4);
+  p.counts = take(E * 4);
+  p.offsets = take((E + 1) * 4);
+  p.perm = take(T * K * 4);
+  p.inv = take(T * K * 4);
+  p.perm_ws = take(permute_ws_words(c->T, c->E) * 4);
+  p.table = take(static_cast<size_t>(max_mtiles(c->T, c->K, c->E, bm)) * sizeof(int4));
+  p.num_mt = take(16);
+  p.x_perm = take(T * K * H * ab);
+  p.h = take(T * K * I * ab);
+  p.out_perm = take(T * K * H * 4);
+  p.shared_h = take(T * Is * ab);
+  p.shared_out = take(Is > 0 ? T * H * 4 : 0);
+  p.total = o;
+  return p;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)                      \
+  do {                                     \
+    moe_status_t st__ = (expr);            \
+    if (st__ != MOE_OK) return st__;       \
+  } while (0)
+
+#define MOE_CUDA(expr) MOE_TRY(cuda_status(expr))
+
+moe_status_t check_device(const DeviceInfo** out) {
+  const DeviceInfo* d = device_info();
+  if (d == nullptr) return MOE_ERR_CUDA;
+  if (!d->supported) return MOE_ERR_UNSUPPORTED;
+  *out = d;
+  return MOE_OK;
+}
+
+bool use_tc_router(const moe_config_t* c) {
+  return c->dtype == MOE_BF16 && c->T >= 256 && c->E >= 32 && c->E % 16 == 0;
+}
+
+// Routing launches (shared by moe_route and moe_layer_forward).
+moe_status_t run_route(const moe_config_t* c, const DeviceInfo* d, const void* x,
+                       const void* w_router, const float* bias, float* logits, int32_t* ids,
+                       float* w, cudaStream_t s) {
+  if (c->T == 0) return MOE_OK;
+  if (x == nullptr) {
+    return cuda_status(launch_topk(logits, nullptr, nullptr, ids, w, c->T, c->E, c->K,
+                                   c->gate_threshold, s));
+  }
+  if (use_tc_router(c)) {
+    GroupedGemm g{};
+    g.mode = kPlain;
+    g.dtype = kBF16;
+    g.A = x;
+    g.rows_alloc = c->T;
+    g.Kd = c->H;
+    g.B = w_router;
+    g.G = 1;
+    g.Nb = c->E;
+    g.N_out = c->E;
+    g.C = logits;
+    g.col_bias = bias;
+    MOE_CUDA(launch_grouped_gemm_tc(g, d->err, d->num_sms, s));
+    return cuda_status(
+        launch_topk(logits, nullptr, nullptr, ids, w, c->T, c->E, c->K, c->gate_threshold, s));
+  }
+  return cuda_status(launch_router_simt_topk(c->dtype, x, w_router, bias, logits, ids, w, c->T,
+                                             c->H, c->E, c->K, c->gate_threshold, s));
+}
+
+// Grouped-GEMM launch descriptions of the two expert GEMMs.  Groups come from `offsets`
+// (tensor-core engine) or from the m-tile table (SIMT engine); with neither, A is one
+// dense group of rows_alloc rows (the shared expert).
+struct Groups {
+  const int32_t* offsets;
+  const int4* table;
+  const int32_t* num_mt;
+  int max_mt;
+  int G;
+};
+
+moe_status_t launch_gemm(const moe_config_t* c, const DeviceInfo* d, const GroupedGemm& g,
+                         cudaStream_t s) {
+  if (c->dtype == MOE_BF16) return cuda_status(launch_grouped_gemm_tc(g, d->err, d->num_sms, s));
+  return cuda_status(launch_grouped_gemm_simt(g, s));
+}
+
+// h = silu(A W_g^T) * (A W_u^T) per group.
+moe_status_t run_gate_up(const moe_config_t* c, const DeviceInfo* d, const void* A,
+                         int rows_alloc, const void* w_gate_up, int I, void* h, const Groups& gr,
+                         cudaStream_t s) {
+  if (rows_alloc == 0) return MOE_OK;
+  GroupedGemm g{};
+  g.mode = kSwiGLU;
+  g.dtype = c->dtype;
+  g.A = A;
+  g.rows_alloc = rows_alloc;
+  g.Kd = c->H;
+  g.B = w_gate_up;
+  g.G = gr.G;
+  g.Nb = 2 * I;
+  g.N_out = I;
+  g.up_offset = I;
+  g.C = h;
+  g.offsets = gr.offsets;
+  g.mtile_table = gr.table;
+  g.num_mtiles = gr.num_mt;
+  g.max_mtiles = gr.max_mt;
+  return launch_gemm(c, d, g, s);
+}
+
+// out = h W_d^T per group.
+moe_status_t run_down(const moe_config_t* c, const DeviceInfo* d, const void* h, int rows_alloc,
+                      const void* w_down, int I, float* out, const Groups& gr, cudaStream_t s) {
+  if (rows_alloc == 0) return MOE_OK;
+  GroupedGemm g{};
+  g.mode = kPlain;
+  g.dtype = c->dtype;
+  g.A = h;
+  g.rows_alloc = rows_alloc;
+  g.Kd = I;
+  g.B = w_down;
+  g.G = gr.G;
+  g.Nb = c->H;
+  g.N_out = c->H;
+  g.C = out;
+  g.offsets = gr.offsets;
+  g.mtile_table = gr.table;
+  g.num_mtiles = gr.num_mt;
+  g.max_mtiles = gr.max_mt;
+  return launch_gemm(c, d, g, s);
+}
+
+// Groups of the routed experts: bf16 reads `offsets` directly; float builds the m-tile
+// table into the workspace first (unless `table_ready`).
+moe_status_t routed_groups(const moe_config_t* c, const int32_t* offsets, void* ws,
+                           const Plan& p, bool table_ready, cudaStream_t s, Groups* out) {
+  Groups gr{};
+  gr.G = c->E;
+  if (c->dtype == MOE_BF16) {
+    gr.offsets = offsets;
+  } else {
+    gr.table = at<int4>(ws, p.table);
+    gr.num_mt = at<int32_t>(ws, p.num_mt);
+    gr.max_mt = max_mtiles(c->T, c->K, c->E, kSimtBM);
+    if (!table_ready)
+      MOE_CUDA(launch_build_mtile_table(offsets, c->E, kSimtBM, const_cast<int4*>(gr.table),
+                                        const_cast<int32_t*>(gr.num_mt), s));
+  }
+  *out = gr;
+  return MOE_OK;
+}
+
+moe_status_t check_ws(const moe_config_t* c, void* ws, size_t ws_bytes, Plan* p) {
+  *p = make_plan(c);
+  if (ws == nullptr || ws_bytes < p->total) return MOE_ERR_WORKSPACE;
+  if (!aligned16(ws)) return MOE_ERR_MISALIGNED;
+  return MOE_OK;
+}
+
+bool any_misaligned(std::initializer_list<const void*> ps) {
+  for (const void* q : ps)
+    if (q != nullptr && !aligned16(q)) return true;
+  return false;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_INTERNAL: return "MOE_ERR_INTERNAL";
+    case MOE_ERR_MISALIGNED: return "MOE_ERR_MISALIGNED";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+const char* moe_version(void) { return "moe_gb300 0.1 sm_103a"; }
+
+moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes) {
+  MOE_TRY(check_config(cfg));
+  if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+  *bytes = make_plan(cfg).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_workspace_views(const moe_config_t* cfg, void* ws, float** logits,
+                                 int32_t** topk_ids, float** topk_w, int32_t** counts,
+                                 int32_t** offsets, int32_t** perm, int32_t** inv, void** x_perm,
+                                 float** out_perm, float** shared_out) {
+  MOE_TRY(check_config(cfg));
+  if (ws == nullptr) return MOE_ERR_WORKSPACE;
+  const Plan p = make_plan(cfg);
+  if (logits) *logits = at<float>(ws, p.logits);
+  if (topk_ids) *topk_ids = at<int32_t>(ws, p.ids);
+  if (topk_w) *topk_w = at<float>(ws, p.w);
+  if (counts) *counts = at<int32_t>(ws, p.counts);
+  if (offsets) *offsets = at<int32_t>(ws, p.offsets);
+  if (perm) *perm = at<int32_t>(ws, p.perm);
+  if (inv) *inv = at<int32_t>(ws, p.inv);
+  if (x_perm) *x_perm = at<void>(ws, p.x_perm);
+  if (out_perm) *out_perm = at<float>(ws, p.out_perm);
+  if (shared_out) *shared_out = cfg->I_shared > 0 ? at<float>(ws, p.shared_out) : nullptr;
+  return MOE_OK;
+}
+
+moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* w_router,
+                       const float* router_bias, float* logits, int32_t* topk_ids, float* topk_w,
+                       moe_stream_t stream) {
+  MOE_TRY(check_config(cfg));
+  if (cfg->T == 0) return MOE_OK;
+  if (logits == nullptr || topk_ids == nullptr || topk_w == nullptr) return MOE_ERR_INVALID_ARG;
+  if (x != nullptr && w_router == nullptr) return MOE_ERR_INVALID_ARG;
+  for (const void* q : std::initializer_list<const void*>{x, w_router, static_cast<const void*>(router_bias),
+                        static_cast<const void*>(logits), static_cast<const void*>(topk_ids),
+                        static_cast<const void*>(topk_w)})
+    if (q != nullptr && !aligned16(q)) return MOE_ERR_MISALIGNED;
+  if (cfg->T == 0) return MOE_OK;
+  const DeviceInfo* d = nullptr;
+  MOE_TRY(check_device(&d));
+  return run_route(cfg, d, x, w_router, router_bias, logits, topk_ids, topk_w,
+                   static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_permute(const moe_config_t* cfg, const void* x, const int32_t* topk_ids,
+                         int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                         void* x_perm, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_config(cfg));
+  if (cfg->T == 0) return MOE_OK;
+  if (x == nullptr || topk_ids == nullptr || counts == nullptr || offsets == nullptr ||
+      perm == nullptr || inv == nullptr || x_perm == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  for (const void* q : std::initializer_list<const void*>{x, static_cast<const void*>(topk_ids), static_cast<const void*>(counts),
+                        static_cast<const void*>(offsets), static_cast<const void*>(perm),
+                        static_cast<const void*>(inv), static_cast<const void*>(x_perm)})
+    if (!aligned16(q)) return MOE_ERR_MISALIGNED;
+  const Plan p = make_plan(cfg);
+  if (ws == nullptr || ws_bytes < p.total) return MOE_ERR_WORKSPACE;
+  if (!aligned16(ws)) return MOE_ERR_MISALIGNED;
+  const DeviceInfo* d = nullptr;
+  MOE_TRY(check_device(&d));
+  return cuda_status(launch_permute(cfg->dtype, x, topk_ids, cfg->T, cfg->H, cfg->E, cfg->K,
+                                    counts, offsets, perm, inv, x_perm, at<int32_t>(ws, p.perm_ws),
+                                    nullptr, nullptr, 0, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_grouped_ffn(const moe_config_t* cfg, const void* x_perm, const int32_t* offsets,
+                             const void* w_gate_up, const void* w_down, float* out_perm, void* ws,
+                             size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_config(cfg));
+  if (cfg->T == 0) return MOE_OK;
+  if (x_perm == nullptr || offsets == nullptr || w_gate_up == nullptr || w_down == nullptr ||
+      out_perm == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (any_misaligned({x_perm, offsets, w_gate_up, w_down, out_perm})) return MOE_ERR_MISALIGNED;
+  Plan p;
+  MOE_TRY(check_ws(cfg, ws, ws_bytes, &p));
+  if (cfg->T == 0) return MOE_OK;
+  const DeviceInfo* d = nullptr;
+  MOE_TRY(check_device(&d));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Groups gr;
+  MOE_TRY(routed_groups(cfg, offsets, ws, p, false, s, &gr));
+  void* h = at<void>(ws, p.h);
+  const int rows = cfg->T * cfg->K;
+  MOE_TRY(run_gate_up(cfg, d, x_perm, rows, w_gate_up, cfg->I, h, gr, s));
+  return run_down(cfg, d, h, rows, w_down, cfg->I, out_perm, gr, s);
+}
+
+moe_status_t moe_expert_gate_up(const moe_config_t* cfg, const void* x_perm,
+                                const int32_t* offsets, const void* w_gate_up, void* h, void* ws,
+                                size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_config(cfg));
+  if (cfg->T == 0) return MOE_OK;
+  if (x_perm == nullptr || offsets == nullptr || w_gate_up == nullptr || h == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (any_misaligned({x_perm, offsets, w_gate_up, h})) return MOE_ERR_MISALIGNED;
+  Plan p;
+  MOE_TRY(check_ws(cfg, ws, ws_bytes, &p));
+  if (cfg->T == 0) return MOE_OK;
+  const DeviceInfo* d = nullptr;
+  MOE_TRY(check_device(&d));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Groups gr;
+  MOE_TRY(routed_groups(cfg, offsets, ws, p, false, s, &gr));
+  return run_gate_up(cfg, d, x_perm, cfg->T * cfg->K, w_gate_up, cfg->I, h, gr, s);
+}
+
+moe_status_t moe_expert_down(const moe_config_t* cfg, const void* h, const int32_t* offsets,
+                             const void* w_down, float* out_perm, void* ws, size_t ws_bytes,
+                             moe_stream_t stream) {
+  MOE_TRY(check_config(cfg));
+  if (cfg->T == 0) return MOE_OK;
+  if (h == nullptr || offsets == nullptr || w_down == nullptr || out_perm == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (any_misaligned({h, offsets, w_down, out_perm})) return MOE_ERR_MISALIGNED;
+  Plan p;
+  MOE_TRY(check_ws(cfg, ws, ws_bytes, &p));
+  if (cfg->T == 0) return MOE_OK;
+  const DeviceInfo* d = nullptr;
+  MOE_TRY(check_device(&d));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Groups gr;
+  MOE_TRY(routed_groups(cfg, offsets, ws, p, false, s, &gr));
+  return run_down(cfg, d, h, cfg->T * cfg->K, w_down, cfg->I, out_perm, gr, s);
+}
+
+moe_status_t moe_combine(const moe_config_t* cfg, const float* out_perm, const int32_t* inv,
+                         const float* topk_w, const float* shared_out, void* y, float* y_f32,
+                         moe_stream_t stream) {
+  MOE_TRY(check_config(cfg));
+  if (cfg->T == 0) return MOE_OK;
+  if (out_perm == nullptr || inv == nullptr || topk_w == nullptr || y == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  for (const void* q : std::initializer_list<const void*>{static_cast<const void*>(out_perm), static_cast<const void*>(inv),
+                        static_cast<const void*>(topk_w), static_cast<const void*>(shared_out), y,
+                        static_cast<const void*>(y_f32)})
+    if (q != nullptr && !aligned16(q)) return MOE_ERR_MISALIGNED;
+  if (cfg->T == 0) return MOE_OK;
+  const DeviceInfo* d = nullptr;
+  MOE_TRY(check_device(&d));
+  return cuda_status(launch_combine(cfg->dtype, out_perm, inv, topk_w, shared_out, y, y_f32,
+                                    cfg->T, cfg->H, cfg->K, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const void* w_router,
+                               const float* router_bias, const void* w_gate_up,
+                               const void* w_down, const void* w_shared_gate_up,
+                               const void* w_shared_down, void* y, float* y_f32, void* ws,
+                               size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_config(cfg));
+  if (cfg->T == 0) return MOE_OK;
+  if (x == nullptr || w_router == nullptr || w_gate_up == nullptr || w_down == nullptr ||
+      y == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  const bool shared = cfg->I_shared > 0;
+  if (shared != (w_shared_gate_up != nullptr) || shared != (w_shared_down != nullptr))
+    return MOE_ERR_INVALID_ARG;
+  for (const void* q : std::initializer_list<const void*>{x, w_router, static_cast<const void*>(router_bias), w_gate_up, w_down,
+                        w_shared_gate_up, w_shared_down, y, static_cast<const void*>(y_f32)})
+    if (q != nullptr && !aligned16(q)) return MOE_ERR_MISALIGNED;
+  const Plan p = make_plan(cfg);
+  if (ws == nullptr || ws_bytes < p.total) return MOE_ERR_WORKSPACE;
+  if (!aligned16(ws)) return MOE_ERR_MISALIGNED;
+  if (cfg->T == 0) return MOE_OK;
+  const DeviceInfo* d = nullptr;
+  MOE_TRY(check_device(&d));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  float* logits = at<float>(ws, p.logits);
+  int32_t* ids = at<int32_t>(ws, p.ids);
+  float* w = at<float>(ws, p.w);
+  int32_t* counts = at<int32_t>(ws, p.counts);
+  int32_t* offsets = at<int32_t>(ws, p.offsets);
+  int32_t* perm = at<int32_t>(ws, p.perm);
+  int32_t* inv = at<int32_t>(ws, p.inv);
+  int4* table = at<int4>(ws, p.table);
+  int32_t* num_mt = at<int32_t>(ws, p.num_mt);
+  void* x_perm = at<void>(ws, p.x_perm);
+  float* out_perm = at<float>(ws, p.out_perm);
+  const bool simt = cfg->dtype == MOE_F32;
+
+  // 1. router scores, top-k, gate drop
+  MOE_TRY(run_route(cfg, d, x, w_router, router_bias, logits, ids, w, s));
+  // 2. dispatch: stable permutation, inverse map, row gather (+ the SIMT m-tile table)
+  MOE_CUDA(launch_permute(cfg->dtype, x, ids, cfg->T, cfg->H, cfg->E, cfg->K, counts, offsets,
+                          perm, inv, x_perm, at<int32_t>(ws, p.perm_ws), simt ? table : nullptr,
+                          simt ? num_mt : nullptr, kSimtBM, s));
+  // 3-4. grouped SwiGLU FFN of the routed experts
+  Groups gr;
+  MOE_TRY(routed_groups(cfg, offsets, ws, p, true, s, &gr));
+  void* h = at<void>(ws, p.h);
+  const int rows = cfg->T * cfg->K;
+  MOE_TRY(run_gate_up(cfg, d, x_perm, rows, w_gate_up, cfg->I, h, gr, s));
+  MOE_TRY(run_down(cfg, d, h, rows, w_down, cfg->I, out_perm, gr, s));
+  // 5. shared expert: the same engine on all T rows of x as one group
+  float* shared_out = nullptr;
+  if (shared) {
+    shared_out = at<float>(ws, p.shared_out);
+    Groups one{};
+    one.G = 1;
+    void* hs = at<void>(ws, p.shared_h);
+    MOE_TRY(run_gate_up(cfg, d, x, cfg->T, w_shared_gate_up, cfg->I_shared, hs, one, s));
+    MOE_TRY(run_down(cfg, d, hs, cfg->T, w_shared_down, cfg->I_shared, shared_out, one, s));
+  }
+  // 6. un-permute and weighted combine
+  return cuda_status(launch_combine(cfg->dtype, out_perm, inv, w, shared_out, y, y_f32, cfg->T,
+                                    cfg->H, cfg->K, s));
+}
+
+moe_status_t moe_sync_check(moe_stream_t stream) {
+  const DeviceInfo* d = device_info();
+  if (d == nullptr) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  unsigned word = 0;
+  if (cudaMemcpy(&word, d->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (word != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpy(d->err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return (word & MOE_DEVERR_TIMEOUT) ? MOE_ERR_TIMEOUT : MOE_ERR_INTERNAL;
+  }
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,94 @@
+// Internal launchers of the MoE layer kernels (host side).  The public C ABI in
+// include/moe.h validates arguments and then calls these.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+enum DType : int { kF32 = 0, kBF16 = 1 };
+
+inline size_t act_bytes(int dtype) { return dtype == kBF16 ? 2 : 4; }
+
+// Rows per m-tile of the tensor-core grouped GEMM and of the SIMT grouped GEMM.
+constexpr int kTcBM = 128;
+constexpr int kSimtBM = 64;
+
+// ------------------------------------------------------------------ routing ----
+// Fused router for small problems: one block per token computes the E logits
+// (x . W_r^T + bias, fp32 accumulation) and one warp takes the top-k.
+cudaError_t launch_router_simt_topk(int dtype, const void* x, const void* w_router,
+                                    const float* bias, float* logits, int32_t* ids, float* w,
+                                    int T, int H, int E, int K, float theta, cudaStream_t s);
+
+// Top-k, softmax over the kept logits and gate drop, one warp per token, from
+// logits already in memory.  If `bias` is non-null it is added first and the
+// biased logits are written back to `logits_out` (which may alias `logits_in`).
+cudaError_t launch_topk(const float* logits_in, const float* bias, float* logits_out,
+                        int32_t* ids, float* w, int T, int E, int K, float theta,
+                        cudaStream_t s);
+
+// ---------------------------------------------------------------- dispatch ----
+// Workspace (int32 words) the permutation needs for T tokens, E experts.
+size_t permute_ws_words(int T, int E);
+// Maximum number of m-tiles of `bm` rows over all groups of T*K rows and E experts.
+inline int max_mtiles(int T, int K, int E, int bm) {
+  return static_cast<int>((static_cast<long long>(T) * K + bm - 1) / bm) + E;
+}
+
+// Stable counting-sort permutation: counts, offsets, perm, inv and the row gather
+// x_perm[r] = x[perm[r]].  If `mtile_table` is non-null the m-tile table of `bm`
+// rows per tile is written as well (entries {expert, row0, row_end, 0}) with its
+// length in *num_mtiles.
+cudaError_t launch_permute(int dtype, const void* x, const int32_t* ids, int T, int H, int E,
+                           int K, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                           void* x_perm, int32_t* ws_words, int4* mtile_table,
+                           int32_t* num_mtiles, int bm, cudaStream_t s);
+
+// The m-tile table of a grouped GEMM from offsets alone.
+cudaError_t launch_build_mtile_table(const int32_t* offsets, int E, int bm, int4* table,
+                                     int32_t* num_mtiles, cudaStream_t s);
+
+// ----------------------------------------------------------------- combine ----
+cudaError_t launch_combine(int dtype, const float* out_perm, const int32_t* inv, const float* w,
+                           const float* shared_out, void* y, float* y_f32, int T, int H, int K,
+                           cudaStream_t s);
+
+// --------------------------------------------------------- grouped GEMMs ----
+// Grouped NT GEMM description shared by the SIMT (float) and the tcgen05 (bf16)
+// engines: for every m-tile (group g, rows row0..row_end-1 of A):
+//   C[row, n] = sum_k A[row, k] * B[g, n, k]                      (mode kPlain)
+//   C[row, n] = silu(sum_k A B[g, n, k]) * (sum_k A B[g, up + n, k])  (mode kSwiGLU)
+// A: [rows_alloc, Kd] row-major; B: [G, Nb, Kd] row-major; C: [rows_alloc, N_out].
+enum GemmMode : int { kPlain = 0, kSwiGLU = 1 };
+
+struct GroupedGemm {
+  int mode;
+  int dtype;                 // act type of A and B; C is act for kSwiGLU, float for kPlain
+  const void* A;
+  int rows_alloc;            // rows of A/C that exist in memory
+  int Kd;                    // reduction length
+  const void* B;
+  int G;                     // groups in B
+  int Nb;                    // rows of one group of B
+  int N_out;                 // output columns
+  int up_offset;             // kSwiGLU: first row of the up block in a group of B
+  void* C;
+  const float* col_bias;     // kPlain only: added per output column, or null
+  // Groups: device row offsets [G+1] of the groups in A (tensor-core engine), or
+  // null for a single group 0 covering rows 0..rows_alloc-1.
+  const int32_t* offsets;
+  // SIMT engine: a device m-tile table {group, row0, row_end, 0} with a device count,
+  // or null for a single group.
+  const int4* mtile_table;
+  const int32_t* num_mtiles;
+  int max_mtiles;            // upper bound of the device count (grid sizing)
+};
+
+cudaError_t launch_grouped_gemm_simt(const GroupedGemm& g, cudaStream_t s);
+cudaError_t launch_grouped_gemm_tc(const GroupedGemm& g, unsigned* err, int num_sms,
+                                   cudaStream_t s);
+
+}  // namespace moe

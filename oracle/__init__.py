@@ -6,6 +6,8 @@ reference legs may import this package.  It shares no code with the CUDA library
 
 from .moe_oracle import (  # noqa: F401
     combine,
+    expert_down,
+    expert_gate_up,
     gate_drop,
     grouped_ffn,
     moe_layer,

@@ -55,6 +55,8 @@ __all__ = [
     "permute",
     "silu",
     "swiglu_ffn",
+    "expert_gate_up",
+    "expert_down",
     "grouped_ffn",
     "combine",
     "moe_layer",
@@ -183,14 +185,26 @@ def swiglu_ffn(x_rows, w_gate_up, w_down):
     x_rows: [R, H]; w_gate_up: [2I, H] with rows 0..I-1 = W_g and I..2I-1 = W_u;
     w_down: [H, I].  Returns o: [R, H] float64 (h is not rounded).
     """
+    return expert_down(expert_gate_up(x_rows, w_gate_up), w_down)
+
+
+def expert_gate_up(x_rows, w_gate_up):
+    """First half of the expert FFN: h = silu(x W_g^T) * (x W_u^T), float64.
+
+    x_rows: [R, H]; w_gate_up: [2I, H] (rows 0..I-1 = W_g, I..2I-1 = W_u).  Returns [R, I].
+    """
     x = np.asarray(x_rows, dtype=np.float64)
     wgu = np.asarray(w_gate_up, dtype=np.float64)
-    wd = np.asarray(w_down, dtype=np.float64)
     I = wgu.shape[0] // 2
-    g = x @ wgu[:I].T
-    u = x @ wgu[I:].T
-    h = silu(g) * u
-    return h @ wd.T
+    return silu(x @ wgu[:I].T) * (x @ wgu[I:].T)
+
+
+def expert_down(h_rows, w_down):
+    """Second half of the expert FFN, the output projection: o = h W_d^T, float64.
+
+    h_rows: [R, I]; w_down: [H, I].  Returns [R, H].
+    """
+    return np.asarray(h_rows, dtype=np.float64) @ np.asarray(w_down, dtype=np.float64).T
 
 
 def grouped_ffn(x_perm, offsets, w_gate_up, w_down):

@@ -1,0 +1,225 @@
+"""GPU parity of the whole layer (moe_layer_forward) against the CPU oracle.
+
+* Small layers (all oracle stages in full) covering every feature: float32 and bf16,
+  tensor-core and SIMT routers, ragged and empty groups, gate drop, shared expert.
+* The workloads at their full sizes, in the launch configuration the benchmark times:
+  routing of every token, the permutation's invariants at full size, and the output
+  of a sample of tokens (including tokens in the largest and the smallest non-empty
+  groups) computed token by token by the oracle.
+* Determinism (two runs are bitwise equal) and edge cases (T=0, T=1, K=E, one expert
+  takes every token, forced-empty experts).
+
+Output tolerance (bf16 layers): max-abs 2e-2 and relative L2 1e-2 on the fp32 sum
+y_f32, plus: the bf16 output equals the round-to-nearest-even of y_f32 bit for bit.
+Float32 layers: max-abs and relative L2 1e-3.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    import mixture_experts_layer_04_gb300 as m
+    from mixture_experts_layer_04_gb300 import build
+
+    build.build()
+    m.load()
+    return m
+
+
+def _tol(shape):
+    if shape.dtype == "f32":
+        return dict(max_abs=H.Y32_MAX_ABS, rel_l2=H.Y32_REL_L2)
+    return dict(max_abs=H.Y_MAX_ABS, rel_l2=H.Y_REL_L2)
+
+
+def _bias_np(inp):
+    return inp["router_bias"].cpu().numpy() if inp["router_bias"] is not None else None
+
+
+def _check_dispatch_properties(r, T, K, E):
+    """Invariants of the permutation that hold at any size."""
+    ids, counts, offsets, perm, inv = r["ids"], r["counts"], r["offsets"], r["perm"], r["inv"]
+    kept = ids >= 0
+    M = int(kept.sum())
+    assert offsets[0] == 0 and offsets[-1] == M and (np.diff(offsets) == counts).all()
+    np.testing.assert_array_equal(counts, np.bincount(ids[kept], minlength=E))
+    assert (inv[~kept] == -1).all()
+    rows = inv[kept]
+    assert np.array_equal(np.sort(rows), np.arange(M))
+    tok = np.nonzero(kept)[0]
+    np.testing.assert_array_equal(perm[rows], tok)
+    exp_of_row = np.repeat(np.arange(E), counts)
+    np.testing.assert_array_equal(exp_of_row[rows], ids[kept])
+    for e in range(E):
+        g = perm[offsets[e]:offsets[e + 1]]
+        assert (np.diff(g) > 0).all()
+
+
+SMALL = [
+    synch for synch in [
+        synth.WORKLOADS["toy"],
+        synth.MoEShape("mixtral_small", T=512, H=512, E=8, K=2, I=1024),
+        synth.MoEShape("qwen_small", T=1024, H=256, E=128, K=8, I=128, bias="normal"),
+        synth.MoEShape("deepseek_small", T=600, H=512, E=64, K=8, I=256, I_shared=256, theta=0.05,
+                       bias="zipf"),
+        synth.MoEShape("ragged", T=333, H=192, E=24, K=3, I=192, I_shared=64, theta=0.1,
+                       bias="normal", seed=4),
+        synth.MoEShape("f32_shared", T=100, H=128, E=6, K=2, I=64, I_shared=128, theta=0.2,
+                       dtype="f32", bias="normal", seed=2),
+    ]
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: s.name)
+def test_layer_small_full_oracle(moe, shape):
+    inp = synth.make_inputs(shape, device="cuda")
+    run = H.LayerRun(moe, shape, inp)
+    run.run()
+    moe.sync_check()
+    r = run.routing()
+    f = H.f64
+    sh = (f(inp["w_shared_gate_up"]), f(inp["w_shared_down"])) if shape.I_shared else (None, None)
+    ref = oracle.moe_layer(f(inp["x"]), f(inp["w_router"]), f(inp["w_gate_up"]), f(inp["w_down"]),
+                           shape.K, shape.theta, _bias_np(inp), *sh)
+    assert np.abs(r["logits"] - ref["logits"]).max() <= 1e-4 * max(1, np.abs(ref["logits"]).max())
+    amb = H.compare_routing(ref["logits"], r["ids"], r["w"], ref["ids"], ref["w"], shape.K, shape.theta)
+    _check_dispatch_properties(r, shape.T, shape.K, shape.E)
+    if not amb.any():
+        np.testing.assert_array_equal(r["counts"], ref["counts"])
+        np.testing.assert_array_equal(r["offsets"], ref["offsets"])
+        np.testing.assert_array_equal(r["perm"][:len(ref["perm"])], ref["perm"])
+        np.testing.assert_array_equal(r["inv"], ref["inv"])
+    ok = ~amb
+    y32 = run.y32.double().cpu().numpy()
+    H.assert_close_y(y32[ok], ref["y"][ok], **_tol(shape))
+    assert torch.equal(run.y, run.y32.to(shape.torch_dtype))
+
+
+def _sample_tokens(r, T, n, seed=0):
+    """n tokens: random ones plus tokens routed to the largest and smallest groups."""
+    rng = np.random.default_rng(seed)
+    counts, ids = r["counts"], r["ids"]
+    nz = np.nonzero(counts)[0]
+    big, small = nz[np.argmax(counts[nz])], nz[np.argmin(counts[nz])]
+    pick = set(rng.choice(T, size=min(T, n), replace=False).tolist())
+    for e in (big, small):
+        hit = np.nonzero((ids == e).any(axis=1))[0]
+        pick.update(hit[:2].tolist())
+    return np.array(sorted(pick))
+
+
+FULL = [
+    ("mixtral", None, 48), ("qwen_prefill", None, 48), ("qwen_decode", 1, 1),
+    ("qwen_decode", 8, 8), ("qwen_decode", 32, 32), ("qwen_decode", 64, 64), ("deepseek", None, 24),
+]
+
+
+@pytest.mark.parametrize("name,T,nsample", FULL, ids=[f"{n}-{t}" for n, t, _ in FULL])
+def test_layer_full_size_sampled(moe, name, T, nsample):
+    shape = synth.WORKLOADS[name]
+    inp = synth.make_inputs(shape, device="cuda", T=T)
+    run = H.LayerRun(moe, shape, inp)
+    run.run()
+    moe.sync_check()
+    Tn = run.T
+    r = run.routing()
+    bias = _bias_np(inp)
+    x64 = H.f64(inp["x"])
+    L_ref = oracle.router_logits(x64, H.f64(inp["w_router"]), bias)
+    assert np.abs(r["logits"] - L_ref).max() <= 1e-4 * max(1, np.abs(L_ref).max())
+    L32 = L_ref.astype(np.float32)
+    ids_ref, w_ref = oracle.route(L32, shape.K, shape.theta)
+    amb = H.compare_routing(L32, r["ids"], r["w"], ids_ref, w_ref, shape.K, shape.theta)
+    assert amb.mean() < 0.02
+    _check_dispatch_properties(r, Tn, shape.K, shape.E)
+    if not amb.any():
+        _, offsets_ref, _, _ = oracle.permute(ids_ref, shape.E)
+        np.testing.assert_array_equal(r["offsets"], offsets_ref)
+    toks = _sample_tokens(r, Tn, nsample)
+    toks = toks[~amb[toks]]
+    sh = {}
+    if shape.I_shared:
+        sh = dict(w_shared_gate_up=H.f64(inp["w_shared_gate_up"]), w_shared_down=H.f64(inp["w_shared_down"]))
+    ref = oracle.moe_layer_tokens(x64[toks], H.f64(inp["w_router"]), H.ExpertSlices(inp["w_gate_up"]),
+                                  H.ExpertSlices(inp["w_down"]), shape.K, shape.theta, bias, **sh)
+    np.testing.assert_array_equal(ref["ids"], r["ids"][toks])
+    y32 = run.y32.double().cpu().numpy()[toks]
+    H.assert_close_y(y32, ref["y"], **_tol(shape))
+    assert torch.equal(run.y, run.y32.to(shape.torch_dtype))
+
+
+def test_deterministic(moe):
+    shape = synth.MoEShape("det", T=2048, H=512, E=64, K=8, I=256, I_shared=128, theta=0.05,
+                           bias="zipf")
+    inp = synth.make_inputs(shape, device="cuda")
+    a = H.LayerRun(moe, shape, inp)
+    b = H.LayerRun(moe, shape, inp)
+    a.run()
+    b.run()
+    a.run()
+    torch.cuda.synchronize()
+    assert torch.equal(a.y, b.y) and torch.equal(a.y32, b.y32)
+
+
+@pytest.mark.parametrize("case", ["T0", "T1", "K_eq_E", "one_expert", "empty_experts"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_edge_cases(moe, case, dtype):
+    base = dict(T=300, H=128, E=8, K=2, I=128, dtype=dtype, seed=8)
+    if case == "T0":
+        base["T"] = 0
+    elif case == "T1":
+        base["T"] = 1
+    elif case == "K_eq_E":
+        base.update(E=4, K=4)
+    shape = synth.MoEShape(case, **base)
+    inp = synth.make_inputs(shape, device="cuda")
+    if case == "one_expert":
+        inp["router_bias"] = torch.full((shape.E,), -1e4, device="cuda")
+        inp["router_bias"][5] = 0.0
+        inp["router_bias"][2] = 0.0
+    elif case == "empty_experts":
+        inp["router_bias"] = torch.zeros(shape.E, device="cuda")
+        inp["router_bias"][1::2] = -1e4
+    run = H.LayerRun(moe, shape, inp)
+    run.run()
+    moe.sync_check()
+    if shape.T == 0:
+        return
+    r = run.routing()
+    f = H.f64
+    ref = oracle.moe_layer(f(inp["x"]), f(inp["w_router"]), f(inp["w_gate_up"]), f(inp["w_down"]),
+                           shape.K, shape.theta, _bias_np(inp))
+    amb = H.compare_routing(ref["logits"], r["ids"], r["w"], ref["ids"], ref["w"], shape.K, shape.theta)
+    if case in ("one_expert", "empty_experts"):
+        assert not amb.any()
+        np.testing.assert_array_equal(r["counts"], ref["counts"])
+        if case == "empty_experts":
+            assert (r["counts"][1::2] == 0).all()
+        else:
+            assert set(np.nonzero(r["counts"])[0]) == {2, 5}
+    H.assert_close_y(run.y32.double().cpu().numpy()[~amb], ref["y"][~amb], **_tol(shape))
+
+
+def test_streams_and_sync_check(moe):
+    shape = synth.MoEShape("s", T=512, H=256, E=16, K=4, I=128, bias="normal")
+    inp = synth.make_inputs(shape, device="cuda")
+    s = torch.cuda.Stream()
+    a = H.LayerRun(moe, shape, inp)
+    with torch.cuda.stream(s):
+        a.run(stream=s)
+    moe.sync_check(s)
+    b = H.LayerRun(moe, shape, inp)
+    b.run()
+    torch.cuda.synchronize()
+    assert torch.equal(a.y, b.y)

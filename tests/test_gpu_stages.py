@@ -1,0 +1,244 @@
+"""GPU parity of every stage of the MoE layer against the CPU oracle, through the C ABI.
+
+Each stage is fed the same inputs as the oracle stage (seeded, synthetic), at sizes the
+oracle finishes in seconds that still span several tiles and a ragged tail:
+  * routing from given float32 logits: ids bit-exact (ties to the lower expert), gates
+    to 1e-5; tokens whose gate lies within rounding of the drop threshold are only
+    checked for validity;
+  * router logits (tensor-core and SIMT paths): within fp32 accumulation error, ids
+    bit-exact on tokens without a near-tie;
+  * permutation: counts, offsets, perm, inv bit-exact, x_perm rows bitwise copies, rows
+    past the kept count untouched;
+  * gate/up + SwiGLU, down projection, and both: within the stated tolerances, rows
+    of neighbouring experts and padding never leak into a group's output;
+  * combine: fp32 sum within 1e-5, the bf16 output is the RNE rounding of it.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    import mixture_experts_layer_04_gb300 as m
+    from mixture_experts_layer_04_gb300 import build
+
+    build.build()
+    m.load()
+    return m
+
+
+def _cfg(moe, T, H_, E, K, I=64, Is=0, theta=0.0, dtype="bf16"):
+    return moe.MoEConfig.make(T, H_, E, K, I, Is, theta, moe.BF16 if dtype == "bf16" else moe.F32)
+
+
+def _logits(T, E, seed, ties):
+    L = synth.random_logits(T, E, seed=seed, scale=1.5)
+    if ties:
+        L[::3] = torch.round(L[::3] * 2) / 2     # exact ties in every third token
+        L[1::7] = 0.25                           # all-equal tokens
+    return L
+
+
+ROUTE_CASES = [
+    (1, 4, 1, 0.0), (37, 8, 2, 0.0), (300, 128, 8, 0.0), (1000, 256, 8, 0.05),
+    (513, 1024, 16, 0.02), (64, 16, 16, 0.0), (200, 64, 4, 0.2), (129, 33, 3, 0.1),
+]
+
+
+@pytest.mark.parametrize("T,E,K,theta", ROUTE_CASES)
+@pytest.mark.parametrize("ties", [False, True])
+def test_route_from_logits_bit_exact(moe, T, E, K, theta, ties):
+    L = _logits(T, E, seed=T + E, ties=ties)
+    c = _cfg(moe, T, 64, E, K, theta=theta)
+    Lg = L.cuda()
+    ids = torch.full((T, K), -9, dtype=torch.int32, device="cuda")
+    w = torch.full((T, K), -9.0, dtype=torch.float32, device="cuda")
+    moe.route(c, None, None, None, Lg, ids, w)
+    torch.cuda.synchronize()
+    ids_ref, w_ref = oracle.route(L.numpy(), K, theta)
+    amb = H.compare_routing(L.numpy(), ids.cpu().numpy(), w.cpu().numpy(), ids_ref, w_ref, K,
+                            theta, margin=None)
+    assert amb.mean() < 0.01
+    assert torch.equal(Lg.cpu(), L)              # logits are an input here: untouched
+
+
+ROUTER_CASES = [
+    # T, H, E, dtype, bias   (bf16 with T >= 256 and E % 16 == 0 uses the tensor cores)
+    (1024, 512, 128, "bf16", "normal"),
+    (257, 256, 256, "bf16", "zipf"),
+    (300, 1024, 8, "bf16", "none"),
+    (64, 2048, 128, "bf16", "normal"),
+    (256, 512, 8, "f32", "none"),
+    (3, 192, 40, "f32", "normal"),
+]
+
+
+@pytest.mark.parametrize("T,H_,E,dtype,bias", ROUTER_CASES)
+def test_router_logits_and_selection(moe, T, H_, E, dtype, bias):
+    K = min(8, E)
+    shape = synth.MoEShape("r", T=T, H=H_, E=E, K=K, I=64, dtype=dtype, bias=bias, seed=11)
+    inp = synth.make_inputs(shape, device="cuda", weights=False)
+    c = _cfg(moe, T, H_, E, K, dtype=dtype)
+    logits = torch.empty(T, E, dtype=torch.float32, device="cuda")
+    ids = torch.empty(T, K, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, K, dtype=torch.float32, device="cuda")
+    moe.route(c, inp["x"], inp["w_router"], inp["router_bias"], logits, ids, w)
+    torch.cuda.synchronize()
+    b = inp["router_bias"].cpu().numpy() if inp["router_bias"] is not None else None
+    L_ref = oracle.router_logits(H.f64(inp["x"]), H.f64(inp["w_router"]), b)
+    got = logits.double().cpu().numpy()
+    assert np.abs(got - L_ref).max() <= 1e-4 * max(1.0, np.abs(L_ref).max())
+    L32 = L_ref.astype(np.float32)
+    ids_ref, w_ref = oracle.route(L32, K, 0.0)
+    amb = H.compare_routing(L32, ids.cpu().numpy(), w.cpu().numpy(), ids_ref, w_ref, K, 0.0)
+    assert amb.mean() < 0.02
+
+
+PERMUTE_CASES = [
+    # T, E, K, theta, H, skew
+    (1, 4, 2, 0.0, 64, "none"), (255, 8, 2, 0.0, 128, "none"), (257, 8, 2, 0.0, 128, "none"),
+    (1000, 128, 8, 0.05, 64, "normal"), (4100, 256, 8, 0.05, 64, "zipf"),
+    (700, 1024, 16, 0.02, 64, "normal"), (300, 16, 16, 0.0, 64, "none"),
+    (513, 32, 1, 0.0, 64, "one"), (999, 64, 4, 0.1, 64, "empties"),
+]
+
+
+def _skewed_ids(T, E, K, theta, skew, seed):
+    L = synth.random_logits(T, E, seed=seed)
+    if skew == "normal":
+        L = L + torch.randn(E, generator=torch.Generator().manual_seed(seed)) * 1.0
+    elif skew == "zipf":
+        r = torch.randperm(E, generator=torch.Generator().manual_seed(seed)).double() + 1
+        L = L + (-1.1 * torch.log(r)).float()
+    elif skew == "one":
+        L[:, E // 2] += 50.0
+    elif skew == "empties":
+        L[:, ::3] -= 1e4
+    return oracle.route(L.numpy(), K, theta)
+
+
+@pytest.mark.parametrize("T,E,K,theta,H_,skew", PERMUTE_CASES)
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_permute_bit_exact(moe, T, E, K, theta, H_, skew, dtype):
+    ids_ref, _ = _skewed_ids(T, E, K, theta, skew, seed=T * 7 + E)
+    counts_r, offsets_r, perm_r, inv_r = oracle.permute(ids_ref, E)
+    M = int(offsets_r[-1])
+    c = _cfg(moe, T, H_, E, K, theta=theta, dtype=dtype)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    x = torch.randn(T, H_, generator=torch.Generator().manual_seed(5)).to(tdt).cuda()
+    ids = torch.from_numpy(ids_ref).cuda()
+    counts = torch.full((E,), -7, dtype=torch.int32, device="cuda")
+    offsets = torch.full((E + 1,), -7, dtype=torch.int32, device="cuda")
+    perm = torch.full((T * K,), -7, dtype=torch.int32, device="cuda")
+    inv = torch.full((T * K,), -7, dtype=torch.int32, device="cuda")
+    x_perm = torch.full((T * K, H_), 3.0, dtype=tdt, device="cuda")
+    ws = torch.empty(moe.workspace_size(c), dtype=torch.uint8, device="cuda")
+    moe.permute(c, x, ids, counts, offsets, perm, inv, x_perm, ws)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(counts.cpu().numpy(), counts_r)
+    np.testing.assert_array_equal(offsets.cpu().numpy(), offsets_r)
+    np.testing.assert_array_equal(perm[:M].cpu().numpy(), perm_r)
+    assert (perm[M:] == -7).all()
+    np.testing.assert_array_equal(inv.view(T, K).cpu().numpy(), inv_r)
+    assert torch.equal(x_perm[:M].cpu(), x.cpu()[torch.from_numpy(perm_r).long()])
+    assert (x_perm[M:] == 3.0).all()
+
+
+FFN_CASES = [
+    # T, H, E, K, I, dtype, skew
+    (300, 256, 8, 2, 128, "bf16", "none"),
+    (1000, 512, 64, 4, 192, "bf16", "normal"),
+    (129, 320, 16, 8, 256, "bf16", "empties"),
+    (700, 256, 4, 1, 128, "bf16", "one"),
+    (256, 512, 8, 2, 1024, "f32", "none"),
+    (77, 128, 4, 3, 64, "f32", "normal"),
+]
+
+
+def _ffn_inputs(T, H_, E, K, I, dtype, skew, seed=1):
+    ids, _ = _skewed_ids(T, E, K, 0.0, skew, seed=seed + T)
+    counts, offsets, perm, inv = oracle.permute(ids, E)
+    shape = synth.MoEShape("f", T=T, H=H_, E=E, K=K, I=I, dtype=dtype, seed=seed)
+    inp = synth.make_inputs(shape, device="cuda")
+    tdt = shape.torch_dtype
+    M = int(offsets[-1])
+    x_perm = torch.full((T * K, H_), float("nan"), dtype=tdt, device="cuda")  # padding = NaN
+    x_perm[:M] = inp["x"][torch.from_numpy(perm).long().cuda()]
+    return shape, inp, offsets, x_perm, M
+
+
+@pytest.mark.parametrize("T,H_,E,K,I,dtype,skew", FFN_CASES)
+def test_grouped_ffn_stages(moe, T, H_, E, K, I, dtype, skew):
+    shape, inp, offsets, x_perm, M = _ffn_inputs(T, H_, E, K, I, dtype, skew)
+    c = _cfg(moe, T, H_, E, K, I=I, dtype=dtype)
+    tdt = shape.torch_dtype
+    off = torch.from_numpy(offsets).cuda()
+    ws = torch.empty(moe.workspace_size(c), dtype=torch.uint8, device="cuda")
+    h = torch.full((T * K, I), -5.0, dtype=tdt, device="cuda")
+    moe.expert_gate_up(c, x_perm, off, inp["w_gate_up"], h, ws)
+    out = torch.full((T * K, H_), -5.0, dtype=torch.float32, device="cuda")
+    moe.expert_down(c, h, off, inp["w_down"], out, ws)
+    out2 = torch.full((T * K, H_), -5.0, dtype=torch.float32, device="cuda")
+    moe.grouped_ffn(c, x_perm, off, inp["w_gate_up"], inp["w_down"], out2, ws)
+    torch.cuda.synchronize()
+    assert (h[M:] == -5.0).all() and (out[M:] == -5.0).all() and (out2[M:] == -5.0).all()
+    xp = H.f64(x_perm[:M])
+    h_gpu = H.f64(h[:M])
+    o_gpu = out[:M].double().cpu().numpy()
+    h_ref = np.zeros((M, I))
+    o_of_hgpu = np.zeros((M, H_))
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 > r0:
+            h_ref[r0:r1] = oracle.expert_gate_up(xp[r0:r1], H.f64(inp["w_gate_up"][e]))
+            o_of_hgpu[r0:r1] = oracle.expert_down(h_gpu[r0:r1], H.f64(inp["w_down"][e]))
+    if dtype == "bf16":
+        # h is rounded once to bf16: half an ulp (2^-9 relative) plus fp32 accumulation
+        assert (np.abs(h_gpu - h_ref) <= 2.0 ** -8 * np.abs(h_ref) + 1e-4).all()
+        H.assert_close_y(o_gpu, o_of_hgpu, max_abs=1e-3, rel_l2=1e-5, what="down")
+    else:
+        H.assert_close_y(h_gpu, h_ref, max_abs=1e-4, rel_l2=1e-5, what="gate_up")
+        H.assert_close_y(o_gpu, o_of_hgpu, max_abs=1e-4, rel_l2=1e-5, what="down")
+    # the fused call equals the two stages, and the whole FFN matches the oracle
+    assert torch.equal(out2[:M], out[:M])
+    o_ref = oracle.grouped_ffn(xp, offsets, H.ExpertSlices(inp["w_gate_up"]),
+                               H.ExpertSlices(inp["w_down"]))
+    if dtype == "bf16":
+        H.assert_close_y(o_gpu, o_ref[:M], what="grouped_ffn")
+    else:
+        H.assert_close_y(o_gpu, o_ref[:M], max_abs=H.Y32_MAX_ABS, rel_l2=H.Y32_REL_L2,
+                         what="grouped_ffn")
+
+
+@pytest.mark.parametrize("T,H_,E,K,shared,dtype", [
+    (1, 64, 4, 2, False, "bf16"), (300, 256, 8, 2, True, "bf16"), (1000, 512, 128, 8, False, "bf16"),
+    (257, 128, 16, 16, True, "f32"), (64, 7168, 256, 8, True, "bf16"),
+])
+def test_combine(moe, T, H_, E, K, shared, dtype):
+    ids, w = _skewed_ids(T, E, K, 0.05, "normal", seed=9)
+    _, offsets, perm, inv = oracle.permute(ids, E)
+    M = int(offsets[-1])
+    g = torch.Generator().manual_seed(3)
+    out_perm = torch.randn(T * K, H_, generator=g)
+    s = torch.randn(T, H_, generator=g) if shared else None
+    c = _cfg(moe, T, H_, E, K, theta=0.05, dtype=dtype)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    y = torch.empty(T, H_, dtype=tdt, device="cuda")
+    y32 = torch.empty(T, H_, dtype=torch.float32, device="cuda")
+    moe.combine(c, out_perm.cuda(), torch.from_numpy(inv).cuda(), torch.from_numpy(w.astype(np.float32)).cuda(),
+                s.cuda() if shared else None, y, y32)
+    torch.cuda.synchronize()
+    ref = oracle.combine(out_perm.double().numpy()[:M], inv, w.astype(np.float32),
+                         s.double().numpy() if shared else None)
+    H.assert_close_y(y32.double().cpu().numpy(), ref, max_abs=1e-5, rel_l2=1e-6, what="combine")
+    assert torch.equal(y, y32.to(tdt))
