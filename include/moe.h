@@ -117,6 +117,29 @@ moe_status_t moe_permute(const moe_config_t* cfg, const void* x, const int32_t* 
                          int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
                          void* x_perm, void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* Largest scratch (int32 words) moe_permute_noalloc can use: it needs
+ * ceil(T/256) * E words, so E = 128 allows T <= 524288 and E = 1024 allows T <= 65536. */
+#define MOE_PERMUTE_NOALLOC_MAX_WORDS 262144
+
+/* moe_permute without a workspace, for callers that cannot allocate device memory (an
+ * inference server that sizes all its device pools once at start-up and allows no
+ * allocation later, a plug-in host that passes a kernel only its inputs and outputs).
+ * No counterpart on the pages: it is a deployment variant of moe_permute.
+ * Same arguments, outputs and results as moe_permute, minus ws/ws_bytes.  The scratch of
+ * the counting sort comes from a fixed 1 MiB array inside the library
+ * (MOE_PERMUTE_NOALLOC_MAX_WORDS int32 words), held on every GPU that loads the library
+ * until the process exits.  It allocates and frees nothing.
+ *  - A problem that needs more than MOE_PERMUTE_NOALLOC_MAX_WORDS words of scratch is
+ *    rejected with MOE_ERR_WORKSPACE before anything is launched.
+ *  - The first call on a device looks up the array's device address on that device
+ *    (the device must be current); make that first call before any stream capture.
+ *  - Every call on a device shares the one array and leaves its contents behind; calls
+ *    that can overlap on the GPU (other streams, other host threads) race on it, so the
+ *    caller must serialise them.  No part of the array needs to start at zero. */
+moe_status_t moe_permute_noalloc(const moe_config_t* cfg, const void* x, const int32_t* topk_ids,
+                                 int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                                 void* x_perm, moe_stream_t stream);
+
 /* Grouped expert FFN over ragged row groups (one launch per GEMM for all experts).
  * Defined by: page section "单机MoE执行流水线" (a grouped GEMM runs several experts'
  * matrices of different row counts in one launch, then each expert applies its

@@ -17,7 +17,7 @@ from typing import Optional
 
 __all__ = [
     "MoEConfig", "MoEError", "F32", "BF16", "library_path", "load", "workspace_size",
-    "route", "permute", "grouped_ffn", "expert_gate_up", "expert_down", "combine", "layer_forward", "workspace_views",
+    "route", "permute", "permute_noalloc", "grouped_ffn", "expert_gate_up", "expert_down", "combine", "layer_forward", "workspace_views",
     "sync_check", "status_string", "version",
 ]
 
@@ -66,6 +66,7 @@ _SIGS = {
     "moe_workspace_size": [_CFG, ctypes.POINTER(ctypes.c_size_t)],
     "moe_route": [_CFG, _P, _P, _P, _P, _P, _P, _P],
     "moe_permute": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+    "moe_permute_noalloc": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P],
     "moe_grouped_ffn": [_CFG, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "moe_expert_gate_up": [_CFG, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "moe_expert_down": [_CFG, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
@@ -143,6 +144,15 @@ def permute(cfg, x, topk_ids, counts, offsets, perm, inv, x_perm, ws, ws_bytes=N
     _check(load().moe_permute(ctypes.byref(cfg), _ptr(x), _ptr(topk_ids), _ptr(counts),
                               _ptr(offsets), _ptr(perm), _ptr(inv), _ptr(x_perm), _ptr(ws), nb,
                               _stream(stream)), "moe_permute")
+
+
+def permute_noalloc(cfg, x, topk_ids, counts, offsets, perm, inv, x_perm, stream=None):
+    """moe_permute for callers that cannot allocate: no workspace; the library's fixed
+    scratch array is used instead (shared by all calls on a device, so overlapping calls
+    must be serialised by the caller)."""
+    _check(load().moe_permute_noalloc(ctypes.byref(cfg), _ptr(x), _ptr(topk_ids), _ptr(counts),
+                                      _ptr(offsets), _ptr(perm), _ptr(inv), _ptr(x_perm),
+                                      _stream(stream)), "moe_permute_noalloc")
 
 
 def grouped_ffn(cfg, x_perm, offsets, w_gate_up, w_down, out_perm, ws, ws_bytes=None, stream=None):
