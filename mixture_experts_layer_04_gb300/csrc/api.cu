@@ -156,8 +156,8 @@ moe_status_t run_route(const moe_config_t* c, const DeviceInfo* d, const void* x
     return cuda_status(
         launch_topk(logits, nullptr, nullptr, ids, w, c->T, c->E, c->K, c->gate_threshold, s));
   }
-  return cuda_status(launch_router_simt_topk(c->dtype, x, w_router, bias, logits, ids, w, c->T,
-                                             c->H, c->E, c->K, c->gate_threshold, s));
+  return cuda_status(launch_router_simt(c->dtype, x, w_router, bias, logits, ids, w, c->T, c->H,
+                                        c->E, c->K, c->gate_threshold, s));
 }
 
 // Grouped-GEMM launch descriptions of the two expert GEMMs.  Groups come from `offsets`
@@ -171,10 +171,18 @@ struct Groups {
   int G;
 };
 
-moe_status_t launch_gemm(const moe_config_t* c, const DeviceInfo* d, const GroupedGemm& g,
+// Decode-sized batches: with at most kSwapMaxTokens tokens no group can have more rows
+// than that, so the tensor-core GEMMs put the weights on the 128-row side of the MMA.
+constexpr int kSwapMaxTokens = 128;
+
+moe_status_t launch_gemm(const moe_config_t* c, const DeviceInfo* d, const GroupedGemm& g0,
                          cudaStream_t s) {
-  if (c->dtype == MOE_BF16) return cuda_status(launch_grouped_gemm_tc(g, d->err, d->num_sms, s));
-  return cuda_status(launch_grouped_gemm_simt(g, s));
+  if (c->dtype == MOE_BF16) {
+    GroupedGemm g = g0;
+    g.swap_tokens = c->T <= kSwapMaxTokens ? c->T : 0;
+    return cuda_status(launch_grouped_gemm_tc(g, d->err, d->num_sms, s));
+  }
+  return cuda_status(launch_grouped_gemm_simt(g0, s));
 }
 
 // h = silu(A W_g^T) * (A W_u^T) per group.

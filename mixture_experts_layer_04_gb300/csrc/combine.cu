@@ -34,6 +34,8 @@ __global__ void __launch_bounds__(kCombineThreads)
                    TOut* __restrict__ y, float* __restrict__ y_f32, int H, int K) {
   __shared__ int rows[kMaxK];
   __shared__ float gates[kMaxK];
+  grid_dep_wait();
+  grid_dep_trigger();
   const int t = blockIdx.x;
   if (threadIdx.x < K) {
     rows[threadIdx.x] = inv[static_cast<size_t>(t) * K + threadIdx.x];
@@ -74,12 +76,10 @@ cudaError_t launch_combine(int dtype, const float* out_perm, const int32_t* inv,
                            cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   if (dtype == kBF16)
-    combine_kernel<__nv_bfloat16><<<T, kCombineThreads, 0, s>>>(
-        out_perm, inv, w, shared_out, static_cast<__nv_bfloat16*>(y), y_f32, H, K);
-  else
-    combine_kernel<float><<<T, kCombineThreads, 0, s>>>(out_perm, inv, w, shared_out,
-                                                        static_cast<float*>(y), y_f32, H, K);
-  return cudaGetLastError();
+    return launch_pdl(combine_kernel<__nv_bfloat16>, dim3(T), dim3(kCombineThreads), 0, s,
+                      out_perm, inv, w, shared_out, static_cast<__nv_bfloat16*>(y), y_f32, H, K);
+  return launch_pdl(combine_kernel<float>, dim3(T), dim3(kCombineThreads), 0, s, out_perm, inv, w,
+                    shared_out, static_cast<float*>(y), y_f32, H, K);
 }
 
 }  // namespace moe

@@ -18,17 +18,6 @@ enum : unsigned { MOE_DEVERR_TIMEOUT = 1u, MOE_DEVERR_BOUNDS = 2u };
 // Wall-clock budget of one bounded wait, in nanoseconds.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
-template <typename T> struct Act;
-template <> struct Act<float> {
-  static __device__ __forceinline__ float load(const float* p) { return *p; }
-  static __device__ __forceinline__ float to_f(float v) { return v; }
-  static __device__ __forceinline__ float from_f(float v) { return v; }
-};
-template <> struct Act<__nv_bfloat16> {
-  static __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
-  static __device__ __forceinline__ __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
-};
-
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
@@ -84,6 +73,14 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int* to
   *total = scratch[nwarps - 1];
   __syncthreads();
   return warp_base + incl - v;
+}
+
+// Programmatic dependent launch: wait for the previous kernel on the stream (and the
+// visibility of its writes) / allow the next one to be scheduled.  Both are no-ops when
+// the kernel was launched without the programmatic-serialization attribute.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- mbarrier ----
@@ -204,6 +201,16 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
         "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
         "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+// 32 lanes x 16 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_ld_wait() {

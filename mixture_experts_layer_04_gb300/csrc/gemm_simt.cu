@@ -28,6 +28,8 @@ __global__ void __launch_bounds__(kThreads)
   __shared__ float Bg[kBK][kBN + 4];
   __shared__ float Bu[kSwi ? kBK : 1][kSwi ? kBN + 4 : 1];
 
+  grid_dep_wait();
+  grid_dep_trigger();
   const int mt = blockIdx.y;
   int g, row0, row_end;
   if (table != nullptr) {
@@ -126,15 +128,11 @@ cudaError_t launch_grouped_gemm_simt(const GroupedGemm& p, cudaStream_t s) {
   const int mt = p.mtile_table != nullptr ? p.max_mtiles : (p.rows_alloc + kBM - 1) / kBM;
   if (mt == 0) return cudaSuccess;
   dim3 grid((p.N_out + kBN - 1) / kBN, mt);
-  if (p.mode == kSwiGLU)
-    grouped_gemm_simt_kernel<true><<<grid, kThreads, 0, s>>>(
-        static_cast<const float*>(p.A), static_cast<const float*>(p.B), static_cast<float*>(p.C),
-        nullptr, p.mtile_table, p.num_mtiles, p.rows_alloc, p.Kd, p.Nb, p.N_out, p.up_offset);
-  else
-    grouped_gemm_simt_kernel<false><<<grid, kThreads, 0, s>>>(
-        static_cast<const float*>(p.A), static_cast<const float*>(p.B), static_cast<float*>(p.C),
-        p.col_bias, p.mtile_table, p.num_mtiles, p.rows_alloc, p.Kd, p.Nb, p.N_out, p.up_offset);
-  return cudaGetLastError();
+  auto kernel = p.mode == kSwiGLU ? grouped_gemm_simt_kernel<true> : grouped_gemm_simt_kernel<false>;
+  return launch_pdl(kernel, grid, dim3(kThreads), 0, s, static_cast<const float*>(p.A),
+                    static_cast<const float*>(p.B), static_cast<float*>(p.C),
+                    p.mode == kSwiGLU ? nullptr : p.col_bias, p.mtile_table, p.num_mtiles,
+                    p.rows_alloc, p.Kd, p.Nb, p.N_out, p.up_offset);
 }
 
 }  // namespace moe

@@ -6,22 +6,37 @@
 // "一个批次如何变成各专家专属的矩阵": prefill gives experts many rows (matrix efficiency
 // matters), decode gives them few (weight reads dominate).
 //
-// Design (one persistent CTA per SM, 192 threads):
-//   warp 0     TMA producer: for every tile and k-block, loads a 128x64 bf16 tile of A
-//              (token rows) and a BNx64 bf16 tile of B (expert weight rows) into a
-//              STAGES-deep shared-memory ring (128-byte swizzle), signalling an mbarrier.
-//   warp 1     MMA issuer: one elected thread issues tcgen05.mma (M=128, N=BN, K=16,
-//              bf16 x bf16 -> fp32) into one of two TMEM accumulators, frees each smem
-//              stage with tcgen05.commit, and signals the epilogue per finished tile.
-//   warps 2-5  epilogue: tcgen05.ld of the accumulator (each warp owns 32 TMEM lanes =
-//              32 rows), SwiGLU or plain fp32 (+ column bias), staging through a swizzled
-//              per-warp shared buffer, then coalesced row-masked global stores.
+// One persistent CTA per SM, 192 threads:
+//   warp 0     TMA producer: for every tile and k-block (64 bf16 = one 128-byte swizzle
+//              row), loads an activation tile (token rows) and a weight tile (expert
+//              weight rows) into a STAGES-deep shared-memory ring, signalling an mbarrier.
+//   warp 1     MMA issuer: one elected thread issues tcgen05.mma (M=128, K=16, bf16 x bf16
+//              -> fp32) into one of two TMEM accumulators, frees each smem stage with
+//              tcgen05.commit, and signals the epilogue when a tile is complete.
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator (each warp owns 32 TMEM lanes),
+//              SwiGLU or plain fp32 (+ column bias), row/column-masked global stores.
 // The two accumulators let the epilogue of tile i overlap the main loop of tile i+1.
 //
-// Ragged groups: the m-tile table lists, per 128-row tile, its expert and the row range
-// it owns.  A tile's TMA load may read rows of the next expert (or zero-filled rows past
-// the end of A); those rows are computed but never stored.  Tiles are rasterised in
-// groups of `swz` m-tiles so that the CTAs resident at one time share weight tiles in L2.
+// Two operand orders:
+//   normal  (prefill): A = 128 token rows, B = BN weight rows.  TMEM lane = token row,
+//           column = output feature.  SwiGLU: the weight tile is BN/2 gate rows followed
+//           by the BN/2 matching up rows, so a thread holds both halves of its outputs.
+//   swapped (decode, few rows per expert): A = 128 weight rows, B = BN token rows (BN =
+//           16..64), so the tensor core does no work on empty token rows and every CTA
+//           streams distinct weight bytes.  TMEM lane = output feature, column = token.
+//           SwiGLU: lanes 0-63 hold gate rows, 64-127 the matching up rows; the up half
+//           goes through shared memory to the warps that own the gate half.
+//
+// Ragged groups: each CTA derives, from the group row offsets, how many token tiles
+// every group has (a block-wide scan in shared memory) and maps a tile index to (group,
+// first row, end row, weight tile) by binary search.  A tile's TMA load may read rows of
+// the next group (or zero-filled rows past the end of A); those rows are computed but
+// never stored.  Tiles are rasterised in groups of `swz` token tiles so that the CTAs
+// resident at one time share weight tiles in L2.
+//
+// Launches use programmatic dependent launch: the prologue (barrier init, TMEM
+// allocation, descriptor prefetch) overlaps the previous kernel, and griddepcontrol.wait
+// precedes the first read of anything an earlier kernel wrote.
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -34,18 +49,18 @@
 namespace moe {
 namespace {
 
-constexpr int BM = kTcBM;  // 128
-constexpr int BK = 64;     // bf16 elements = 128 bytes = one swizzle row
+constexpr int BK = 64;  // bf16 elements = 128 bytes = one swizzle row
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kSwz = 8;
+constexpr int kMaxGroups = 1024;
 
-struct __align__(64) TcParams {
-  CUtensorMap tmA;
-  CUtensorMap tmB;
+struct TcParams {
+  CUtensorMap tmAct;  // [rows_alloc, Kd] activations (token rows)
+  CUtensorMap tmWgt;  // [G, Nb, Kd] weights
   void* C;
   const float* col_bias;
-  const int32_t* offsets;  // [num_groups+1] row offsets of the groups in A, or null
+  const int32_t* offsets;  // [num_groups+1] row offsets of the groups, or null
   unsigned* err;
   int num_groups;
   int rows_alloc;
@@ -56,30 +71,32 @@ struct __align__(64) TcParams {
   int swz;
 };
 
-template <int BN, int MODE>
+template <int BN, int MODE, bool SWAP>
 struct TcCfg {
-  static constexpr int kABytes = BM * BK * 2;
-  static constexpr int kBBytes = BN * BK * 2;
-  static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStagesRaw = (200 * 1024) / kStageBytes;
+  static constexpr int kActRows = SWAP ? BN : 128;   // token rows per tile
+  static constexpr int kWgtRows = SWAP ? 128 : BN;   // weight rows per tile
+  static constexpr int kActBytes = kActRows * BK * 2;
+  static constexpr int kWgtBytes = kWgtRows * BK * 2;
+  static constexpr int kStageBytes = kActBytes + kWgtBytes;
+  static constexpr int kStagesRaw = (192 * 1024) / kStageBytes;
   static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
-  static constexpr int kBnOut = MODE == kSwiGLU ? BN / 2 : BN;
-  static constexpr int kTmemCols = 2 * BN;
-  static constexpr int kRowBytes = MODE == kSwiGLU ? 64 : 128;  // staged bytes per row per chunk
-  static constexpr int kStgBytes = kEpiWarps * 32 * kRowBytes;
+  static constexpr int kWgtBox = MODE == kSwiGLU ? kWgtRows / 2 : kWgtRows;  // rows per TMA box
+  static constexpr int kColsOut = MODE == kSwiGLU ? kWgtRows / 2 : kWgtRows; // outputs per tile
+  static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
+  static constexpr int kStgBytes =
+      SWAP ? (MODE == kSwiGLU ? 64 * BN * 4 : 0) : kEpiWarps * 32 * (MODE == kSwiGLU ? 64 : 128);
   static constexpr int kBarBytes = 256;
-  static constexpr int kSchedBytes = 2 * 1028 * 4 + 32 * 4;  // offsets, m-tile prefix, scratch
+  static constexpr int kSchedBytes = 2 * (kMaxGroups + 4) * 4 + 32 * 4;
   static constexpr int kSmem = 1024 + kStages * kStageBytes + kStgBytes + kBarBytes + kSchedBytes;
-  static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0,
-                "TMEM columns must be a power of two in [32, 512]");
+  static_assert((kTmemCols & (kTmemCols - 1)) == 0 && kTmemCols <= 512, "TMEM columns");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M=128");
   static_assert(kSmem <= 232448, "shared memory per CTA");
 };
 
-// Tile idx -> (group g, rows row0..row_end-1 of A, n_tile).  s_off holds the group row
-// offsets and s_mt the exclusive prefix of m-tiles per group (both in shared memory).
+// Tile idx -> (group g, token rows row0..row_end-1, weight tile n_tile).  s_off holds the
+// group row offsets and s_mt the exclusive prefix of token tiles per group.
 __device__ __forceinline__ void decode_tile(const TcParams& p, const int* s_off, const int* s_mt,
-                                            int num_mt, int idx, int& g, int& row0,
+                                            int num_mt, int tile_rows, int idx, int& g, int& row0,
                                             int& row_end, int& n_tile) {
   const int gsz = p.swz * p.n_tiles;
   const int grp = idx / gsz;
@@ -95,11 +112,11 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, const int* s_off,
       if (s_mt[mid] <= mt) lo = mid; else hi = mid - 1;
     }
     g = lo;
-    row0 = s_off[g] + (mt - s_mt[g]) * BM;
+    row0 = s_off[g] + (mt - s_mt[g]) * tile_rows;
     row_end = s_off[g + 1];
   } else {
     g = 0;
-    row0 = mt * BM;
+    row0 = mt * tile_rows;
     row_end = p.rows_alloc;
   }
 }
@@ -133,23 +150,47 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <int BN, int MODE>
-__global__ void __launch_bounds__(kThreads, 1) tc_grouped_gemm_kernel(const __grid_constant__ TcParams p) {
-  using Cfg = TcCfg<BN, MODE>;
+// Barrier among the four epilogue warps only (named barrier 1, 128 threads).
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Reads NC (16 or 32) consecutive columns of this warp's 32 TMEM lanes into v[0..NC).
+template <int NC>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[32]) {
+  if constexpr (NC == 16) {
+    uint32_t r[16];
+    tmem_ld_32x32b_x16(taddr, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+  } else {
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(taddr, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+  }
+}
+
+template <int BN, int MODE, bool SWAP>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_grouped_gemm_kernel(const __grid_constant__ TcParams p) {
+  using Cfg = TcCfg<BN, MODE, SWAP>;
   constexpr int S = Cfg::kStages;
+  constexpr int kTileRows = Cfg::kActRows;
+  constexpr int kNC = BN < 32 ? BN : 32;  // TMEM columns per load in the swapped epilogue
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* sA = smem;
-  uint8_t* sB = sA + S * Cfg::kABytes;
-  uint8_t* sStg = sB + S * Cfg::kBBytes;
+  uint8_t* sAct = smem;
+  uint8_t* sWgt = sAct + S * Cfg::kActBytes;
+  uint8_t* sStg = sWgt + S * Cfg::kWgtBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + Cfg::kStgBytes);
   // bars: full[S], empty[S], tfull[2], tempty[2], mma_done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_off = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(bars) + Cfg::kBarBytes);
-  int* s_mt = s_off + 1028;
-  int* s_scan = s_mt + 1028;
+  int* s_mt = s_off + kMaxGroups + 4;
+  int* s_scan = s_mt + kMaxGroups + 4;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t bar0 = smem_u32(bars);
@@ -171,8 +212,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_grouped_gemm_kernel(const __gr
     mbar_init(mma_done_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
-    tma_prefetch_desc(&p.tmA);
-    tma_prefetch_desc(&p.tmB);
+    tma_prefetch_desc(&p.tmAct);
+    tma_prefetch_desc(&p.tmWgt);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
@@ -183,7 +224,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_grouped_gemm_kernel(const __gr
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  // Ragged schedule: every CTA derives the m-tiles of every group from the offsets.
+  // Everything below may read what earlier kernels on the stream wrote.
+  grid_dep_wait();
+  grid_dep_trigger();
+
+  // Ragged schedule: every CTA derives the token tiles of every group from the offsets.
   int num_mt;
   if (p.offsets != nullptr) {
     const int G = p.num_groups;
@@ -192,18 +237,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_grouped_gemm_kernel(const __gr
     const int per = (G + blockDim.x - 1) / blockDim.x;
     const int beg = min(G, static_cast<int>(threadIdx.x) * per), end = min(G, beg + per);
     int mine = 0;
-    for (int q = beg; q < end; ++q) mine += (s_off[q + 1] - s_off[q] + BM - 1) / BM;
+    for (int q = beg; q < end; ++q) mine += (s_off[q + 1] - s_off[q] + kTileRows - 1) / kTileRows;
     int all = 0;
     int run = block_exclusive_scan(mine, s_scan, &all);
     for (int q = beg; q < end; ++q) {
       s_mt[q] = run;
-      run += (s_off[q + 1] - s_off[q] + BM - 1) / BM;
+      run += (s_off[q + 1] - s_off[q] + kTileRows - 1) / kTileRows;
     }
     if (threadIdx.x == 0) s_mt[G] = all;
     __syncthreads();
     num_mt = all;
   } else {
-    num_mt = (p.rows_alloc + BM - 1) / BM;
+    num_mt = (p.rows_alloc + kTileRows - 1) / kTileRows;
   }
   const int total = num_mt * p.n_tiles;
 
@@ -216,8 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_grouped_gemm_kernel(const __gr
       bool ok = true;
       for (int idx = blockIdx.x; idx < total && ok; idx += gridDim.x) {
         int g, row0, row_end, n_tile;
-        decode_tile(p, s_off, s_mt, num_mt, idx, g, row0, row_end, n_tile);
-        const int n0 = n_tile * Cfg::kBnOut;
+        decode_tile(p, s_off, s_mt, num_mt, kTileRows, idx, g, row0, row_end, n_tile);
+        const int n0 = n_tile * Cfg::kColsOut;  // first weight row of the tile
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
             ok = false;
@@ -225,15 +270,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_grouped_gemm_kernel(const __gr
           }
           const uint32_t fb = full_bar(stage);
           mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
-          const uint32_t a_dst = smem_u32(sA + stage * Cfg::kABytes);
-          const uint32_t b_dst = smem_u32(sB + stage * Cfg::kBBytes);
-          tma_load_2d(a_dst, &p.tmA, fb, kb * BK, row0);
-          if constexpr (MODE == kSwiGLU) {
-            tma_load_3d(b_dst, &p.tmB, fb, kb * BK, n0, g);
-            tma_load_3d(b_dst + (BN / 2) * 128, &p.tmB, fb, kb * BK, p.up_offset + n0, g);
-          } else {
-            tma_load_3d(b_dst, &p.tmB, fb, kb * BK, n0, g);
-          }
+          const uint32_t a_dst = smem_u32(sAct + stage * Cfg::kActBytes);
+          const uint32_t w_dst = smem_u32(sWgt + stage * Cfg::kWgtBytes);
+          tma_load_2d(a_dst, &p.tmAct, fb, kb * BK, row0);
+          tma_load_3d(w_dst, &p.tmWgt, fb, kb * BK, n0, g);
+          if constexpr (MODE == kSwiGLU)
+            tma_load_3d(w_dst + Cfg::kWgtBox * 128, &p.tmWgt, fb, kb * BK, p.up_offset + n0, g);
           ++issued;
           if (++stage == S) {
             stage = 0;
@@ -259,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_grouped_gemm_kernel(const __gr
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA ----
     if (elect_one_sync()) {
-      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+      constexpr uint32_t idesc = idesc_bf16_f32(128, BN);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
@@ -276,8 +318,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_grouped_gemm_kernel(const __gr
             break;
           }
           tc_fence_after();
-          const uint32_t a_base = smem_u32(sA + stage * Cfg::kABytes);
-          const uint32_t b_base = smem_u32(sB + stage * Cfg::kBBytes);
+          const uint32_t act = smem_u32(sAct + stage * Cfg::kActBytes);
+          const uint32_t wgt = smem_u32(sWgt + stage * Cfg::kWgtBytes);
+          const uint32_t a_base = SWAP ? wgt : act;
+          const uint32_t b_base = SWAP ? act : wgt;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t ad = smem_desc_sw128(a_base + kk * 32);
@@ -303,81 +347,144 @@ __global__ void __launch_bounds__(kThreads, 1) tc_grouped_gemm_kernel(const __gr
   } else {
     // ------------------------------------------------------------ epilogue ----
     const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
-    const uint32_t stg = smem_u32(sStg) + static_cast<uint32_t>((warp - 2) * 32 * Cfg::kRowBytes);
     int local = 0;
     for (int idx = blockIdx.x; idx < total; idx += gridDim.x, ++local) {
       int g, row0, row_end, n_tile;
-      decode_tile(p, s_off, s_mt, num_mt, idx, g, row0, row_end, n_tile);
+      decode_tile(p, s_off, s_mt, num_mt, kTileRows, idx, g, row0, row_end, n_tile);
       const int acc = local & 1;
       const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
-      if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.err)) break;
+      const bool ready = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.err);
+      if constexpr (SWAP && MODE == kSwiGLU) {
+        // the four epilogue warps meet at named barriers below: leave together or not at all
+        epi_bar();
+        if (*abort_flag) break;
+      } else if (!ready) {
+        break;
+      }
       tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                              static_cast<uint32_t>(acc * BN);
-      const int tile_row0 = row0 + quad * 32;  // first global row of this warp's 32 rows
-      const int col0 = n_tile * Cfg::kBnOut;
-      if constexpr (MODE == kSwiGLU) {
-        __nv_bfloat16* C = static_cast<__nv_bfloat16*>(p.C);
+      const int col0 = n_tile * Cfg::kColsOut;
+      if constexpr (!SWAP) {
+        const uint32_t stg =
+            smem_u32(sStg) + static_cast<uint32_t>((warp - 2) * 32 * (MODE == kSwiGLU ? 64 : 128));
+        const int tile_row0 = row0 + quad * 32;  // first global row of this warp's 32 rows
+        if constexpr (MODE == kSwiGLU) {
+          __nv_bfloat16* C = static_cast<__nv_bfloat16*>(p.C);
 #pragma unroll 1
-        for (int c = 0; c < BN / 2; c += 32) {
-          uint32_t gr[32], ur[32];
-          tmem_ld_32x32b_x32(t_row + c, gr);
-          tmem_ld_32x32b_x32(t_row + BN / 2 + c, ur);
-          tmem_ld_wait();
-          uint32_t pk[16];
+          for (int c = 0; c < BN / 2; c += 32) {
+            uint32_t gr[32], ur[32];
+            tmem_ld_32x32b_x32(t_row + c, gr);
+            tmem_ld_32x32b_x32(t_row + BN / 2 + c, ur);
+            tmem_ld_wait();
+            uint32_t pk[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float h0 = silu_f(__uint_as_float(gr[2 * j])) * __uint_as_float(ur[2 * j]);
-            const float h1 =
-                silu_f(__uint_as_float(gr[2 * j + 1])) * __uint_as_float(ur[2 * j + 1]);
-            pk[j] = pack_bf16x2(h0, h1);
+            for (int j = 0; j < 16; ++j) {
+              const float h0 = silu_f(__uint_as_float(gr[2 * j])) * __uint_as_float(ur[2 * j]);
+              const float h1 =
+                  silu_f(__uint_as_float(gr[2 * j + 1])) * __uint_as_float(ur[2 * j + 1]);
+              pk[j] = pack_bf16x2(h0, h1);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              st_shared_v4(stg + stg_off<64>(lane, u), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2],
+                           pk[4 * u + 3]);
+            __syncwarp();
+#pragma unroll
+            for (int pass = 0; pass < 4; ++pass) {
+              const int rr = pass * 8 + (lane >> 2), u = lane & 3;
+              const uint4 v = ld_shared_v4(stg + stg_off<64>(rr, u));
+              const int grow = tile_row0 + rr;
+              const int col = col0 + c + u * 8;
+              if (grow < row_end && col < p.N_out)
+                *reinterpret_cast<uint4*>(C + static_cast<size_t>(grow) * p.N_out + col) = v;
+            }
+            __syncwarp();
           }
+        } else {
+          float* C = static_cast<float*>(p.C);
+#pragma unroll 1
+          for (int c = 0; c < BN; c += 32) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(t_row + c, r);
+            tmem_ld_wait();
+            if (p.col_bias != nullptr) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            st_shared_v4(stg + stg_off<64>(lane, u), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2],
-                         pk[4 * u + 3]);
-          __syncwarp();
+              for (int j = 0; j < 32; ++j) {
+                const int col = col0 + c + j;
+                const float b = col < p.N_out ? __ldg(p.col_bias + col) : 0.f;
+                r[j] = __float_as_uint(__uint_as_float(r[j]) + b);
+              }
+            }
 #pragma unroll
-          for (int pass = 0; pass < 4; ++pass) {
-            const int rr = pass * 8 + (lane >> 2), u = lane & 3;
-            const uint4 v = ld_shared_v4(stg + stg_off<64>(rr, u));
-            const int grow = tile_row0 + rr;
-            const int col = col0 + c + u * 8;
-            if (grow < row_end && col < p.N_out)
-              *reinterpret_cast<uint4*>(C + static_cast<size_t>(grow) * p.N_out + col) = v;
+            for (int u = 0; u < 8; ++u)
+              st_shared_v4(stg + stg_off<128>(lane, u), r[4 * u], r[4 * u + 1], r[4 * u + 2],
+                           r[4 * u + 3]);
+            __syncwarp();
+#pragma unroll
+            for (int pass = 0; pass < 8; ++pass) {
+              const int rr = pass * 4 + (lane >> 3), u = lane & 7;
+              const uint4 v = ld_shared_v4(stg + stg_off<128>(rr, u));
+              const int grow = tile_row0 + rr;
+              const int col = col0 + c + u * 4;
+              if (grow < row_end && col < p.N_out)
+                *reinterpret_cast<uint4*>(C + static_cast<size_t>(grow) * p.N_out + col) = v;
+            }
+            __syncwarp();
           }
-          __syncwarp();
         }
       } else {
-        float* C = static_cast<float*>(p.C);
+        // swapped: lane = weight row of the tile, column j = token row0 + j
+        if constexpr (MODE == kSwiGLU) {
+          // lanes 0-63: gate rows (quads 0, 1); lanes 64-127: up rows (quads 2, 3).
+          // xchg[r][j] holds up row r for token j, rotated by r to spread the banks.
+          float* xchg = reinterpret_cast<float*>(sStg);
+          if (quad >= 2) {
+            const int r = (quad - 2) * 32 + lane;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(t_row + c, r);
-          tmem_ld_wait();
-          if (p.col_bias != nullptr) {
+            for (int c = 0; c < BN; c += kNC) {
+              float v[32];
+              tmem_ld_cols<kNC>(t_row + c, v);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int col = col0 + c + j;
-              const float b = col < p.N_out ? __ldg(p.col_bias + col) : 0.f;
-              r[j] = __float_as_uint(__uint_as_float(r[j]) + b);
+              for (int j = 0; j < kNC; ++j) xchg[r * BN + ((c + j + r) % BN)] = v[j];
             }
           }
+          epi_bar();
+          if (quad < 2) {
+            __nv_bfloat16* C = static_cast<__nv_bfloat16*>(p.C);
+            const int r = quad * 32 + lane;
+            const int col = col0 + r;
+#pragma unroll 1
+            for (int c = 0; c < BN; c += kNC) {
+              float v[32];
+              tmem_ld_cols<kNC>(t_row + c, v);
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            st_shared_v4(stg + stg_off<128>(lane, u), r[4 * u], r[4 * u + 1], r[4 * u + 2],
-                         r[4 * u + 3]);
-          __syncwarp();
-#pragma unroll
-          for (int pass = 0; pass < 8; ++pass) {
-            const int rr = pass * 4 + (lane >> 3), u = lane & 7;
-            const uint4 v = ld_shared_v4(stg + stg_off<128>(rr, u));
-            const int grow = tile_row0 + rr;
-            const int col = col0 + c + u * 4;
-            if (grow < row_end && col < p.N_out)
-              *reinterpret_cast<uint4*>(C + static_cast<size_t>(grow) * p.N_out + col) = v;
+              for (int j = 0; j < kNC; ++j) {
+                const int tok = row0 + c + j;
+                if (tok < row_end && col < p.N_out) {
+                  const float u = xchg[r * BN + ((c + j + r) % BN)];
+                  C[static_cast<size_t>(tok) * p.N_out + col] =
+                      __float2bfloat16_rn(silu_f(v[j]) * u);
+                }
+              }
+            }
           }
-          __syncwarp();
+          epi_bar();
+        } else {
+          float* C = static_cast<float*>(p.C);
+          const int col = col0 + quad * 32 + lane;
+          const float b = (p.col_bias != nullptr && col < p.N_out) ? __ldg(p.col_bias + col) : 0.f;
+#pragma unroll 1
+          for (int c = 0; c < BN; c += kNC) {
+            float v[32];
+            tmem_ld_cols<kNC>(t_row + c, v);
+#pragma unroll
+            for (int j = 0; j < kNC; ++j) {
+              const int tok = row0 + c + j;
+              if (tok < row_end && col < p.N_out)
+                C[static_cast<size_t>(tok) * p.N_out + col] = v[j] + b;
+            }
+          }
         }
       }
       tc_fence_before();
@@ -433,25 +540,26 @@ bool make_map_3d(CUtensorMap* m, const void* base, uint64_t G, uint64_t rows, ui
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int MODE>
+template <int BN, int MODE, bool SWAP>
 cudaError_t launch_one(const GroupedGemm& g, unsigned* err, int num_sms, cudaStream_t s) {
-  using Cfg = TcCfg<BN, MODE>;
-  static int attr_set_dev = -1;  // per-process: the attribute is per function and device
+  using Cfg = TcCfg<BN, MODE, SWAP>;
+  auto kernel = tc_grouped_gemm_kernel<BN, MODE, SWAP>;
+  static int attr_set_dev = -1;  // the attribute is per function and device
   int dev = 0;
   cudaGetDevice(&dev);
   if (attr_set_dev != dev) {
-    cudaError_t e = cudaFuncSetAttribute(tc_grouped_gemm_kernel<BN, MODE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+    cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     if (e != cudaSuccess) return e;
     attr_set_dev = dev;
   }
   TcParams p;
   memset(&p, 0, sizeof(p));
-  const uint32_t b_box = MODE == kSwiGLU ? BN / 2 : BN;
-  if (!make_map_2d(&p.tmA, g.A, static_cast<uint64_t>(g.rows_alloc), static_cast<uint64_t>(g.Kd), BM))
+  if (!make_map_2d(&p.tmAct, g.A, static_cast<uint64_t>(g.rows_alloc), static_cast<uint64_t>(g.Kd),
+                   Cfg::kActRows))
     return cudaErrorInvalidValue;
-  if (!make_map_3d(&p.tmB, g.B, static_cast<uint64_t>(g.G), static_cast<uint64_t>(g.Nb),
-                   static_cast<uint64_t>(g.Kd), b_box))
+  if (!make_map_3d(&p.tmWgt, g.B, static_cast<uint64_t>(g.G), static_cast<uint64_t>(g.Nb),
+                   static_cast<uint64_t>(g.Kd), Cfg::kWgtBox))
     return cudaErrorInvalidValue;
   p.C = g.C;
   p.col_bias = g.col_bias;
@@ -461,27 +569,44 @@ cudaError_t launch_one(const GroupedGemm& g, unsigned* err, int num_sms, cudaStr
   p.rows_alloc = g.rows_alloc;
   p.num_kb = g.Kd / BK;
   p.N_out = g.N_out;
-  p.n_tiles = (g.N_out + Cfg::kBnOut - 1) / Cfg::kBnOut;
+  p.n_tiles = (g.N_out + Cfg::kColsOut - 1) / Cfg::kColsOut;
   p.up_offset = g.up_offset;
   p.swz = kSwz;
-  const long long max_mt =
-      g.offsets != nullptr ? (g.rows_alloc + BM - 1) / BM + g.G : (g.rows_alloc + BM - 1) / BM;
+  const long long rows_tiles = (g.rows_alloc + Cfg::kActRows - 1) / Cfg::kActRows;
+  const long long max_mt = g.offsets != nullptr ? rows_tiles + g.G : rows_tiles;
   const long long max_tiles = max_mt * p.n_tiles;
   if (max_tiles == 0) return cudaSuccess;
-  const int grid = static_cast<int>(max_tiles < num_sms ? max_tiles : num_sms);
-  tc_grouped_gemm_kernel<BN, MODE><<<grid, kThreads, Cfg::kSmem, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kernel, dim3(static_cast<unsigned>(max_tiles < num_sms ? max_tiles : num_sms)),
+                    dim3(kThreads), Cfg::kSmem, s, p);
 }
 
 }  // namespace
 
+int tc_swap_tokens(int max_rows_per_group) {
+  if (max_rows_per_group <= 16) return 16;
+  if (max_rows_per_group <= 32) return 32;
+  return 64;
+}
+
 cudaError_t launch_grouped_gemm_tc(const GroupedGemm& g, unsigned* err, int num_sms,
                                    cudaStream_t s) {
   if (g.dtype != kBF16) return cudaErrorInvalidValue;
-  if (g.mode == kSwiGLU) return launch_one<256, kSwiGLU>(g, err, num_sms, s);
-  if (g.N_out > 128) return launch_one<256, kPlain>(g, err, num_sms, s);
-  if (g.N_out > 64) return launch_one<128, kPlain>(g, err, num_sms, s);
-  return launch_one<64, kPlain>(g, err, num_sms, s);
+  if (g.G > kMaxGroups) return cudaErrorInvalidValue;
+  if (g.swap_tokens > 0) {
+    const int bt = tc_swap_tokens(g.swap_tokens);
+    if (g.mode == kSwiGLU) {
+      if (bt == 16) return launch_one<16, kSwiGLU, true>(g, err, num_sms, s);
+      if (bt == 32) return launch_one<32, kSwiGLU, true>(g, err, num_sms, s);
+      return launch_one<64, kSwiGLU, true>(g, err, num_sms, s);
+    }
+    if (bt == 16) return launch_one<16, kPlain, true>(g, err, num_sms, s);
+    if (bt == 32) return launch_one<32, kPlain, true>(g, err, num_sms, s);
+    return launch_one<64, kPlain, true>(g, err, num_sms, s);
+  }
+  if (g.mode == kSwiGLU) return launch_one<256, kSwiGLU, false>(g, err, num_sms, s);
+  if (g.N_out > 128) return launch_one<256, kPlain, false>(g, err, num_sms, s);
+  if (g.N_out > 64) return launch_one<128, kPlain, false>(g, err, num_sms, s);
+  return launch_one<64, kPlain, false>(g, err, num_sms, s);
 }
 
 }  // namespace moe

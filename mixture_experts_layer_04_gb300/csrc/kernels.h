@@ -6,22 +6,47 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cstring>
+#include <utility>
+
 namespace moe {
 
 enum DType : int { kF32 = 0, kBF16 = 1 };
 
 inline size_t act_bytes(int dtype) { return dtype == kBF16 ? 2 : 4; }
 
+// Launch with programmatic stream serialization: the kernel may be scheduled while the
+// previous kernel on the stream is still running; every kernel of this library calls
+// griddepcontrol.wait before reading what an earlier kernel wrote.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t lc;
+  std::memset(&lc, 0, sizeof(lc));
+  lc.gridDim = grid;
+  lc.blockDim = block;
+  lc.dynamicSmemBytes = smem;
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, kernel, std::forward<Args>(args)...);
+}
+
 // Rows per m-tile of the tensor-core grouped GEMM and of the SIMT grouped GEMM.
 constexpr int kTcBM = 128;
 constexpr int kSimtBM = 64;
 
 // ------------------------------------------------------------------ routing ----
-// Fused router for small problems: one block per token computes the E logits
-// (x . W_r^T + bias, fp32 accumulation) and one warp takes the top-k.
-cudaError_t launch_router_simt_topk(int dtype, const void* x, const void* w_router,
-                                    const float* bias, float* logits, int32_t* ids, float* w,
-                                    int T, int H, int E, int K, float theta, cudaStream_t s);
+// Router logits on the CUDA cores for small problems (few tokens or few experts):
+// logits = x . W_r^T + bias with fp32 accumulation, 8 experts x 8 tokens per block.
+// When E <= 8 the same kernel also takes the top-k (one launch); otherwise it is
+// followed by launch_topk.
+cudaError_t launch_router_simt(int dtype, const void* x, const void* w_router,
+                               const float* bias, float* logits, int32_t* ids, float* w,
+                               int T, int H, int E, int K, float theta, cudaStream_t s);
 
 // Top-k, softmax over the kept logits and gate drop, one warp per token, from
 // logits already in memory.  If `bias` is non-null it is added first and the
@@ -85,6 +110,10 @@ struct GroupedGemm {
   const int4* mtile_table;
   const int32_t* num_mtiles;
   int max_mtiles;            // upper bound of the device count (grid sizing)
+  // Tensor-core engine only: 0 = token rows on the 128-row MMA side (prefill); > 0 =
+  // the largest number of token rows a group can have, with weights on the 128-row side
+  // and tokens in tiles of 16/32/64 (decode).
+  int swap_tokens;
 };
 
 cudaError_t launch_grouped_gemm_simt(const GroupedGemm& g, cudaStream_t s);

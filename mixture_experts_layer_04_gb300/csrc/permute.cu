@@ -30,6 +30,8 @@ __global__ void __launch_bounds__(kRankTokens)
     permute_rank_kernel(const int32_t* __restrict__ ids, int T, int E, int K,
                         int32_t* __restrict__ rank_out, int32_t* __restrict__ block_counts) {
   extern __shared__ uint32_t masks[];  // [8][E]
+  grid_dep_wait();
+  grid_dep_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int i = tid; i < 8 * E; i += kRankTokens) masks[i] = 0u;
   __syncthreads();
@@ -72,6 +74,8 @@ __global__ void __launch_bounds__(kScanThreads)
                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                         int4* __restrict__ mtile_table, int32_t* __restrict__ num_mtiles, int bm) {
   __shared__ int scratch[32];
+  grid_dep_wait();
+  grid_dep_trigger();
   const int e = threadIdx.x;
   int total = 0;
   if (e < E) {
@@ -102,6 +106,8 @@ __global__ void __launch_bounds__(kScanThreads)
     mtile_table_kernel(const int32_t* __restrict__ offsets, int E, int4* __restrict__ table,
                        int32_t* __restrict__ num_mtiles, int bm) {
   __shared__ int scratch[32];
+  grid_dep_wait();
+  grid_dep_trigger();
   const int e = threadIdx.x;
   const int base = e < E ? offsets[e] : 0;
   const int count = e < E ? offsets[e + 1] - base : 0;
@@ -119,6 +125,8 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
                            const int32_t* __restrict__ block_base, int T, int E, int K,
                            int row_units, int32_t* __restrict__ inv, int32_t* __restrict__ perm,
                            const uint4* __restrict__ x, uint4* __restrict__ x_perm) {
+  grid_dep_wait();
+  grid_dep_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kScatterWarps + warp;
   if (t >= T) return;
@@ -154,26 +162,24 @@ cudaError_t launch_permute(int dtype, const void* x, const int32_t* ids, int T, 
                            int32_t* num_mtiles, int bm, cudaStream_t s) {
   const int nb = (T + kRankTokens - 1) / kRankTokens;
   if (nb > 0) {
-    permute_rank_kernel<<<nb, kRankTokens, 8 * E * sizeof(uint32_t), s>>>(ids, T, E, K, inv,
-                                                                          ws_words);
-    cudaError_t err = cudaGetLastError();
+    cudaError_t err = launch_pdl(permute_rank_kernel, dim3(nb), dim3(kRankTokens),
+                                 8 * E * sizeof(uint32_t), s, ids, T, E, K, inv, ws_words);
     if (err != cudaSuccess) return err;
   }
-  permute_scan_kernel<<<1, kScanThreads, 0, s>>>(ws_words, nb, E, counts, offsets, mtile_table,
-                                                 num_mtiles, bm);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_pdl(permute_scan_kernel, dim3(1), dim3(kScanThreads), 0, s, ws_words,
+                               nb, E, counts, offsets, mtile_table, num_mtiles, bm);
   if (err != cudaSuccess || T == 0) return err;
   const int row_units = static_cast<int>(static_cast<size_t>(H) * act_bytes(dtype) / 16);
-  permute_scatter_kernel<<<(T + kScatterWarps - 1) / kScatterWarps, kScatterWarps * 32, 0, s>>>(
-      ids, ws_words, T, E, K, row_units, inv, perm, static_cast<const uint4*>(x),
-      static_cast<uint4*>(x_perm));
-  return cudaGetLastError();
+  return launch_pdl(permute_scatter_kernel, dim3((T + kScatterWarps - 1) / kScatterWarps),
+                    dim3(kScatterWarps * 32), 0, s, ids, static_cast<const int32_t*>(ws_words), T,
+                    E, K, row_units, inv, perm, static_cast<const uint4*>(x),
+                    static_cast<uint4*>(x_perm));
 }
 
 cudaError_t launch_build_mtile_table(const int32_t* offsets, int E, int bm, int4* table,
                                      int32_t* num_mtiles, cudaStream_t s) {
-  mtile_table_kernel<<<1, kScanThreads, 0, s>>>(offsets, E, table, num_mtiles, bm);
-  return cudaGetLastError();
+  return launch_pdl(mtile_table_kernel, dim3(1), dim3(kScanThreads), 0, s, offsets, E, table,
+                    num_mtiles, bm);
 }
 
 }  // namespace moe

@@ -71,69 +71,91 @@ __device__ void warp_topk_softmax(const float* L, int E, int K, float theta, int
   }
 }
 
-template <typename TIn>
-__device__ __forceinline__ float dot_row(const TIn* a, const TIn* b, int H, int lane);
-
-template <>
-__device__ __forceinline__ float dot_row<float>(const float* a, const float* b, int H, int lane) {
-  float acc = 0.f;
-  const float4* a4 = reinterpret_cast<const float4*>(a);
-  const float4* b4 = reinterpret_cast<const float4*>(b);
-  for (int i = lane; i < H / 4; i += 32) {
-    float4 p = a4[i], q = __ldg(b4 + i);
-    acc = fmaf(p.x, q.x, acc);
-    acc = fmaf(p.y, q.y, acc);
-    acc = fmaf(p.z, q.z, acc);
-    acc = fmaf(p.w, q.w, acc);
-  }
-  return warp_sum(acc);
-}
-
-template <>
-__device__ __forceinline__ float dot_row<__nv_bfloat16>(const __nv_bfloat16* a,
-                                                        const __nv_bfloat16* b, int H, int lane) {
-  float acc = 0.f;
-  const uint4* a4 = reinterpret_cast<const uint4*>(a);
-  const uint4* b4 = reinterpret_cast<const uint4*>(b);
-  for (int i = lane; i < H / 8; i += 32) {
-    uint4 p = a4[i], q = __ldg(b4 + i);
-    const __nv_bfloat162* pp = reinterpret_cast<const __nv_bfloat162*>(&p);
-    const __nv_bfloat162* qq = reinterpret_cast<const __nv_bfloat162*>(&q);
+// Widens the 16-byte chunk i of a row of TIn into floats (8 bf16 or 4 float).
+template <typename TIn> struct Vec;
+template <> struct Vec<__nv_bfloat16> {
+  static constexpr int N = 8;
+  static __device__ __forceinline__ void load(const __nv_bfloat16* p, int i, float (&f)[8]) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(p) + i);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      float2 fp = __bfloat1622float2(pp[j]);
-      float2 fq = __bfloat1622float2(qq[j]);
-      acc = fmaf(fp.x, fq.x, acc);
-      acc = fmaf(fp.y, fq.y, acc);
+      const float2 v = __bfloat1622float2(h[j]);
+      f[2 * j] = v.x;
+      f[2 * j + 1] = v.y;
     }
   }
-  return warp_sum(acc);
-}
-
-constexpr int kRouterWarps = 8;
-
-// One block per token: warp w computes the logits of experts w, w+8, ...; then warp 0
-// takes the top-k.  Used when the router GEMM is too small for the tensor cores
-// (few tokens or few experts) and for float32 layers.
-template <typename TIn>
-__global__ void __launch_bounds__(kRouterWarps * 32)
-    router_simt_topk_kernel(const TIn* __restrict__ x, const TIn* __restrict__ w_router,
-                            const float* __restrict__ bias, float* __restrict__ logits,
-                            int32_t* __restrict__ ids, float* __restrict__ w, int H, int E, int K,
-                            float theta) {
-  extern __shared__ float Ls[];
-  const int t = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const TIn* xr = x + static_cast<size_t>(t) * H;
-  for (int e = warp; e < E; e += kRouterWarps) {
-    float d = dot_row<TIn>(xr, w_router + static_cast<size_t>(e) * H, H, lane);
-    if (lane == 0) Ls[e] = bias != nullptr ? d + bias[e] : d;
+};
+template <> struct Vec<float> {
+  static constexpr int N = 4;
+  static __device__ __forceinline__ void load(const float* p, int i, float (&f)[8]) {
+    const float4 u = __ldg(reinterpret_cast<const float4*>(p) + i);
+    f[0] = u.x;
+    f[1] = u.y;
+    f[2] = u.z;
+    f[3] = u.w;
   }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) logits[static_cast<size_t>(t) * E + e] = Ls[e];
-  if (warp == 0)
-    warp_topk_softmax(Ls, E, K, theta, ids + static_cast<size_t>(t) * K,
-                      w + static_cast<size_t>(t) * K);
+};
+
+constexpr int kRouterExperts = 8;  // warps per block, one expert each
+constexpr int kRouterTokens = 8;   // tokens per block
+
+// logits[t, e] = x[t] . W_r[e] + bias[e] for 8 experts x 8 tokens per block.  Each warp
+// keeps its expert's weights streaming through registers once and reuses them for the
+// block's 8 tokens (whose rows the 8 warps share through L1).  With E <= 8 one block
+// holds every logit of its tokens, and warp t then takes token t's top-k (fuse_topk).
+template <typename TIn>
+__global__ void __launch_bounds__(kRouterExperts * 32)
+    router_logits_kernel(const TIn* __restrict__ x, const TIn* __restrict__ w_router,
+                         const float* __restrict__ bias, float* __restrict__ logits,
+                         int32_t* __restrict__ ids, float* __restrict__ w, int T, int H, int E,
+                         int K, float theta, int fuse_topk) {
+  __shared__ float Ls[kRouterTokens][kRouterExperts];
+  grid_dep_wait();
+  grid_dep_trigger();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * kRouterExperts + warp;
+  constexpr int V = Vec<TIn>::N;
+  for (int t0 = blockIdx.y * kRouterTokens; t0 < T; t0 += gridDim.y * kRouterTokens) {
+  const int nt = min(kRouterTokens, T - t0);
+  if (e < E) {
+    float acc[kRouterTokens];
+#pragma unroll
+    for (int tt = 0; tt < kRouterTokens; ++tt) acc[tt] = 0.f;
+    const TIn* wr = w_router + static_cast<size_t>(e) * H;
+    const int chunks = H / V;
+#pragma unroll 2
+    for (int i = lane; i < chunks; i += 32) {
+      float wv[8];
+      Vec<TIn>::load(wr, i, wv);
+#pragma unroll
+      for (int tt = 0; tt < kRouterTokens; ++tt) {
+        if (tt < nt) {
+          float xv[8];
+          Vec<TIn>::load(x + static_cast<size_t>(t0 + tt) * H, i, xv);
+#pragma unroll
+          for (int j = 0; j < V; ++j) acc[tt] = fmaf(xv[j], wv[j], acc[tt]);
+        }
+      }
+    }
+    const float b = bias != nullptr ? bias[e] : 0.f;
+#pragma unroll
+    for (int tt = 0; tt < kRouterTokens; ++tt) {
+      const float v = warp_sum(acc[tt]) + b;
+      if (tt < nt && lane == 0) {
+        logits[static_cast<size_t>(t0 + tt) * E + e] = v;
+        Ls[tt][warp] = v;
+      }
+    }
+  }
+  if (fuse_topk) {
+    __syncthreads();
+    if (warp < nt)
+      warp_topk_softmax(Ls[warp], E, K, theta, ids + static_cast<size_t>(t0 + warp) * K,
+                        w + static_cast<size_t>(t0 + warp) * K);
+    __syncthreads();
+  }
+  }
 }
 
 constexpr int kTopkWarps = 4;
@@ -144,6 +166,8 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
                 float* __restrict__ logits_out, int32_t* __restrict__ ids, float* __restrict__ w,
                 int T, int E, int K, float theta) {
   extern __shared__ float Ls_all[];
+  grid_dep_wait();
+  grid_dep_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kTopkWarps + warp;
   if (t >= T) return;
@@ -164,21 +188,25 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
 
 }  // namespace
 
-cudaError_t launch_router_simt_topk(int dtype, const void* x, const void* w_router,
-                                    const float* bias, float* logits, int32_t* ids, float* w,
-                                    int T, int H, int E, int K, float theta, cudaStream_t s) {
+cudaError_t launch_router_simt(int dtype, const void* x, const void* w_router,
+                               const float* bias, float* logits, int32_t* ids, float* w,
+                               int T, int H, int E, int K, float theta, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  const size_t smem = static_cast<size_t>(E) * sizeof(float);
-  if (dtype == kBF16) {
-    router_simt_topk_kernel<__nv_bfloat16><<<T, kRouterWarps * 32, smem, s>>>(
-        static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w_router), bias,
-        logits, ids, w, H, E, K, theta);
-  } else {
-    router_simt_topk_kernel<float><<<T, kRouterWarps * 32, smem, s>>>(
-        static_cast<const float*>(x), static_cast<const float*>(w_router), bias, logits, ids, w,
-        H, E, K, theta);
-  }
-  return cudaGetLastError();
+  const int fuse = E <= kRouterExperts ? 1 : 0;
+  const int tblocks = (T + kRouterTokens - 1) / kRouterTokens;
+  const dim3 grid((E + kRouterExperts - 1) / kRouterExperts, tblocks < 65535 ? tblocks : 65535);
+  cudaError_t err;
+  if (dtype == kBF16)
+    err = launch_pdl(router_logits_kernel<__nv_bfloat16>, grid, dim3(kRouterExperts * 32), 0, s,
+                     static_cast<const __nv_bfloat16*>(x),
+                     static_cast<const __nv_bfloat16*>(w_router), bias, logits, ids, w, T, H, E,
+                     K, theta, fuse);
+  else
+    err = launch_pdl(router_logits_kernel<float>, grid, dim3(kRouterExperts * 32), 0, s,
+                     static_cast<const float*>(x), static_cast<const float*>(w_router), bias,
+                     logits, ids, w, T, H, E, K, theta, fuse);
+  if (err != cudaSuccess || fuse) return err;
+  return launch_topk(logits, nullptr, nullptr, ids, w, T, E, K, theta, s);
 }
 
 cudaError_t launch_topk(const float* logits_in, const float* bias, float* logits_out,
@@ -187,9 +215,8 @@ cudaError_t launch_topk(const float* logits_in, const float* bias, float* logits
   if (T == 0) return cudaSuccess;
   const int blocks = (T + kTopkWarps - 1) / kTopkWarps;
   const size_t smem = static_cast<size_t>(kTopkWarps) * E * sizeof(float);
-  topk_kernel<<<blocks, kTopkWarps * 32, smem, s>>>(logits_in, bias, logits_out, ids, w, T, E, K,
-                                                     theta);
-  return cudaGetLastError();
+  return launch_pdl(topk_kernel, dim3(blocks), dim3(kTopkWarps * 32), smem, s, logits_in, bias,
+                    logits_out, ids, w, T, E, K, theta);
 }
 
 }  // namespace moe

@@ -67,7 +67,6 @@ def _check_dispatch_properties(r, T, K, E):
 
 
 SMALL = [
-    synch for synch in [
         synth.WORKLOADS["toy"],
         synth.MoEShape("mixtral_small", T=512, H=512, E=8, K=2, I=1024),
         synth.MoEShape("qwen_small", T=1024, H=256, E=128, K=8, I=128, bias="normal"),
@@ -75,9 +74,12 @@ SMALL = [
                        bias="zipf"),
         synth.MoEShape("ragged", T=333, H=192, E=24, K=3, I=192, I_shared=64, theta=0.1,
                        bias="normal", seed=4),
+        synth.MoEShape("decode_shared", T=16, H=256, E=32, K=8, I=128, I_shared=128,
+                       theta=0.05, bias="zipf", seed=5),
+        synth.MoEShape("decode_128", T=128, H=512, E=16, K=4, I=192, I_shared=64, bias="normal",
+                       seed=6),
         synth.MoEShape("f32_shared", T=100, H=128, E=6, K=2, I=64, I_shared=128, theta=0.2,
                        dtype="f32", bias="normal", seed=2),
-    ]
 ]
 
 

@@ -160,6 +160,11 @@ FFN_CASES = [
     (1000, 512, 64, 4, 192, "bf16", "normal"),
     (129, 320, 16, 8, 256, "bf16", "empties"),
     (700, 256, 4, 1, 128, "bf16", "one"),
+    (64, 256, 16, 8, 128, "bf16", "normal"),     # decode sizes: weights on the MMA's M side
+    (8, 512, 128, 8, 192, "bf16", "none"),
+    (128, 256, 8, 2, 256, "bf16", "one"),         # one expert gets 128 rows: two token tiles
+    (1, 128, 4, 2, 64, "bf16", "none"),
+    (33, 320, 8, 4, 128, "bf16", "empties"),
     (256, 512, 8, 2, 1024, "f32", "none"),
     (77, 128, 4, 3, 64, "f32", "normal"),
 ]
