@@ -53,6 +53,9 @@ def parse():
     ap.add_argument("--tokens", type=int, default=None, help="token count (decode sweeps)")
     ap.add_argument("--cpu-sample", type=int, default=None, help="tokens in the CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", dest="graph", action="store_true", default=None,
+                    help="replay the layer from a CUDA graph (default: on for T <= 128)")
+    ap.add_argument("--no-graph", dest="graph", action="store_false")
     return ap.parse_args()
 
 
@@ -133,9 +136,18 @@ def kernel_launches_per_step(shape, T):
     if T == 0:
         return 0
     n = 0
-    tc_router = shape.dtype == "bf16" and T >= 256 and shape.E >= 32 and shape.E % 16 == 0
-    n += 2 if tc_router else 1            # router GEMM + top-k, or the fused SIMT router
-    n += 3                                # rank, scan, scatter-gather
+    b = 2 if shape.dtype == "bf16" else 4
+    E, H, K = shape.E, shape.H, shape.K
+    tc_router = shape.dtype == "bf16" and T >= 256 and E >= 32 and E % 16 == 0
+    wsmem_router = E <= 16 and E * H * b <= 96 * 1024 and T >= 64
+    fused_small = T <= 64 and (E * 8 * 4 + (2 * E + 1) * 4 + T * K * 12 + T * E * 4) <= 200 * 1024
+    if tc_router:
+        n += 2                            # router GEMM + top-k
+    elif wsmem_router:
+        n += 1                            # router with the top-k fused
+    else:
+        n += 1 if fused_small else 2      # partial logits (+ top-k unless fused below)
+    n += 1 if T <= 256 else 3             # one-launch permutation, or rank + scan + scatter
     n += 2                                # grouped gate/up, grouped down
     if shape.I_shared:
         n += 2
@@ -194,12 +206,28 @@ def run_ours(args, rank, world, local):
         step()
     moe.sync_check(stream)
 
+    # Decode-sized layers are launch-bound: capture the whole layer once in a CUDA graph
+    # (every kernel, with its programmatic-dependent-launch edges) and replay it.
+    use_graph = args.graph if args.graph is not None else T <= 128
+    layer_step = step
+    if use_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            moe.layer_forward(cfg, inp["x"], inp["w_router"], inp["router_bias"], inp["w_gate_up"],
+                              inp["w_down"], inp.get("w_shared_gate_up"), inp.get("w_shared_down"),
+                              y, None, ws, stream=torch.cuda.current_stream(dev))
+        layer_step = graph.replay
+        for _ in range(3):
+            flush.zero_()
+            layer_step()
+        torch.cuda.synchronize(dev)
+
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
         t_wall0 = time.perf_counter()
-        times = timed(step, args.steps)
+        times = timed(layer_step, args.steps)
         t_wall = time.perf_counter() - t_wall0
     if world > 1:
         torch.distributed.barrier()
@@ -316,6 +344,7 @@ def run_ours(args, rank, world, local):
                    "I": shape.I, "I_shared": shape.I_shared, "theta": shape.theta,
                    "router_bias": shape.bias, "l2": "flushed between steps (512 MiB write)",
                    "parallelism": "replicas" if world > 1 else "single-gpu",
+                   "cuda_graph": bool(use_graph),
                    "kept_assignments": alg["M"], "experts_touched": alg["touched"],
                    "group_rows_max": int(counts.max()), "empty_experts": int((counts == 0).sum())},
         "roofline": roof,

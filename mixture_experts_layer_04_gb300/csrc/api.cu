@@ -65,9 +65,14 @@ moe_status_t check_config(const moe_config_t* c) {
   return MOE_OK;
 }
 
+bool use_tc_router(const moe_config_t* c) {
+  return c->dtype == MOE_BF16 && c->T >= 256 && c->E >= 32 && c->E % 16 == 0;
+}
+
 // Workspace plan: every region 256-byte aligned.
 struct Plan {
-  size_t logits, ids, w, counts, offsets, perm, inv, perm_ws, table, num_mt, x_perm, h, out_perm,
+  size_t logits, partial, ids, w, counts, offsets, perm, inv, perm_ws, table, num_mt, x_perm, h,
+      out_perm,
       shared_h, shared_out, total;
 };
 
@@ -85,6 +90,12 @@ Plan make_plan(const moe_config_t* c) {
     return at;
   };
   p.logits = take(T * E * 4);
+  // H-slice partial logits of the CUDA-core router (when neither the tensor-core nor the
+  // shared-memory router serves this shape)
+  const bool part_router = !use_tc_router(c) && !router_uses_wsmem(c->dtype, c->T, c->H, c->E);
+  p.partial = take(part_router ? static_cast<size_t>(router_slices(c->T, c->H, c->E, c->dtype)) *
+                                     T * E * 4
+                               : 0);
   p.ids = take(T * K * 4);
   p.w = take(T * K * 4);
   p.counts = take(E * 4);
@@ -126,17 +137,21 @@ moe_status_t check_device(const DeviceInfo** out) {
   return MOE_OK;
 }
 
-bool use_tc_router(const moe_config_t* c) {
-  return c->dtype == MOE_BF16 && c->T >= 256 && c->E >= 32 && c->E % 16 == 0;
-}
 
 // Routing launches (shared by moe_route and moe_layer_forward).
+// Routing launches (shared by moe_route and moe_layer_forward).  `partial` is scratch
+// for the CUDA-core router's H-slice partial sums (at least slices*T*E floats), or null
+// to use one slice written straight into `logits`.  With `defer_topk` (layer forward,
+// small T) the router only writes the partials and *deferred_slices tells the caller to
+// take the top-k inside the fused small permutation.
 moe_status_t run_route(const moe_config_t* c, const DeviceInfo* d, const void* x,
                        const void* w_router, const float* bias, float* logits, int32_t* ids,
-                       float* w, cudaStream_t s) {
+                       float* w, float* partial, bool defer_topk, int* deferred_slices,
+                       cudaStream_t s) {
+  if (deferred_slices != nullptr) *deferred_slices = 0;
   if (c->T == 0) return MOE_OK;
   if (x == nullptr) {
-    return cuda_status(launch_topk(logits, nullptr, nullptr, ids, w, c->T, c->E, c->K,
+    return cuda_status(launch_topk(logits, 1, nullptr, nullptr, ids, w, c->T, c->E, c->K,
                                    c->gate_threshold, s));
   }
   if (use_tc_router(c)) {
@@ -154,10 +169,20 @@ moe_status_t run_route(const moe_config_t* c, const DeviceInfo* d, const void* x
     g.col_bias = bias;
     MOE_CUDA(launch_grouped_gemm_tc(g, d->err, d->num_sms, s));
     return cuda_status(
-        launch_topk(logits, nullptr, nullptr, ids, w, c->T, c->E, c->K, c->gate_threshold, s));
+        launch_topk(logits, 1, nullptr, nullptr, ids, w, c->T, c->E, c->K, c->gate_threshold, s));
   }
-  return cuda_status(launch_router_simt(c->dtype, x, w_router, bias, logits, ids, w, c->T, c->H,
-                                        c->E, c->K, c->gate_threshold, s));
+  if (router_uses_wsmem(c->dtype, c->T, c->H, c->E))
+    return cuda_status(launch_router_wsmem(c->dtype, x, w_router, bias, logits, ids, w, c->T, c->H,
+                                           c->E, c->K, c->gate_threshold, s));
+  const int S = partial != nullptr ? router_slices(c->T, c->H, c->E, c->dtype) : 1;
+  float* part = partial != nullptr ? partial : logits;
+  MOE_CUDA(launch_router_partial(c->dtype, x, w_router, part, S, c->T, c->H, c->E, s));
+  if (defer_topk && topk_permute_fusable(c->T, c->E, c->K)) {
+    *deferred_slices = S;
+    return MOE_OK;
+  }
+  return cuda_status(launch_topk(part, S, bias, logits, ids, w, c->T, c->E, c->K,
+                                 c->gate_threshold, s));
 }
 
 // Grouped-GEMM launch descriptions of the two expert GEMMs.  Groups come from `offsets`
@@ -328,8 +353,8 @@ moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* w_rou
   if (cfg->T == 0) return MOE_OK;
   const DeviceInfo* d = nullptr;
   MOE_TRY(check_device(&d));
-  return run_route(cfg, d, x, w_router, router_bias, logits, topk_ids, topk_w,
-                   static_cast<cudaStream_t>(stream));
+  return run_route(cfg, d, x, w_router, router_bias, logits, topk_ids, topk_w, nullptr, false,
+                   nullptr, static_cast<cudaStream_t>(stream));
 }
 
 moe_status_t moe_permute(const moe_config_t* cfg, const void* x, const int32_t* topk_ids,
@@ -471,11 +496,22 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
   const bool simt = cfg->dtype == MOE_F32;
 
   // 1. router scores, top-k, gate drop
-  MOE_TRY(run_route(cfg, d, x, w_router, router_bias, logits, ids, w, s));
-  // 2. dispatch: stable permutation, inverse map, row gather (+ the SIMT m-tile table)
-  MOE_CUDA(launch_permute(cfg->dtype, x, ids, cfg->T, cfg->H, cfg->E, cfg->K, counts, offsets,
-                          perm, inv, x_perm, at<int32_t>(ws, p.perm_ws), simt ? table : nullptr,
-                          simt ? num_mt : nullptr, kSimtBM, s));
+  int deferred = 0;
+  float* partial = at<float>(ws, p.partial);
+  MOE_TRY(run_route(cfg, d, x, w_router, router_bias, logits, ids, w, partial, true, &deferred, s));
+  // 2. dispatch: stable permutation, inverse map, row gather (+ the SIMT m-tile table);
+  //    for small batches the top-k runs inside the same launch
+  if (deferred > 0) {
+    MOE_CUDA(launch_topk_permute_small(partial, deferred, router_bias, logits, ids, w,
+                                       cfg->gate_threshold, cfg->dtype, x, cfg->T, cfg->H, cfg->E,
+                                       cfg->K, counts, offsets, perm, inv, x_perm,
+                                       simt ? table : nullptr, simt ? num_mt : nullptr, kSimtBM,
+                                       s));
+  } else {
+    MOE_CUDA(launch_permute(cfg->dtype, x, ids, cfg->T, cfg->H, cfg->E, cfg->K, counts, offsets,
+                            perm, inv, x_perm, at<int32_t>(ws, p.perm_ws), simt ? table : nullptr,
+                            simt ? num_mt : nullptr, kSimtBM, s));
+  }
   // 3-4. grouped SwiGLU FFN of the routed experts
   Groups gr;
   MOE_TRY(routed_groups(cfg, offsets, ws, p, true, s, &gr));

@@ -40,18 +40,22 @@ constexpr int kTcBM = 128;
 constexpr int kSimtBM = 64;
 
 // ------------------------------------------------------------------ routing ----
-// Router logits on the CUDA cores for small problems (few tokens or few experts):
-// logits = x . W_r^T + bias with fp32 accumulation, 8 experts x 8 tokens per block.
-// When E <= 8 the same kernel also takes the top-k (one launch); otherwise it is
-// followed by launch_topk.
-cudaError_t launch_router_simt(int dtype, const void* x, const void* w_router,
-                               const float* bias, float* logits, int32_t* ids, float* w,
-                               int T, int H, int E, int K, float theta, cudaStream_t s);
+// Router logits on the CUDA cores (see route.cu for when each is used).
+// Few experts with W_r in shared memory; top-k fused (one launch).
+bool router_uses_wsmem(int dtype, int T, int H, int E);
+cudaError_t launch_router_wsmem(int dtype, const void* x, const void* w_router,
+                                const float* bias, float* logits, int32_t* ids, float* w, int T,
+                                int H, int E, int K, float theta, cudaStream_t s);
+// Number of H slices of the partial-logits router for this shape (deterministic).
+int router_slices(int T, int H, int E, int dtype);
+// partial[s][t][e] over H slice s (no bias), S = router_slices(...) slices.
+cudaError_t launch_router_partial(int dtype, const void* x, const void* w_router, float* partial,
+                                  int S, int T, int H, int E, cudaStream_t s);
 
-// Top-k, softmax over the kept logits and gate drop, one warp per token, from
-// logits already in memory.  If `bias` is non-null it is added first and the
-// biased logits are written back to `logits_out` (which may alias `logits_in`).
-cudaError_t launch_topk(const float* logits_in, const float* bias, float* logits_out,
+// Top-k, softmax over the kept logits and gate drop, one warp per token.  The logits are
+// the sum of S partial slices [S][T][E] (S = 1: plain logits) plus `bias` (may be null);
+// they are written to `logits_out` when non-null (which may alias `partial` if S == 1).
+cudaError_t launch_topk(const float* partial, int S, const float* bias, float* logits_out,
                         int32_t* ids, float* w, int T, int E, int K, float theta,
                         cudaStream_t s);
 
@@ -71,6 +75,17 @@ cudaError_t launch_permute(int dtype, const void* x, const int32_t* ids, int T, 
                            int K, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
                            void* x_perm, int32_t* ws_words, int4* mtile_table,
                            int32_t* num_mtiles, int bm, cudaStream_t s);
+
+// Routing and the permutation in one launch for small batches: logits = sum of the
+// router's S partial slices + bias (written to `logits`), top-k/softmax/gate drop
+// (written to ids/w), then the permutation as launch_permute.
+bool topk_permute_fusable(int T, int E, int K);
+cudaError_t launch_topk_permute_small(const float* partial, int S, const float* bias,
+                                      float* logits, int32_t* ids, float* w, float theta,
+                                      int dtype, const void* x, int T, int H, int E, int K,
+                                      int32_t* counts, int32_t* offsets, int32_t* perm,
+                                      int32_t* inv, void* x_perm, int4* mtile_table,
+                                      int32_t* num_mtiles, int bm, cudaStream_t s);
 
 // The m-tile table of a grouped GEMM from offsets alone.
 cudaError_t launch_build_mtile_table(const int32_t* offsets, int E, int bm, int4* table,

@@ -19,6 +19,7 @@
 //               vectorised copy of the token row to each of its K rows.
 #include "common.cuh"
 #include "kernels.h"
+#include "topk.cuh"
 
 namespace moe {
 namespace {
@@ -149,7 +150,200 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
   }
 }
 
+constexpr int kSmallThreads = 1024;
+
+struct SmallRoute {
+  const float* partial;  // [S][T][E] router partial logits
+  int S;
+  const float* bias;
+  float* logits;         // [T][E] out
+  int32_t* ids_out;      // [T][K] out
+  float* w_out;          // [T][K] out
+  float theta;
+};
+constexpr int kSmallMaxT = 256;                 // token bit masks of 8 words per expert
+constexpr int kSmallMaskWords = kSmallMaxT / 32;
+constexpr int kSmallFusedMaxT = 64;                // routing fused into the permutation
+
+// The whole permutation in one launch for small batches (T <= 256).  Every block
+// recomputes the (cheap) index math of all T*K assignments in shared memory -- counts by
+// shared atomics, offsets by a block scan, ranks from per-expert token bit masks -- so no
+// block depends on another; block 0 stores counts/offsets/perm/inv (and the m-tile table
+// when asked), and every block copies its share of the rows into x_perm, one warp per row.
+template <bool kRoute>
+__global__ void __launch_bounds__(kSmallThreads)
+    permute_small_kernel(const int32_t* __restrict__ ids_in, SmallRoute rt, int T, int E, int K,
+                         int row_units, int32_t* __restrict__ counts,
+                         int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
+                         int32_t* __restrict__ inv, const uint4* __restrict__ x,
+                         uint4* __restrict__ x_perm, int4* __restrict__ mtile_table,
+                         int32_t* __restrict__ num_mtiles, int bm) {
+  extern __shared__ uint32_t smem_u[];
+  uint32_t* masks = smem_u;                                        // [E][8]
+  int* cnt = reinterpret_cast<int*>(masks + E * kSmallMaskWords);  // [E]
+  int* off = cnt + E;                                              // [E+1]
+  int* rows = off + E + 1;                                         // [T*K]
+  __shared__ int scratch[32];
+  grid_dep_wait();
+  grid_dep_trigger();
+  const int tid = threadIdx.x;
+  const int TK = T * K;
+  const int32_t* ids = ids_in;
+  if constexpr (kRoute) {
+    // routing of all T tokens (every block computes it; block 0 stores it): logits = sum
+    // of the router's H-slice partials in slice order + bias, then the warp top-k
+    float* Ls = reinterpret_cast<float*>(rows + TK);     // [T][E]
+    int32_t* sids = reinterpret_cast<int32_t*>(Ls + T * E);  // [T*K]
+    float* sw = reinterpret_cast<float*>(sids + TK);     // [T*K]
+    for (int i = tid; i < T * E; i += blockDim.x) {
+      float v = 0.f;
+      for (int sl = 0; sl < rt.S; ++sl) v += rt.partial[static_cast<size_t>(sl) * T * E + i];
+      if (rt.bias != nullptr) v += rt.bias[i % E];
+      Ls[i] = v;
+      if (blockIdx.x == 0) rt.logits[i] = v;
+    }
+    __syncthreads();
+    const int nwarps = blockDim.x >> 5;
+    for (int t = tid >> 5; t < T; t += nwarps)
+      warp_topk_softmax(Ls + t * E, E, K, rt.theta, sids + t * K, sw + t * K);
+    __syncthreads();
+    if (blockIdx.x == 0)
+      for (int i = tid; i < TK; i += blockDim.x) {
+        rt.ids_out[i] = sids[i];
+        rt.w_out[i] = sw[i];
+      }
+    ids = sids;
+  }
+  for (int i = tid; i < E * kSmallMaskWords; i += blockDim.x) masks[i] = 0u;
+  __syncthreads();
+  for (int a = tid; a < TK; a += blockDim.x) {
+    const int e = ids[a];
+    if (e >= 0) {
+      const int t = a / K;
+      atomicOr(&masks[e * kSmallMaskWords + (t >> 5)], 1u << (t & 31));
+    }
+  }
+  __syncthreads();
+  int c = 0;
+  if (tid < E) {
+#pragma unroll
+    for (int w = 0; w < kSmallMaskWords; ++w) c += __popc(masks[tid * kSmallMaskWords + w]);
+  }
+  int M = 0;
+  const int base = block_exclusive_scan(tid < E ? c : 0, scratch, &M);
+  if (tid < E) {
+    cnt[tid] = c;
+    off[tid] = base;
+  }
+  if (tid == 0) off[E] = M;
+  __syncthreads();
+  for (int a = tid; a < TK; a += blockDim.x) {
+    const int e = ids[a];
+    int row = -1;
+    if (e >= 0) {
+      const int t = a / K;
+      const uint32_t* m = masks + e * kSmallMaskWords;
+      int r = __popc(m[t >> 5] & ((1u << (t & 31)) - 1u));
+      for (int w = 0; w < (t >> 5); ++w) r += __popc(m[w]);
+      row = off[e] + r;
+    }
+    rows[a] = row;
+  }
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    if (tid < E) counts[tid] = cnt[tid];
+    for (int i = tid; i <= E; i += blockDim.x) offsets[i] = off[i];
+    for (int a = tid; a < TK; a += blockDim.x) {
+      inv[a] = rows[a];
+      if (rows[a] >= 0) perm[rows[a]] = a / K;
+    }
+    if (mtile_table != nullptr) {
+      const int nt = tid < E ? (cnt[tid] + bm - 1) / bm : 0;
+      int all = 0;
+      const int first = block_exclusive_scan(nt, scratch, &all);
+      if (tid < E)
+        for (int j = 0; j < nt; ++j)
+          mtile_table[first + j] = make_int4(tid, off[tid] + j * bm, off[tid] + cnt[tid], 0);
+      if (tid == 0) *num_mtiles = all;
+    }
+  }
+  // row copies: assignment a -> x_perm[rows[a]] = x[a / K], one warp per assignment
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int a = blockIdx.x * (kSmallThreads / 32) + warp; a < TK;
+       a += gridDim.x * (kSmallThreads / 32)) {
+    const int r = rows[a];
+    if (r < 0) continue;
+    const uint4* src = x + static_cast<size_t>(a / K) * row_units;
+    uint4* dst = x_perm + static_cast<size_t>(r) * row_units;
+    for (int i = lane; i < row_units; i += 32) dst[i] = src[i];
+  }
+}
+
+
+size_t small_smem_bytes(int T, int E, int K, bool route) {
+  size_t b = static_cast<size_t>(E) * kSmallMaskWords * 4 + (2 * E + 1) * 4 +
+             static_cast<size_t>(T) * K * 4;
+  if (route) b += static_cast<size_t>(T) * E * 4 + static_cast<size_t>(T) * K * 8;
+  return b;
+}
+
+constexpr size_t kSmallMaxSmem = 200 * 1024;
+
+template <bool kRoute>
+cudaError_t launch_small_t(int dtype, const void* x, const int32_t* ids, const SmallRoute* rt,
+                           int T, int H, int E, int K, int32_t* counts, int32_t* offsets,
+                           int32_t* perm, int32_t* inv, void* x_perm, int4* mtile_table,
+                           int32_t* num_mtiles, int bm, cudaStream_t s) {
+  static int attr_dev = -1;  // opt in to more than 48 KB of dynamic shared memory once
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (attr_dev != dev) {
+    cudaError_t e = cudaFuncSetAttribute(permute_small_kernel<kRoute>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmallMaxSmem));
+    if (e != cudaSuccess) return e;
+    attr_dev = dev;
+  }
+  const size_t smem = small_smem_bytes(T, E, K, kRoute);
+  if (smem > kSmallMaxSmem) return cudaErrorInvalidValue;
+  const int row_units = static_cast<int>(static_cast<size_t>(H) * act_bytes(dtype) / 16);
+  int blocks = (T * K + 31) / 32;
+  blocks = blocks < 148 ? blocks : 148;
+  SmallRoute r{};
+  if (rt != nullptr) r = *rt;
+  return launch_pdl(permute_small_kernel<kRoute>, dim3(blocks), dim3(kSmallThreads), smem, s, ids,
+                    r, T, E, K, row_units, counts, offsets, perm, inv,
+                    static_cast<const uint4*>(x), static_cast<uint4*>(x_perm), mtile_table,
+                    num_mtiles, bm);
+}
+
+cudaError_t launch_small(int dtype, const void* x, const int32_t* ids, const SmallRoute* rt,
+                         int T, int H, int E, int K, int32_t* counts, int32_t* offsets,
+                         int32_t* perm, int32_t* inv, void* x_perm, int4* mtile_table,
+                         int32_t* num_mtiles, int bm, cudaStream_t s) {
+  if (rt != nullptr)
+    return launch_small_t<true>(dtype, x, ids, rt, T, H, E, K, counts, offsets, perm, inv, x_perm,
+                                mtile_table, num_mtiles, bm, s);
+  return launch_small_t<false>(dtype, x, ids, rt, T, H, E, K, counts, offsets, perm, inv, x_perm,
+                               mtile_table, num_mtiles, bm, s);
+}
+
 }  // namespace
+
+bool topk_permute_fusable(int T, int E, int K) {
+  return T > 0 && T <= kSmallFusedMaxT && small_smem_bytes(T, E, K, true) <= kSmallMaxSmem;
+}
+
+cudaError_t launch_topk_permute_small(const float* partial, int S, const float* bias,
+                                      float* logits, int32_t* ids, float* w, float theta,
+                                      int dtype, const void* x, int T, int H, int E, int K,
+                                      int32_t* counts, int32_t* offsets, int32_t* perm,
+                                      int32_t* inv, void* x_perm, int4* mtile_table,
+                                      int32_t* num_mtiles, int bm, cudaStream_t s) {
+  SmallRoute rt{partial, S, bias, logits, ids, w, theta};
+  return launch_small(dtype, x, nullptr, &rt, T, H, E, K, counts, offsets, perm, inv, x_perm,
+                      mtile_table, num_mtiles, bm, s);
+}
 
 size_t permute_ws_words(int T, int E) {
   const size_t nb = (static_cast<size_t>(T) + kRankTokens - 1) / kRankTokens;
@@ -160,6 +354,9 @@ cudaError_t launch_permute(int dtype, const void* x, const int32_t* ids, int T, 
                            int K, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
                            void* x_perm, int32_t* ws_words, int4* mtile_table,
                            int32_t* num_mtiles, int bm, cudaStream_t s) {
+  if (T > 0 && T <= kSmallMaxT)
+    return launch_small(dtype, x, ids, nullptr, T, H, E, K, counts, offsets, perm, inv, x_perm,
+                        mtile_table, num_mtiles, bm, s);
   const int nb = (T + kRankTokens - 1) / kRankTokens;
   if (nb > 0) {
     cudaError_t err = launch_pdl(permute_rank_kernel, dim3(nb), dim3(kRankTokens),

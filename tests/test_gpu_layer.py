@@ -150,6 +150,9 @@ def test_layer_full_size_sampled(moe, name, T, nsample):
         np.testing.assert_array_equal(r["offsets"], offsets_ref)
     toks = _sample_tokens(r, Tn, nsample)
     toks = toks[~amb[toks]]
+    assert len(toks) >= max(1, nsample // 2), "too few unambiguous sampled tokens"
+    experts_checked = len(np.unique(r["ids"][toks][r["ids"][toks] >= 0]))
+    assert experts_checked >= min(shape.E // 4, 8)
     sh = {}
     if shape.I_shared:
         sh = dict(w_shared_gate_up=H.f64(inp["w_shared_gate_up"]), w_shared_down=H.f64(inp["w_shared_down"]))

@@ -78,6 +78,8 @@ ROUTER_CASES = [
     (257, 256, 256, "bf16", "zipf"),
     (300, 1024, 8, "bf16", "none"),
     (64, 2048, 128, "bf16", "normal"),
+    (16, 7168, 256, "bf16", "zipf"),           # one slice of 896 units: several bursts
+    (100, 1088, 24, "bf16", "normal"),
     (256, 512, 8, "f32", "none"),
     (3, 192, 40, "f32", "normal"),
 ]
