@@ -56,6 +56,9 @@ def parse():
     ap.add_argument("--graph", dest="graph", action="store_true", default=None,
                     help="replay the layer from a CUDA graph (default: on for T <= 128)")
     ap.add_argument("--no-graph", dest="graph", action="store_false")
+    ap.add_argument("--fused-combine", dest="fused", action="store_true", default=None,
+                    help="fuse the combine into the down GEMM (MOE_FLAG_FUSED_COMBINE)")
+    ap.add_argument("--gather-combine", dest="fused", action="store_false")
     return ap.parse_args()
 
 
@@ -179,7 +182,10 @@ def run_ours(args, rank, world, local):
     T = args.tokens if args.tokens is not None else shape.T
     inp = synth.make_inputs(shape.with_(seed=shape.seed + rank), device=dev, T=T)
     dt = moe.BF16 if shape.dtype == "bf16" else moe.F32
-    cfg = moe.MoEConfig.make(T, shape.H, shape.E, shape.K, shape.I, shape.I_shared, shape.theta, dt)
+    fused = bool(args.fused) if args.fused is not None else False
+    flags = moe.FLAG_FUSED_COMBINE if fused else 0
+    cfg = moe.MoEConfig.make(T, shape.H, shape.E, shape.K, shape.I, shape.I_shared, shape.theta, dt,
+                             flags)
     ws = torch.empty(moe.workspace_size(cfg), dtype=torch.uint8, device=dev)
     y = torch.empty(T, shape.H, dtype=shape.torch_dtype, device=dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -345,6 +351,7 @@ def run_ours(args, rank, world, local):
                    "router_bias": shape.bias, "l2": "flushed between steps (512 MiB write)",
                    "parallelism": "replicas" if world > 1 else "single-gpu",
                    "cuda_graph": bool(use_graph),
+                   "combine": "fused scatter-add (fp32, order not fixed)" if fused else "gather (deterministic)",
                    "kept_assignments": alg["M"], "experts_touched": alg["touched"],
                    "group_rows_max": int(counts.max()), "empty_experts": int((counts == 0).sum())},
         "roofline": roof,

@@ -60,6 +60,19 @@ typedef enum {
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
 
+/* moe_config_t.flags */
+enum {
+  /* moe_layer_forward only, bf16 layers: fuse the combine into the down projection.  Each
+   * routed row of the down GEMM is scaled by its gate and added in fp32 straight into its
+   * token's row of the fp32 sum (which the shared expert initialises, else it starts at
+   * zero); one pass then rounds the sum to bf16.  This removes the [T*K, H] fp32
+   * intermediate and the separate combine.  The K additions of a token happen in no fixed
+   * order, so y and y_f32 are correct to fp32 rounding but not bitwise reproducible from
+   * run to run.  Without this flag (default) the combine gathers in slot order and every
+   * output is deterministic.  Float32 layers ignore the flag. */
+  MOE_FLAG_FUSED_COMBINE = 1u
+};
+
 typedef struct {
   int32_t T;               /* tokens */
   int32_t H;               /* hidden size */
@@ -69,7 +82,7 @@ typedef struct {
   int32_t I_shared;        /* shared expert intermediate size, 0 = no shared expert */
   float gate_threshold;    /* theta: drop kept gates below it (slot 0 never), 0 = off */
   int32_t dtype;           /* moe_dtype_t of activations and weights */
-  uint32_t flags;          /* reserved, must be 0 */
+  uint32_t flags;          /* MOE_FLAG_* bits; 0 = defaults */
 } moe_config_t;
 
 typedef void* moe_stream_t; /* a cudaStream_t */

@@ -16,13 +16,16 @@ import os
 from typing import Optional
 
 __all__ = [
-    "MoEConfig", "MoEError", "F32", "BF16", "library_path", "load", "workspace_size",
+    "MoEConfig", "MoEError", "F32", "BF16", "FLAG_FUSED_COMBINE", "library_path", "load", "workspace_size",
     "route", "permute", "permute_noalloc", "grouped_ffn", "expert_gate_up", "expert_down", "combine", "layer_forward", "workspace_views",
     "sync_check", "status_string", "version",
 ]
 
 F32 = 0
 BF16 = 1
+# moe_config_t.flags: fuse the combine into the down projection (bf16 layers; y is then
+# correct to fp32 rounding but not bitwise reproducible run to run)
+FLAG_FUSED_COMBINE = 1
 
 _STATUS = {
     0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",

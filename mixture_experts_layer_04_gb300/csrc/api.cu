@@ -53,7 +53,7 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 moe_status_t check_config(const moe_config_t* c) {
   if (c == nullptr) return MOE_ERR_INVALID_ARG;
-  if (c->flags != 0u) return MOE_ERR_INVALID_ARG;
+  if ((c->flags & ~static_cast<uint32_t>(MOE_FLAG_FUSED_COMBINE)) != 0u) return MOE_ERR_INVALID_ARG;
   if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if (c->T < 0 || c->H <= 0 || c->E <= 0 || c->K <= 0 || c->I <= 0 || c->I_shared < 0)
     return MOE_ERR_INVALID_ARG;
@@ -72,7 +72,7 @@ bool use_tc_router(const moe_config_t* c) {
 // Workspace plan: every region 256-byte aligned.
 struct Plan {
   size_t logits, partial, ids, w, counts, offsets, perm, inv, perm_ws, table, num_mt, x_perm, h,
-      out_perm,
+      out_perm, row_w, y32,
       shared_h, shared_out, total;
 };
 
@@ -110,6 +110,9 @@ Plan make_plan(const moe_config_t* c) {
   p.out_perm = take(T * K * H * 4);
   p.shared_h = take(T * Is * ab);
   p.shared_out = take(Is > 0 ? T * H * 4 : 0);
+  const bool fused = (c->flags & MOE_FLAG_FUSED_COMBINE) != 0u;
+  p.row_w = take(fused ? T * K * 4 : 0);
+  p.y32 = take(fused ? T * H * 4 : 0);
   p.total = o;
   return p;
 }
@@ -173,7 +176,7 @@ moe_status_t run_route(const moe_config_t* c, const DeviceInfo* d, const void* x
   }
   if (router_uses_wsmem(c->dtype, c->T, c->H, c->E))
     return cuda_status(launch_router_wsmem(c->dtype, x, w_router, bias, logits, ids, w, c->T, c->H,
-                                           c->E, c->K, c->gate_threshold, s));
+                                           c->E, c->K, c->gate_threshold, d->err, s));
   const int S = partial != nullptr ? router_slices(c->T, c->H, c->E, c->dtype) : 1;
   float* part = partial != nullptr ? partial : logits;
   MOE_CUDA(launch_router_partial(c->dtype, x, w_router, part, S, c->T, c->H, c->E, s));
@@ -253,6 +256,30 @@ moe_status_t run_down(const moe_config_t* c, const DeviceInfo* d, const void* h,
   g.mtile_table = gr.table;
   g.num_mtiles = gr.num_mt;
   g.max_mtiles = gr.max_mt;
+  return launch_gemm(c, d, g, s);
+}
+
+// The fused combine: y32[perm[r]] += row_w[r] * (h[r] W_d^T) for every kept row r, with
+// the additions done at L2 (bf16 layers on the tensor cores only).
+moe_status_t run_down_scatter(const moe_config_t* c, const DeviceInfo* d, const void* h,
+                              int rows_alloc, const void* w_down, int I, float* y32,
+                              const Groups& gr, const int32_t* perm, const float* row_w,
+                              cudaStream_t s) {
+  if (rows_alloc == 0) return MOE_OK;
+  GroupedGemm g{};
+  g.mode = kScatter;
+  g.dtype = c->dtype;
+  g.A = h;
+  g.rows_alloc = rows_alloc;
+  g.Kd = I;
+  g.B = w_down;
+  g.G = gr.G;
+  g.Nb = c->H;
+  g.N_out = c->H;
+  g.C = y32;
+  g.offsets = gr.offsets;
+  g.row_token = perm;
+  g.row_w = row_w;
   return launch_gemm(c, d, g, s);
 }
 
@@ -376,7 +403,8 @@ moe_status_t moe_permute(const moe_config_t* cfg, const void* x, const int32_t* 
   MOE_TRY(check_device(&d));
   return cuda_status(launch_permute(cfg->dtype, x, topk_ids, cfg->T, cfg->H, cfg->E, cfg->K,
                                     counts, offsets, perm, inv, x_perm, at<int32_t>(ws, p.perm_ws),
-                                    nullptr, nullptr, 0, static_cast<cudaStream_t>(stream)));
+                                    nullptr, nullptr, 0, nullptr, nullptr,
+                                    static_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_grouped_ffn(const moe_config_t* cfg, const void* x_perm, const int32_t* offsets,
@@ -494,6 +522,8 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
   void* x_perm = at<void>(ws, p.x_perm);
   float* out_perm = at<float>(ws, p.out_perm);
   const bool simt = cfg->dtype == MOE_F32;
+  // the fused combine needs the tensor-core engine; float32 layers keep the gather combine
+  const bool fused = (cfg->flags & MOE_FLAG_FUSED_COMBINE) != 0u && !simt;
 
   // 1. router scores, top-k, gate drop
   int deferred = 0;
@@ -506,11 +536,12 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
                                        cfg->gate_threshold, cfg->dtype, x, cfg->T, cfg->H, cfg->E,
                                        cfg->K, counts, offsets, perm, inv, x_perm,
                                        simt ? table : nullptr, simt ? num_mt : nullptr, kSimtBM,
-                                       s));
+                                       fused ? at<float>(ws, p.row_w) : nullptr, s));
   } else {
     MOE_CUDA(launch_permute(cfg->dtype, x, ids, cfg->T, cfg->H, cfg->E, cfg->K, counts, offsets,
                             perm, inv, x_perm, at<int32_t>(ws, p.perm_ws), simt ? table : nullptr,
-                            simt ? num_mt : nullptr, kSimtBM, s));
+                            simt ? num_mt : nullptr, kSimtBM, w,
+                            fused ? at<float>(ws, p.row_w) : nullptr, s));
   }
   // 3-4. grouped SwiGLU FFN of the routed experts
   Groups gr;
@@ -518,6 +549,25 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
   void* h = at<void>(ws, p.h);
   const int rows = cfg->T * cfg->K;
   MOE_TRY(run_gate_up(cfg, d, x_perm, rows, w_gate_up, cfg->I, h, gr, s));
+  if (fused) {
+    // 5'. shared expert written straight into the fp32 sum (or the sum zeroed), then the
+    //     down projection adds every routed row, scaled by its gate, into its token's row,
+    //     and one pass rounds the sum to the output type
+    float* y32 = y_f32 != nullptr ? y_f32 : at<float>(ws, p.y32);
+    if (shared) {
+      Groups one{};
+      one.G = 1;
+      void* hs = at<void>(ws, p.shared_h);
+      MOE_TRY(run_gate_up(cfg, d, x, cfg->T, w_shared_gate_up, cfg->I_shared, hs, one, s));
+      MOE_TRY(run_down(cfg, d, hs, cfg->T, w_shared_down, cfg->I_shared, y32, one, s));
+    } else {
+      MOE_CUDA(cudaMemsetAsync(y32, 0, static_cast<size_t>(cfg->T) * cfg->H * sizeof(float), s));
+    }
+    MOE_TRY(run_down_scatter(cfg, d, h, rows, w_down, cfg->I, y32, gr, perm,
+                             at<float>(ws, p.row_w), s));
+    return cuda_status(
+        launch_finalize(cfg->dtype, y32, y, static_cast<long long>(cfg->T) * cfg->H, s));
+  }
   MOE_TRY(run_down(cfg, d, h, rows, w_down, cfg->I, out_perm, gr, s));
   // 5. shared expert: the same engine on all T rows of x as one group
   float* shared_out = nullptr;

@@ -61,6 +61,8 @@ struct TcParams {
   void* C;
   const float* col_bias;
   const int32_t* offsets;  // [num_groups+1] row offsets of the groups, or null
+  const int32_t* row_token;  // kScatter: destination row (token) of every A row
+  const float* row_w;        // kScatter: scale of every A row (its route weight)
   unsigned* err;
   int num_groups;
   int rows_alloc;
@@ -148,6 +150,16 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Fire-and-forget fp32 additions into global memory (performed at L2).
+__device__ __forceinline__ void red_add_v4(float* p, const uint4& v) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(__uint_as_float(v.x)),
+               "f"(__uint_as_float(v.y)), "f"(__uint_as_float(v.z)), "f"(__uint_as_float(v.w))
+               : "memory");
+}
+__device__ __forceinline__ void red_add_f32(float* p, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
 // Barrier among the four epilogue warps only (named barrier 1, 128 threads).
@@ -403,11 +415,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else {
           float* C = static_cast<float*>(p.C);
+          // kScatter: this thread's row is scaled by its route weight and added into the
+          // output row of its token (the fused combine); other rows are stored as they are
+          float rw = 1.f;
+          if constexpr (MODE == kScatter) {
+            const int grow = tile_row0 + lane;
+            rw = grow < row_end ? __ldg(p.row_w + grow) : 0.f;
+          }
 #pragma unroll 1
           for (int c = 0; c < BN; c += 32) {
             uint32_t r[32];
             tmem_ld_32x32b_x32(t_row + c, r);
             tmem_ld_wait();
+            if constexpr (MODE == kScatter) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * rw);
+            }
             if (p.col_bias != nullptr) {
 #pragma unroll
               for (int j = 0; j < 32; ++j) {
@@ -427,8 +450,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint4 v = ld_shared_v4(stg + stg_off<128>(rr, u));
               const int grow = tile_row0 + rr;
               const int col = col0 + c + u * 4;
-              if (grow < row_end && col < p.N_out)
-                *reinterpret_cast<uint4*>(C + static_cast<size_t>(grow) * p.N_out + col) = v;
+              if (grow < row_end && col < p.N_out) {
+                if constexpr (MODE == kScatter) {
+                  const int tok = __ldg(p.row_token + grow);
+                  red_add_v4(C + static_cast<size_t>(tok) * p.N_out + col, v);
+                } else {
+                  *reinterpret_cast<uint4*>(C + static_cast<size_t>(grow) * p.N_out + col) = v;
+                }
+              }
             }
             __syncwarp();
           }
@@ -480,9 +509,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld_cols<kNC>(t_row + c, v);
 #pragma unroll
             for (int j = 0; j < kNC; ++j) {
-              const int tok = row0 + c + j;
-              if (tok < row_end && col < p.N_out)
-                C[static_cast<size_t>(tok) * p.N_out + col] = v[j] + b;
+              const int row = row0 + c + j;
+              if (row < row_end && col < p.N_out) {
+                if constexpr (MODE == kScatter) {
+                  const int tok = __ldg(p.row_token + row);
+                  red_add_f32(C + static_cast<size_t>(tok) * p.N_out + col,
+                              __ldg(p.row_w + row) * v[j]);
+                } else {
+                  C[static_cast<size_t>(row) * p.N_out + col] = v[j] + b;
+                }
+              }
             }
           }
         }
@@ -564,6 +600,8 @@ cudaError_t launch_one(const GroupedGemm& g, unsigned* err, int num_sms, cudaStr
   p.C = g.C;
   p.col_bias = g.col_bias;
   p.offsets = g.offsets;
+  p.row_token = g.row_token;
+  p.row_w = g.row_w;
   p.num_groups = g.G;
   p.err = err;
   p.rows_alloc = g.rows_alloc;
@@ -599,10 +637,16 @@ cudaError_t launch_grouped_gemm_tc(const GroupedGemm& g, unsigned* err, int num_
       if (bt == 32) return launch_one<32, kSwiGLU, true>(g, err, num_sms, s);
       return launch_one<64, kSwiGLU, true>(g, err, num_sms, s);
     }
+    if (g.mode == kScatter) {
+      if (bt == 16) return launch_one<16, kScatter, true>(g, err, num_sms, s);
+      if (bt == 32) return launch_one<32, kScatter, true>(g, err, num_sms, s);
+      return launch_one<64, kScatter, true>(g, err, num_sms, s);
+    }
     if (bt == 16) return launch_one<16, kPlain, true>(g, err, num_sms, s);
     if (bt == 32) return launch_one<32, kPlain, true>(g, err, num_sms, s);
     return launch_one<64, kPlain, true>(g, err, num_sms, s);
   }
+  if (g.mode == kScatter) return launch_one<256, kScatter, false>(g, err, num_sms, s);
   if (g.mode == kSwiGLU) return launch_one<256, kSwiGLU, false>(g, err, num_sms, s);
   if (g.N_out > 128) return launch_one<256, kPlain, false>(g, err, num_sms, s);
   if (g.N_out > 64) return launch_one<128, kPlain, false>(g, err, num_sms, s);

@@ -45,7 +45,7 @@ constexpr int kSimtBM = 64;
 bool router_uses_wsmem(int dtype, int T, int H, int E);
 cudaError_t launch_router_wsmem(int dtype, const void* x, const void* w_router,
                                 const float* bias, float* logits, int32_t* ids, float* w, int T,
-                                int H, int E, int K, float theta, cudaStream_t s);
+                                int H, int E, int K, float theta, unsigned* err, cudaStream_t s);
 // Number of H slices of the partial-logits router for this shape (deterministic).
 int router_slices(int T, int H, int E, int dtype);
 // partial[s][t][e] over H slice s (no bias), S = router_slices(...) slices.
@@ -70,11 +70,12 @@ inline int max_mtiles(int T, int K, int E, int bm) {
 // Stable counting-sort permutation: counts, offsets, perm, inv and the row gather
 // x_perm[r] = x[perm[r]].  If `mtile_table` is non-null the m-tile table of `bm`
 // rows per tile is written as well (entries {expert, row0, row_end, 0}) with its
-// length in *num_mtiles.
+// length in *num_mtiles.  If `row_w` is non-null, row_w[r] = gate_w of row r's slot.
 cudaError_t launch_permute(int dtype, const void* x, const int32_t* ids, int T, int H, int E,
                            int K, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
                            void* x_perm, int32_t* ws_words, int4* mtile_table,
-                           int32_t* num_mtiles, int bm, cudaStream_t s);
+                           int32_t* num_mtiles, int bm, const float* gate_w, float* row_w,
+                           cudaStream_t s);
 
 // Routing and the permutation in one launch for small batches: logits = sum of the
 // router's S partial slices + bias (written to `logits`), top-k/softmax/gate drop
@@ -85,13 +86,15 @@ cudaError_t launch_topk_permute_small(const float* partial, int S, const float* 
                                       int dtype, const void* x, int T, int H, int E, int K,
                                       int32_t* counts, int32_t* offsets, int32_t* perm,
                                       int32_t* inv, void* x_perm, int4* mtile_table,
-                                      int32_t* num_mtiles, int bm, cudaStream_t s);
+                                      int32_t* num_mtiles, int bm, float* row_w, cudaStream_t s);
 
 // The m-tile table of a grouped GEMM from offsets alone.
 cudaError_t launch_build_mtile_table(const int32_t* offsets, int E, int bm, int4* table,
                                      int32_t* num_mtiles, cudaStream_t s);
 
 // ----------------------------------------------------------------- combine ----
+// y = act(y_f32) elementwise (the last step of the fused combine).
+cudaError_t launch_finalize(int dtype, const float* y_f32, void* y, long long n, cudaStream_t s);
 cudaError_t launch_combine(int dtype, const float* out_perm, const int32_t* inv, const float* w,
                            const float* shared_out, void* y, float* y_f32, int T, int H, int K,
                            cudaStream_t s);
@@ -102,7 +105,9 @@ cudaError_t launch_combine(int dtype, const float* out_perm, const int32_t* inv,
 //   C[row, n] = sum_k A[row, k] * B[g, n, k]                      (mode kPlain)
 //   C[row, n] = silu(sum_k A B[g, n, k]) * (sum_k A B[g, up + n, k])  (mode kSwiGLU)
 // A: [rows_alloc, Kd] row-major; B: [G, Nb, Kd] row-major; C: [rows_alloc, N_out].
-enum GemmMode : int { kPlain = 0, kSwiGLU = 1 };
+//   C[row_token[row], n] += row_w[row] * sum_k A[row, k] * B[g, n, k]  (mode kScatter:
+//   the combine fused into the down projection; fp32 additions at L2, order not fixed)
+enum GemmMode : int { kPlain = 0, kSwiGLU = 1, kScatter = 2 };
 
 struct GroupedGemm {
   int mode;
@@ -129,6 +134,8 @@ struct GroupedGemm {
   // the largest number of token rows a group can have, with weights on the 128-row side
   // and tokens in tiles of 16/32/64 (decode).
   int swap_tokens;
+  const int32_t* row_token;  // kScatter only
+  const float* row_w;        // kScatter only
 };
 
 cudaError_t launch_grouped_gemm_simt(const GroupedGemm& g, cudaStream_t s);

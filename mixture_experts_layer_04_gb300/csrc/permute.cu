@@ -125,7 +125,8 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
     permute_scatter_kernel(const int32_t* __restrict__ ids,
                            const int32_t* __restrict__ block_base, int T, int E, int K,
                            int row_units, int32_t* __restrict__ inv, int32_t* __restrict__ perm,
-                           const uint4* __restrict__ x, uint4* __restrict__ x_perm) {
+                           const uint4* __restrict__ x, uint4* __restrict__ x_perm,
+                           const float* __restrict__ gate_w, float* __restrict__ row_w) {
   grid_dep_wait();
   grid_dep_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -139,6 +140,7 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
       row = block_base[static_cast<size_t>(b) * E + e] + inv[static_cast<size_t>(t) * K + lane];
       inv[static_cast<size_t>(t) * K + lane] = row;
       perm[row] = t;
+      if (row_w != nullptr) row_w[row] = gate_w[static_cast<size_t>(t) * K + lane];
     }
   }
   const uint4* src = x + static_cast<size_t>(t) * row_units;
@@ -177,7 +179,8 @@ __global__ void __launch_bounds__(kSmallThreads)
                          int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
                          int32_t* __restrict__ inv, const uint4* __restrict__ x,
                          uint4* __restrict__ x_perm, int4* __restrict__ mtile_table,
-                         int32_t* __restrict__ num_mtiles, int bm) {
+                         int32_t* __restrict__ num_mtiles, int bm,
+                         const float* __restrict__ gate_w, float* __restrict__ row_w) {
   extern __shared__ uint32_t smem_u[];
   uint32_t* masks = smem_u;                                        // [E][8]
   int* cnt = reinterpret_cast<int*>(masks + E * kSmallMaskWords);  // [E]
@@ -189,6 +192,7 @@ __global__ void __launch_bounds__(kSmallThreads)
   const int tid = threadIdx.x;
   const int TK = T * K;
   const int32_t* ids = ids_in;
+  const float* gates = gate_w;
   if constexpr (kRoute) {
     // routing of all T tokens (every block computes it; block 0 stores it): logits = sum
     // of the router's H-slice partials in slice order + bias, then the warp top-k
@@ -213,6 +217,7 @@ __global__ void __launch_bounds__(kSmallThreads)
         rt.w_out[i] = sw[i];
       }
     ids = sids;
+    gates = sw;
   }
   for (int i = tid; i < E * kSmallMaskWords; i += blockDim.x) masks[i] = 0u;
   __syncthreads();
@@ -255,7 +260,10 @@ __global__ void __launch_bounds__(kSmallThreads)
     for (int i = tid; i <= E; i += blockDim.x) offsets[i] = off[i];
     for (int a = tid; a < TK; a += blockDim.x) {
       inv[a] = rows[a];
-      if (rows[a] >= 0) perm[rows[a]] = a / K;
+      if (rows[a] >= 0) {
+        perm[rows[a]] = a / K;
+        if (row_w != nullptr) row_w[rows[a]] = gates[a];
+      }
     }
     if (mtile_table != nullptr) {
       const int nt = tid < E ? (cnt[tid] + bm - 1) / bm : 0;
@@ -293,7 +301,8 @@ template <bool kRoute>
 cudaError_t launch_small_t(int dtype, const void* x, const int32_t* ids, const SmallRoute* rt,
                            int T, int H, int E, int K, int32_t* counts, int32_t* offsets,
                            int32_t* perm, int32_t* inv, void* x_perm, int4* mtile_table,
-                           int32_t* num_mtiles, int bm, cudaStream_t s) {
+                           int32_t* num_mtiles, int bm, const float* gate_w, float* row_w,
+                           cudaStream_t s) {
   static int attr_dev = -1;  // opt in to more than 48 KB of dynamic shared memory once
   int dev = 0;
   cudaGetDevice(&dev);
@@ -314,18 +323,19 @@ cudaError_t launch_small_t(int dtype, const void* x, const int32_t* ids, const S
   return launch_pdl(permute_small_kernel<kRoute>, dim3(blocks), dim3(kSmallThreads), smem, s, ids,
                     r, T, E, K, row_units, counts, offsets, perm, inv,
                     static_cast<const uint4*>(x), static_cast<uint4*>(x_perm), mtile_table,
-                    num_mtiles, bm);
+                    num_mtiles, bm, gate_w, row_w);
 }
 
 cudaError_t launch_small(int dtype, const void* x, const int32_t* ids, const SmallRoute* rt,
                          int T, int H, int E, int K, int32_t* counts, int32_t* offsets,
                          int32_t* perm, int32_t* inv, void* x_perm, int4* mtile_table,
-                         int32_t* num_mtiles, int bm, cudaStream_t s) {
+                         int32_t* num_mtiles, int bm, const float* gate_w, float* row_w,
+                         cudaStream_t s) {
   if (rt != nullptr)
     return launch_small_t<true>(dtype, x, ids, rt, T, H, E, K, counts, offsets, perm, inv, x_perm,
-                                mtile_table, num_mtiles, bm, s);
+                                mtile_table, num_mtiles, bm, gate_w, row_w, s);
   return launch_small_t<false>(dtype, x, ids, rt, T, H, E, K, counts, offsets, perm, inv, x_perm,
-                               mtile_table, num_mtiles, bm, s);
+                               mtile_table, num_mtiles, bm, gate_w, row_w, s);
 }
 
 }  // namespace
@@ -339,10 +349,10 @@ cudaError_t launch_topk_permute_small(const float* partial, int S, const float* 
                                       int dtype, const void* x, int T, int H, int E, int K,
                                       int32_t* counts, int32_t* offsets, int32_t* perm,
                                       int32_t* inv, void* x_perm, int4* mtile_table,
-                                      int32_t* num_mtiles, int bm, cudaStream_t s) {
+                                      int32_t* num_mtiles, int bm, float* row_w, cudaStream_t s) {
   SmallRoute rt{partial, S, bias, logits, ids, w, theta};
   return launch_small(dtype, x, nullptr, &rt, T, H, E, K, counts, offsets, perm, inv, x_perm,
-                      mtile_table, num_mtiles, bm, s);
+                      mtile_table, num_mtiles, bm, nullptr, row_w, s);
 }
 
 size_t permute_ws_words(int T, int E) {
@@ -353,10 +363,11 @@ size_t permute_ws_words(int T, int E) {
 cudaError_t launch_permute(int dtype, const void* x, const int32_t* ids, int T, int H, int E,
                            int K, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
                            void* x_perm, int32_t* ws_words, int4* mtile_table,
-                           int32_t* num_mtiles, int bm, cudaStream_t s) {
+                           int32_t* num_mtiles, int bm, const float* gate_w, float* row_w,
+                           cudaStream_t s) {
   if (T > 0 && T <= kSmallMaxT)
     return launch_small(dtype, x, ids, nullptr, T, H, E, K, counts, offsets, perm, inv, x_perm,
-                        mtile_table, num_mtiles, bm, s);
+                        mtile_table, num_mtiles, bm, gate_w, row_w, s);
   const int nb = (T + kRankTokens - 1) / kRankTokens;
   if (nb > 0) {
     cudaError_t err = launch_pdl(permute_rank_kernel, dim3(nb), dim3(kRankTokens),
@@ -370,7 +381,7 @@ cudaError_t launch_permute(int dtype, const void* x, const int32_t* ids, int T, 
   return launch_pdl(permute_scatter_kernel, dim3((T + kScatterWarps - 1) / kScatterWarps),
                     dim3(kScatterWarps * 32), 0, s, ids, static_cast<const int32_t*>(ws_words), T,
                     E, K, row_units, inv, perm, static_cast<const uint4*>(x),
-                    static_cast<uint4*>(x_perm));
+                    static_cast<uint4*>(x_perm), gate_w, row_w);
 }
 
 cudaError_t launch_build_mtile_table(const int32_t* offsets, int E, int bm, int4* table,

@@ -89,7 +89,7 @@ extern "C" moe_status_t moe_permute_noalloc(const moe_config_t* cfg, const void*
   if (su != MOE_OK) return su;
   const cudaError_t e =
       launch_permute(cfg->dtype, x, topk_ids, cfg->T, cfg->H, cfg->E, cfg->K, counts, offsets,
-                     perm, inv, x_perm, scratch, nullptr, nullptr, 0,
+                     perm, inv, x_perm, scratch, nullptr, nullptr, 0, nullptr, nullptr,
                      static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

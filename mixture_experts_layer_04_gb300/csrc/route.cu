@@ -60,18 +60,33 @@ __global__ void __launch_bounds__(256, 3)
     router_wsmem_kernel(const TIn* __restrict__ x, const TIn* __restrict__ w_router,
                         const float* __restrict__ bias, float* __restrict__ logits,
                         int32_t* __restrict__ ids, float* __restrict__ w, int T, int H, int E,
-                        int K, float theta) {
+                        int K, float theta, unsigned* err) {
   extern __shared__ uint4 wsm[];  // [E][H] TIn, then 8 warps x kWsMaxE floats
+  __shared__ uint64_t wbar;
+  __shared__ int wfail;
   grid_dep_wait();
   grid_dep_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int V = Vec<TIn>::N;
   const int row_units = H / V;    // 16-byte units per row
   const int units = E * row_units;
-  const uint4* wg = reinterpret_cast<const uint4*>(w_router);
-  for (int i = threadIdx.x; i < units; i += blockDim.x) wsm[i] = __ldg(wg + i);
-  float* Ls = reinterpret_cast<float*>(wsm + units) + warp * kWsMaxE;
+  // W_r -> shared memory with one bulk copy (no chain of per-thread round trips)
+  const uint32_t bar = smem_u32(&wbar);
+  if (threadIdx.x == 0) {
+    wfail = 0;
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(units) * 16u);
+    bulk_copy_g2s(smem_u32(wsm), w_router, static_cast<uint32_t>(units) * 16u, bar);
+  }
   __syncthreads();
+  if (!mbar_wait(bar, 0, &wfail, nullptr)) wfail = 1;
+  __syncthreads();
+  if (wfail) {
+    if (threadIdx.x == 0) report_error(err, MOE_DEVERR_TIMEOUT);
+    return;
+  }
+  float* Ls = reinterpret_cast<float*>(wsm + units) + warp * kWsMaxE;
   for (int t = blockIdx.x * 8 + warp; t < T; t += gridDim.x * 8) {
     float acc[kWsMaxE];
 #pragma unroll
@@ -246,7 +261,7 @@ bool router_uses_wsmem(int dtype, int T, int H, int E) {
 
 cudaError_t launch_router_wsmem(int dtype, const void* x, const void* w_router,
                                 const float* bias, float* logits, int32_t* ids, float* w, int T,
-                                int H, int E, int K, float theta, cudaStream_t s) {
+                                int H, int E, int K, float theta, unsigned* err, cudaStream_t s) {
   const size_t smem = static_cast<size_t>(E) * H * act_bytes(dtype) + 8 * kWsMaxE * sizeof(float);
   static int attr_dev = -1;  // opt in to more than 48 KB of dynamic shared memory once
   int dev = 0;
@@ -267,10 +282,10 @@ cudaError_t launch_router_wsmem(int dtype, const void* x, const void* w_router,
     return launch_pdl(router_wsmem_kernel<__nv_bfloat16>, dim3(blocks), dim3(256), smem, s,
                       static_cast<const __nv_bfloat16*>(x),
                       static_cast<const __nv_bfloat16*>(w_router), bias, logits, ids, w, T, H, E,
-                      K, theta);
+                      K, theta, err);
   return launch_pdl(router_wsmem_kernel<float>, dim3(blocks), dim3(256), smem, s,
                     static_cast<const float*>(x), static_cast<const float*>(w_router), bias,
-                    logits, ids, w, T, H, E, K, theta);
+                    logits, ids, w, T, H, E, K, theta, err);
 }
 
 cudaError_t launch_router_partial(int dtype, const void* x, const void* w_router, float* partial,

@@ -103,14 +103,14 @@ def assert_close_y(got, want, max_abs=Y_MAX_ABS, rel_l2=Y_REL_L2, what="y"):
 class LayerRun:
     """Buffers and one moe_layer_forward call of a workload on the GPU."""
 
-    def __init__(self, moe, shape, inputs, T=None):
+    def __init__(self, moe, shape, inputs, T=None, flags=0):
         self.moe = moe
         self.shape = shape
         self.inp = inputs
         self.T = inputs["x"].shape[0] if T is None else T
         s = shape
         dt = moe.BF16 if s.dtype == "bf16" else moe.F32
-        self.cfg = moe.MoEConfig.make(self.T, s.H, s.E, s.K, s.I, s.I_shared, s.theta, dt)
+        self.cfg = moe.MoEConfig.make(self.T, s.H, s.E, s.K, s.I, s.I_shared, s.theta, dt, flags)
         self.ws = torch.empty(moe.workspace_size(self.cfg), dtype=torch.uint8, device="cuda")
         self.y = torch.empty(self.T, s.H, dtype=s.torch_dtype, device="cuda")
         self.y32 = torch.empty(self.T, s.H, dtype=torch.float32, device="cuda")

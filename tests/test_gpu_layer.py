@@ -83,10 +83,11 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("fused", [False, True], ids=["gather_combine", "fused_combine"])
 @pytest.mark.parametrize("shape", SMALL, ids=lambda s: s.name)
-def test_layer_small_full_oracle(moe, shape):
+def test_layer_small_full_oracle(moe, shape, fused):
     inp = synth.make_inputs(shape, device="cuda")
-    run = H.LayerRun(moe, shape, inp)
+    run = H.LayerRun(moe, shape, inp, flags=moe.FLAG_FUSED_COMBINE if fused else 0)
     run.run()
     moe.sync_check()
     r = run.routing()
@@ -127,11 +128,12 @@ FULL = [
 ]
 
 
+@pytest.mark.parametrize("fused", [False, True], ids=["gather_combine", "fused_combine"])
 @pytest.mark.parametrize("name,T,nsample", FULL, ids=[f"{n}-{t}" for n, t, _ in FULL])
-def test_layer_full_size_sampled(moe, name, T, nsample):
+def test_layer_full_size_sampled(moe, name, T, nsample, fused):
     shape = synth.WORKLOADS[name]
     inp = synth.make_inputs(shape, device="cuda", T=T)
-    run = H.LayerRun(moe, shape, inp)
+    run = H.LayerRun(moe, shape, inp, flags=moe.FLAG_FUSED_COMBINE if fused else 0)
     run.run()
     moe.sync_check()
     Tn = run.T
@@ -162,6 +164,21 @@ def test_layer_full_size_sampled(moe, name, T, nsample):
     y32 = run.y32.double().cpu().numpy()[toks]
     H.assert_close_y(y32, ref["y"], **_tol(shape))
     assert torch.equal(run.y, run.y32.to(shape.torch_dtype))
+
+
+def test_fused_combine_matches_gather_combine(moe):
+    """The fused combine differs from the deterministic gather only by fp32 rounding order."""
+    shape = synth.MoEShape("fc", T=1500, H=512, E=64, K=8, I=256, I_shared=128, theta=0.05,
+                           bias="zipf", seed=9)
+    inp = synth.make_inputs(shape, device="cuda")
+    a = H.LayerRun(moe, shape, inp)
+    b = H.LayerRun(moe, shape, inp, flags=moe.FLAG_FUSED_COMBINE)
+    a.run()
+    b.run()
+    torch.cuda.synchronize()
+    d = (a.y32 - b.y32).abs().max().item()
+    assert d <= 1e-5 * max(1.0, a.y32.abs().max().item())
+    assert torch.equal(b.y, b.y32.to(torch.bfloat16))
 
 
 def test_deterministic(moe):
