@@ -5,8 +5,9 @@
 
 A step is one moe_layer_forward over one batch of synthetic tokens (router, top-k,
 gate drop, permutation, grouped SwiGLU FFN, shared expert, combine).  Timing: CUDA
-events on the launching stream around each step, with an L2 flush (a 512 MiB write)
-between steps outside the events; W untimed warm-up steps; max over ranks.  With
+events on the launching stream around each step, with an L2 flush between steps outside
+the events (a 512 MiB write, then a 512 MiB read of another buffer, so the previous
+step's data is evicted and no dirty lines are left behind); W untimed warm-up steps; max over ranks.  With
 N > 1 (torchrun) every rank runs an independent replica on its own GPU (the layer has
 no exchange step on one GPU): weak scaling, value = all tokens / slowest rank's time.
 
@@ -189,6 +190,13 @@ def run_ours(args, rank, world, local):
     ws = torch.empty(moe.workspace_size(cfg), dtype=torch.uint8, device=dev)
     y = torch.empty(T, shape.H, dtype=shape.torch_dtype, device=dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_rd = torch.zeros(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        # write a buffer larger than L2, then read another one: the inputs of the previous
+        # step are evicted and no dirty lines are left for the timed kernels to write back
+        flush.zero_()
+        flush_rd.sum()
     stream = torch.cuda.current_stream(dev)
 
     def step():
@@ -200,7 +208,7 @@ def run_ours(args, rank, world, local):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(n)]
         for a, b in evs:
-            flush.zero_()
+            flush_l2()
             a.record(stream)
             fn()
             b.record(stream)
@@ -208,7 +216,7 @@ def run_ours(args, rank, world, local):
         return [a.elapsed_time(b) for a, b in evs]
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2()
         step()
     moe.sync_check(stream)
 
@@ -224,7 +232,7 @@ def run_ours(args, rank, world, local):
                               y, None, ws, stream=torch.cuda.current_stream(dev))
         layer_step = graph.replay
         for _ in range(3):
-            flush.zero_()
+            flush_l2()
             layer_step()
         torch.cuda.synchronize(dev)
 
@@ -348,7 +356,7 @@ def run_ours(args, rank, world, local):
         "data": "synthetic (seeded; x~N(0,1), W_r~N(0,1/H), expert W~N(0,0.02))",
         "config": {"workload": args.config, "T": T, "H": shape.H, "E": shape.E, "K": shape.K,
                    "I": shape.I, "I_shared": shape.I_shared, "theta": shape.theta,
-                   "router_bias": shape.bias, "l2": "flushed between steps (512 MiB write)",
+                   "router_bias": shape.bias, "l2": "flushed between steps: 512 MiB write, then 512 MiB read of another buffer",
                    "parallelism": "replicas" if world > 1 else "single-gpu",
                    "cuda_graph": bool(use_graph),
                    "combine": "fused scatter-add (fp32, order not fixed)" if fused else "gather (deterministic)",

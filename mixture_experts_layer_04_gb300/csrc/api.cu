@@ -202,12 +202,16 @@ struct Groups {
 // Decode-sized batches: with at most kSwapMaxTokens tokens no group can have more rows
 // than that, so the tensor-core GEMMs put the weights on the 128-row side of the MMA.
 constexpr int kSwapMaxTokens = 128;
+constexpr int kPairMinRowsPerGroup = 768;
 
 moe_status_t launch_gemm(const moe_config_t* c, const DeviceInfo* d, const GroupedGemm& g0,
                          cudaStream_t s) {
   if (c->dtype == MOE_BF16) {
     GroupedGemm g = g0;
     g.swap_tokens = c->T <= kSwapMaxTokens ? c->T : 0;
+    // large groups (>= 768 rows on average) run on CTA pairs with 256-row tiles; smaller,
+    // ragged groups keep 128-row tiles (less padding in each group's last tile)
+    g.pair = (g.swap_tokens == 0 && g.rows_alloc >= kPairMinRowsPerGroup * g.G) ? 1 : 0;
     return cuda_status(launch_grouped_gemm_tc(g, d->err, d->num_sms, s));
   }
   return cuda_status(launch_grouped_gemm_simt(g0, s));

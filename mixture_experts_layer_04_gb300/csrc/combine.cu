@@ -27,14 +27,57 @@ __device__ __forceinline__ void store4(__nv_bfloat16* y, size_t i, float4 v) {
   reinterpret_cast<uint2*>(y)[i] = u;
 }
 
-// Block (t, by): token t, columns [512 by, 512 by + 512) -- one float4 per thread, so
-// small batches still spread over many blocks and each thread's K row loads are issued
-// together.
+// Many tokens: one block per token walks its row, four columns per thread per step.
 template <typename TOut>
 __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(const float* __restrict__ out_perm, const int32_t* __restrict__ inv,
                    const float* __restrict__ w, const float* __restrict__ shared_out,
                    TOut* __restrict__ y, float* __restrict__ y_f32, int H, int K) {
+  __shared__ int rows[kMaxK];
+  __shared__ float gates[kMaxK];
+  grid_dep_wait();
+  grid_dep_trigger();
+  const int t = blockIdx.x;
+  if (threadIdx.x < K) {
+    rows[threadIdx.x] = inv[static_cast<size_t>(t) * K + threadIdx.x];
+    gates[threadIdx.x] = w[static_cast<size_t>(t) * K + threadIdx.x];
+  }
+  __syncthreads();
+  const int H4 = H / 4;
+  const float4* o4 = reinterpret_cast<const float4*>(out_perm);
+  for (int c = threadIdx.x; c < H4; c += kCombineThreads) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < K; ++k) {
+      const int r = rows[k];
+      if (r < 0) continue;
+      const float g = gates[k];
+      const float4 v = o4[static_cast<size_t>(r) * H4 + c];
+      acc.x = fmaf(g, v.x, acc.x);
+      acc.y = fmaf(g, v.y, acc.y);
+      acc.z = fmaf(g, v.z, acc.z);
+      acc.w = fmaf(g, v.w, acc.w);
+    }
+    if (shared_out != nullptr) {
+      const float4 sv = reinterpret_cast<const float4*>(shared_out)[static_cast<size_t>(t) * H4 + c];
+      acc.x += sv.x;
+      acc.y += sv.y;
+      acc.z += sv.z;
+      acc.w += sv.w;
+    }
+    const size_t i = static_cast<size_t>(t) * H4 + c;
+    store4(y, i, acc);
+    if (y_f32 != nullptr) reinterpret_cast<float4*>(y_f32)[i] = acc;
+  }
+}
+
+// Few tokens: block (t, by) handles token t's columns [512 by, 512 by + 512), one float4
+// per thread with its K row loads issued together, so a small batch still spreads over
+// many blocks.  Same arithmetic (fp32, slot order) as combine_kernel.
+template <typename TOut>
+__global__ void __launch_bounds__(kCombineThreads)
+    combine_split_kernel(const float* __restrict__ out_perm, const int32_t* __restrict__ inv,
+                         const float* __restrict__ w, const float* __restrict__ shared_out,
+                         TOut* __restrict__ y, float* __restrict__ y_f32, int H, int K) {
   __shared__ int rows[kMaxK];
   __shared__ float gates[kMaxK];
   grid_dep_wait();
@@ -104,11 +147,18 @@ cudaError_t launch_combine(int dtype, const float* out_perm, const int32_t* inv,
                            const float* shared_out, void* y, float* y_f32, int T, int H, int K,
                            cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  const dim3 grid(T, (H / 4 + kCombineThreads - 1) / kCombineThreads);
+  if (T < 1024) {  // few tokens: spread each token's columns over several blocks
+    const dim3 grid(T, (H / 4 + kCombineThreads - 1) / kCombineThreads);
+    if (dtype == kBF16)
+      return launch_pdl(combine_split_kernel<__nv_bfloat16>, grid, dim3(kCombineThreads), 0, s,
+                        out_perm, inv, w, shared_out, static_cast<__nv_bfloat16*>(y), y_f32, H, K);
+    return launch_pdl(combine_split_kernel<float>, grid, dim3(kCombineThreads), 0, s, out_perm,
+                      inv, w, shared_out, static_cast<float*>(y), y_f32, H, K);
+  }
   if (dtype == kBF16)
-    return launch_pdl(combine_kernel<__nv_bfloat16>, grid, dim3(kCombineThreads), 0, s, out_perm,
-                      inv, w, shared_out, static_cast<__nv_bfloat16*>(y), y_f32, H, K);
-  return launch_pdl(combine_kernel<float>, grid, dim3(kCombineThreads), 0, s, out_perm, inv, w,
+    return launch_pdl(combine_kernel<__nv_bfloat16>, dim3(T), dim3(kCombineThreads), 0, s,
+                      out_perm, inv, w, shared_out, static_cast<__nv_bfloat16*>(y), y_f32, H, K);
+  return launch_pdl(combine_kernel<float>, dim3(T), dim3(kCombineThreads), 0, s, out_perm, inv, w,
                     shared_out, static_cast<float*>(y), y_f32, H, K);
 }
 

@@ -183,6 +183,96 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[32]) {
   }
 }
 
+// Epilogue of one accumulator tile in the normal operand order.  This warp owns the 32
+// TMEM lanes at t_row (token rows tile_row0 .. tile_row0+31 of A, stored when < row_end);
+// accumulator column j is output feature col0 + j (SwiGLU: columns BN/2 + j hold the up
+// half).  `stg` is this warp's staging buffer in shared memory.
+template <int BN, int MODE>
+__device__ __forceinline__ void epilogue_rows(const TcParams& p, uint32_t t_row, uint32_t stg,
+                                              int lane, int tile_row0, int row_end, int col0) {
+  if constexpr (MODE == kSwiGLU) {
+    __nv_bfloat16* C = static_cast<__nv_bfloat16*>(p.C);
+#pragma unroll 1
+    for (int c = 0; c < BN / 2; c += 32) {
+      uint32_t gr[32], ur[32];
+      tmem_ld_32x32b_x32(t_row + c, gr);
+      tmem_ld_32x32b_x32(t_row + BN / 2 + c, ur);
+      tmem_ld_wait();
+      uint32_t pk[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float h0 = silu_f(__uint_as_float(gr[2 * j])) * __uint_as_float(ur[2 * j]);
+        const float h1 =
+            silu_f(__uint_as_float(gr[2 * j + 1])) * __uint_as_float(ur[2 * j + 1]);
+        pk[j] = pack_bf16x2(h0, h1);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        st_shared_v4(stg + stg_off<64>(lane, u), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2],
+                     pk[4 * u + 3]);
+      __syncwarp();
+#pragma unroll
+      for (int pass = 0; pass < 4; ++pass) {
+        const int rr = pass * 8 + (lane >> 2), u = lane & 3;
+        const uint4 v = ld_shared_v4(stg + stg_off<64>(rr, u));
+        const int grow = tile_row0 + rr;
+        const int col = col0 + c + u * 8;
+        if (grow < row_end && col < p.N_out)
+          *reinterpret_cast<uint4*>(C + static_cast<size_t>(grow) * p.N_out + col) = v;
+      }
+      __syncwarp();
+    }
+  } else {
+    float* C = static_cast<float*>(p.C);
+    // kScatter: this thread's row is scaled by its route weight and added into the
+    // output row of its token (the fused combine); other rows are stored as they are
+    float rw = 1.f;
+    if constexpr (MODE == kScatter) {
+      const int grow = tile_row0 + lane;
+      rw = grow < row_end ? __ldg(p.row_w + grow) : 0.f;
+    }
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(t_row + c, r);
+      tmem_ld_wait();
+      if constexpr (MODE == kScatter) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * rw);
+      }
+      if (p.col_bias != nullptr) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int col = col0 + c + j;
+          const float b = col < p.N_out ? __ldg(p.col_bias + col) : 0.f;
+          r[j] = __float_as_uint(__uint_as_float(r[j]) + b);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        st_shared_v4(stg + stg_off<128>(lane, u), r[4 * u], r[4 * u + 1], r[4 * u + 2],
+                     r[4 * u + 3]);
+      __syncwarp();
+#pragma unroll
+      for (int pass = 0; pass < 8; ++pass) {
+        const int rr = pass * 4 + (lane >> 3), u = lane & 7;
+        const uint4 v = ld_shared_v4(stg + stg_off<128>(rr, u));
+        const int grow = tile_row0 + rr;
+        const int col = col0 + c + u * 4;
+        if (grow < row_end && col < p.N_out) {
+          if constexpr (MODE == kScatter) {
+            const int tok = __ldg(p.row_token + grow);
+            red_add_v4(C + static_cast<size_t>(tok) * p.N_out + col, v);
+          } else {
+            *reinterpret_cast<uint4*>(C + static_cast<size_t>(grow) * p.N_out + col) = v;
+          }
+        }
+      }
+      __syncwarp();
+    }
+  }
+}
+
 template <int BN, int MODE, bool SWAP>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_grouped_gemm_kernel(const __grid_constant__ TcParams p) {
@@ -381,87 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t stg =
             smem_u32(sStg) + static_cast<uint32_t>((warp - 2) * 32 * (MODE == kSwiGLU ? 64 : 128));
         const int tile_row0 = row0 + quad * 32;  // first global row of this warp's 32 rows
-        if constexpr (MODE == kSwiGLU) {
-          __nv_bfloat16* C = static_cast<__nv_bfloat16*>(p.C);
-#pragma unroll 1
-          for (int c = 0; c < BN / 2; c += 32) {
-            uint32_t gr[32], ur[32];
-            tmem_ld_32x32b_x32(t_row + c, gr);
-            tmem_ld_32x32b_x32(t_row + BN / 2 + c, ur);
-            tmem_ld_wait();
-            uint32_t pk[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float h0 = silu_f(__uint_as_float(gr[2 * j])) * __uint_as_float(ur[2 * j]);
-              const float h1 =
-                  silu_f(__uint_as_float(gr[2 * j + 1])) * __uint_as_float(ur[2 * j + 1]);
-              pk[j] = pack_bf16x2(h0, h1);
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              st_shared_v4(stg + stg_off<64>(lane, u), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2],
-                           pk[4 * u + 3]);
-            __syncwarp();
-#pragma unroll
-            for (int pass = 0; pass < 4; ++pass) {
-              const int rr = pass * 8 + (lane >> 2), u = lane & 3;
-              const uint4 v = ld_shared_v4(stg + stg_off<64>(rr, u));
-              const int grow = tile_row0 + rr;
-              const int col = col0 + c + u * 8;
-              if (grow < row_end && col < p.N_out)
-                *reinterpret_cast<uint4*>(C + static_cast<size_t>(grow) * p.N_out + col) = v;
-            }
-            __syncwarp();
-          }
-        } else {
-          float* C = static_cast<float*>(p.C);
-          // kScatter: this thread's row is scaled by its route weight and added into the
-          // output row of its token (the fused combine); other rows are stored as they are
-          float rw = 1.f;
-          if constexpr (MODE == kScatter) {
-            const int grow = tile_row0 + lane;
-            rw = grow < row_end ? __ldg(p.row_w + grow) : 0.f;
-          }
-#pragma unroll 1
-          for (int c = 0; c < BN; c += 32) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(t_row + c, r);
-            tmem_ld_wait();
-            if constexpr (MODE == kScatter) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * rw);
-            }
-            if (p.col_bias != nullptr) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const int col = col0 + c + j;
-                const float b = col < p.N_out ? __ldg(p.col_bias + col) : 0.f;
-                r[j] = __float_as_uint(__uint_as_float(r[j]) + b);
-              }
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-              st_shared_v4(stg + stg_off<128>(lane, u), r[4 * u], r[4 * u + 1], r[4 * u + 2],
-                           r[4 * u + 3]);
-            __syncwarp();
-#pragma unroll
-            for (int pass = 0; pass < 8; ++pass) {
-              const int rr = pass * 4 + (lane >> 3), u = lane & 7;
-              const uint4 v = ld_shared_v4(stg + stg_off<128>(rr, u));
-              const int grow = tile_row0 + rr;
-              const int col = col0 + c + u * 4;
-              if (grow < row_end && col < p.N_out) {
-                if constexpr (MODE == kScatter) {
-                  const int tok = __ldg(p.row_token + grow);
-                  red_add_v4(C + static_cast<size_t>(tok) * p.N_out + col, v);
-                } else {
-                  *reinterpret_cast<uint4*>(C + static_cast<size_t>(grow) * p.N_out + col) = v;
-                }
-              }
-            }
-            __syncwarp();
-          }
-        }
+        epilogue_rows<BN, MODE>(p, t_row, stg, lane, tile_row0, row_end, col0);
       } else {
         // swapped: lane = weight row of the tile, column j = token row0 + j
         if constexpr (MODE == kSwiGLU) {
@@ -532,6 +542,234 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, Cfg::kTmemCols);
+}
+
+
+// ------------------------------------------------------ CTA pairs (2 SMs) ----
+// The same grouped GEMM on pairs of CTAs (a cluster of 2) with tcgen05.mma.cta_group::2:
+// one 256 x 256 accumulator tile per pair, rows 0-127 in the even CTA's TMEM and 128-255
+// in the odd CTA's.  Each CTA loads its own 128 rows of A and one half of the 256 B rows
+// (SwiGLU: the even CTA the 128 gate rows, the odd CTA the matching 128 up rows), so a
+// stage is 32 KB per CTA and 6 stages fit; per SM the L2->shared traffic per MMA FLOP is
+// two thirds of the single-CTA kernel's.
+//   * both CTAs' TMA loads complete on the even CTA's full barrier (cta_group::2 loads);
+//   * the even CTA's single MMA thread issues the pair MMAs and commits with a multicast
+//     arrive on both CTAs' empty (per stage) and tmem-full (per accumulator) barriers;
+//   * both CTAs' epilogue warps arrive on the even CTA's tmem-empty barrier (count 8);
+//   * a cluster barrier after initialisation and before TMEM release keeps every
+//     remote arrive and shared-memory read inside the peer's lifetime.
+template <int MODE>
+struct TcPairCfg {
+  static constexpr int kABytes = 128 * BK * 2;  // this CTA's 128 rows of A
+  static constexpr int kBBytes = 128 * BK * 2;  // this CTA's half of the 256 B rows
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = 6;
+  static constexpr int kBN = 256;  // MMA N over the pair
+  static constexpr int kColsOut = MODE == kSwiGLU ? 128 : 256;
+  static constexpr int kTmemCols = 512;
+  static constexpr int kStgBytes = kEpiWarps * 32 * (MODE == kSwiGLU ? 64 : 128);
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSchedBytes = 2 * (kMaxGroups + 4) * 4 + 32 * 4;
+  static constexpr int kSmem = 1024 + kStages * kStageBytes + kStgBytes + kBarBytes + kSchedBytes;
+  static_assert(kSmem <= 232448, "shared memory per CTA");
+};
+
+template <int MODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    tc_pair_gemm_kernel(const __grid_constant__ TcParams p) {
+  using Cfg = TcPairCfg<MODE>;
+  constexpr int S = Cfg::kStages;
+  constexpr int BN = Cfg::kBN;
+  constexpr int kTileRows = 256;  // token rows per pair tile
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + S * Cfg::kABytes;
+  uint8_t* sStg = sB + S * Cfg::kBBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + Cfg::kStgBytes);
+  // bars: full[S], empty[S], tfull[2], tempty[2], mma_done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* s_off = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(bars) + Cfg::kBarBytes);
+  int* s_mt = s_off + kMaxGroups + 4;
+  int* s_scan = s_mt + kMaxGroups + 4;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
+  const uint32_t mma_done_bar = bar0 + 8u * (2 * S + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 2 * kEpiWarps);
+    }
+    mbar_init(mma_done_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&p.tmAct);
+    tma_prefetch_desc(&p.tmWgt);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), Cfg::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // the peer's barriers exist before anything arrives on them
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  grid_dep_wait();
+  grid_dep_trigger();
+
+  int num_mt;
+  if (p.offsets != nullptr) {
+    const int G = p.num_groups;
+    for (int i = threadIdx.x; i <= G; i += blockDim.x) s_off[i] = p.offsets[i];
+    __syncthreads();
+    const int per = (G + blockDim.x - 1) / blockDim.x;
+    const int beg = min(G, static_cast<int>(threadIdx.x) * per), end = min(G, beg + per);
+    int mine = 0;
+    for (int q = beg; q < end; ++q) mine += (s_off[q + 1] - s_off[q] + kTileRows - 1) / kTileRows;
+    int all = 0;
+    int run = block_exclusive_scan(mine, s_scan, &all);
+    for (int q = beg; q < end; ++q) {
+      s_mt[q] = run;
+      run += (s_off[q + 1] - s_off[q] + kTileRows - 1) / kTileRows;
+    }
+    if (threadIdx.x == 0) s_mt[G] = all;
+    __syncthreads();
+    num_mt = all;
+  } else {
+    num_mt = (p.rows_alloc + kTileRows - 1) / kTileRows;
+  }
+  const int total = num_mt * p.n_tiles;
+  const int pair = static_cast<int>(blockIdx.x >> 1), npairs = static_cast<int>(gridDim.x >> 1);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer ----
+    if (elect_one_sync()) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (int idx = pair; idx < total && ok; idx += npairs) {
+        int g, row0, row_end, n_tile;
+        decode_tile(p, s_off, s_mt, num_mt, kTileRows, idx, g, row0, row_end, n_tile);
+        const int n0 = n_tile * Cfg::kColsOut;
+        const int a_row = row0 + static_cast<int>(rank) * 128;
+        const int b_row = MODE == kSwiGLU ? (rank == 0 ? n0 : p.up_offset + n0)
+                                          : n0 + static_cast<int>(rank) * 128;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb_leader = mapa_shared(full_bar(stage), 0);
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * Cfg::kStageBytes);
+          tma_load_2d_pair(smem_u32(sA + stage * Cfg::kABytes), &p.tmAct, fb_leader, kb * BK, a_row);
+          tma_load_3d_pair(smem_u32(sB + stage * Cfg::kBBytes), &p.tmWgt, fb_leader, kb * BK, b_row, g);
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (rank == 0) {
+        // Drain: both CTAs' loads complete on the even CTA's full barriers.
+        const int n = issued < S ? static_cast<int>(issued) : S;
+        int s = stage;
+        uint32_t ph = phase;
+        volatile int no_abort = 0;
+        for (int j = 0; j < n; ++j) {
+          if (--s < 0) {
+            s = S - 1;
+            ph ^= 1u;
+          }
+          mbar_wait(full_bar(s), ph, &no_abort, p.err);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA ----
+    if (rank == 0 && elect_one_sync()) {
+      constexpr uint32_t idesc = idesc_bf16_f32(256, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool ok = true;
+      for (int idx = pair; idx < total && ok; idx += npairs, ++local) {
+        const int acc = local & 1;
+        const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
+        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.err)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + stage * Cfg::kABytes);
+          const uint32_t b_base = smem_u32(sB + stage * Cfg::kBBytes);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc_mma_bf16_pair(d_tmem, smem_desc_sw128(a_base + kk * 32),
+                             smem_desc_sw128(b_base + kk * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
+          tc_commit_pair(empty_bar(stage), 0x3);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) tc_commit_pair(tfull_bar(acc), 0x3);
+      }
+      if (!ok || *abort_flag) {
+        tc_commit_pair(mma_done_bar, 0x1);
+        volatile int no_abort = 0;
+        mbar_wait(mma_done_bar, 0, &no_abort, p.err);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue ----
+    const int quad = warp & 3;
+    const uint32_t stg =
+        smem_u32(sStg) + static_cast<uint32_t>((warp - 2) * 32 * (MODE == kSwiGLU ? 64 : 128));
+    int local = 0;
+    for (int idx = pair; idx < total; idx += npairs, ++local) {
+      int g, row0, row_end, n_tile;
+      decode_tile(p, s_off, s_mt, num_mt, kTileRows, idx, g, row0, row_end, n_tile);
+      const int acc = local & 1;
+      const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
+      if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.err)) break;
+      tc_fence_after();
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                             static_cast<uint32_t>(acc * BN);
+      const int tile_row0 = row0 + static_cast<int>(rank) * 128 + quad * 32;
+      epilogue_rows<BN, MODE>(p, t_row, stg, lane, tile_row0, row_end, n_tile * Cfg::kColsOut);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // no peer still reads this CTA's shared memory or arrives on it
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
 }
 
 // ------------------------------------------------------------------ host ----
@@ -618,6 +856,49 @@ cudaError_t launch_one(const GroupedGemm& g, unsigned* err, int num_sms, cudaStr
                     dim3(kThreads), Cfg::kSmem, s, p);
 }
 
+
+template <int MODE>
+cudaError_t launch_pair(const GroupedGemm& g, unsigned* err, int num_sms, cudaStream_t s) {
+  using Cfg = TcPairCfg<MODE>;
+  auto kernel = tc_pair_gemm_kernel<MODE>;
+  static int attr_set_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (attr_set_dev != dev) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set_dev = dev;
+  }
+  TcParams p;
+  memset(&p, 0, sizeof(p));
+  if (!make_map_2d(&p.tmAct, g.A, static_cast<uint64_t>(g.rows_alloc), static_cast<uint64_t>(g.Kd),
+                   128))
+    return cudaErrorInvalidValue;
+  if (!make_map_3d(&p.tmWgt, g.B, static_cast<uint64_t>(g.G), static_cast<uint64_t>(g.Nb),
+                   static_cast<uint64_t>(g.Kd), 128))
+    return cudaErrorInvalidValue;
+  p.C = g.C;
+  p.col_bias = g.col_bias;
+  p.offsets = g.offsets;
+  p.row_token = g.row_token;
+  p.row_w = g.row_w;
+  p.num_groups = g.G;
+  p.err = err;
+  p.rows_alloc = g.rows_alloc;
+  p.num_kb = g.Kd / BK;
+  p.N_out = g.N_out;
+  p.n_tiles = (g.N_out + Cfg::kColsOut - 1) / Cfg::kColsOut;
+  p.up_offset = g.up_offset;
+  p.swz = kSwz;
+  const long long rows_tiles = (g.rows_alloc + 255) / 256;
+  const long long max_mt = g.offsets != nullptr ? rows_tiles + g.G : rows_tiles;
+  const long long max_tiles = max_mt * p.n_tiles;
+  if (max_tiles == 0) return cudaSuccess;
+  const long long pairs = max_tiles < num_sms / 2 ? max_tiles : num_sms / 2;
+  return launch_pdl(kernel, dim3(static_cast<unsigned>(2 * pairs)), dim3(kThreads), Cfg::kSmem, s,
+                    p);
+}
 }  // namespace
 
 int tc_swap_tokens(int max_rows_per_group) {
@@ -645,6 +926,11 @@ cudaError_t launch_grouped_gemm_tc(const GroupedGemm& g, unsigned* err, int num_
     if (bt == 16) return launch_one<16, kPlain, true>(g, err, num_sms, s);
     if (bt == 32) return launch_one<32, kPlain, true>(g, err, num_sms, s);
     return launch_one<64, kPlain, true>(g, err, num_sms, s);
+  }
+  if (g.pair) {
+    if (g.mode == kSwiGLU) return launch_pair<kSwiGLU>(g, err, num_sms, s);
+    if (g.mode == kScatter) return launch_pair<kScatter>(g, err, num_sms, s);
+    if (g.N_out > 128) return launch_pair<kPlain>(g, err, num_sms, s);
   }
   if (g.mode == kScatter) return launch_one<256, kScatter, false>(g, err, num_sms, s);
   if (g.mode == kSwiGLU) return launch_one<256, kSwiGLU, false>(g, err, num_sms, s);

@@ -136,6 +136,8 @@ struct GroupedGemm {
   int swap_tokens;
   const int32_t* row_token;  // kScatter only
   const float* row_w;        // kScatter only
+  // Tensor-core engine, normal order only: run on CTA pairs (cta_group::2, 256-row tiles)
+  int pair;
 };
 
 cudaError_t launch_grouped_gemm_simt(const GroupedGemm& g, cudaStream_t s);
