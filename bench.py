@@ -40,6 +40,9 @@ import torch  # noqa: E402
 import synth  # noqa: E402
 
 FLUSH_BYTES = 512 << 20
+PROFILES_DIR = os.path.join(ROOT, "profiles")
+KERNEL_SOURCES = [os.path.join(ROOT, "mixture_experts_layer_04_gb300", "csrc", f)
+                  for f in ("gemm_tc.cu", "common.cuh")]
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -132,6 +135,28 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def recorded_traffic(workload, kernel):
+    """DRAM bytes per launch of `kernel` on `workload` from a committed ncu summary under
+    profiles/, or None when there is none or the kernel sources changed since it was taken
+    (the summary records a hash of the kernel sources)."""
+    import glob
+    import hashlib
+    import re
+
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    digest = h.hexdigest()[:16]
+    pat = re.compile(r"traffic: workload=(\S+) kernel=(\S+) bytes_per_launch=(\d+) source_sha256=(\w+)")
+    for path in sorted(glob.glob(os.path.join(PROFILES_DIR, "*.md"))):
+        with open(path) as fh:
+            for m in pat.finditer(fh.read()):
+                if m.group(1) == workload and m.group(2) == kernel and m.group(4) == digest:
+                    return int(m.group(3))
+    return None
 
 
 def kernel_launches_per_step(shape, T):
@@ -310,7 +335,8 @@ def run_ours(args, rank, world, local):
         achieved = alg["gate_up_flops"] / gu_s / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4)}
-    roof["traffic"] = None
+    roof["traffic"] = recorded_traffic(args.config if args.tokens is None else
+                                       f"{args.config}-T{T}", "gate_up")
     roof["kernel"] = "tc_grouped_gemm_kernel<256,SwiGLU> (moe_expert_gate_up)"
     roof["peak_source"] = peak_kind
 

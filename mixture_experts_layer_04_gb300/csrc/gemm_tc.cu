@@ -52,7 +52,7 @@ namespace {
 constexpr int BK = 64;  // bf16 elements = 128 bytes = one swizzle row
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
-constexpr int kSwz = 8;
+constexpr int kSwz = 16;  // token tiles per raster chunk
 constexpr int kMaxGroups = 1024;
 
 struct TcParams {
@@ -97,27 +97,39 @@ struct TcCfg {
 
 // Tile idx -> (group g, token rows row0..row_end-1, weight tile n_tile).  s_off holds the
 // group row offsets and s_mt the exclusive prefix of token tiles per group.
+// Order: groups one after another; inside a group, chunks of up to `swz` token tiles, and
+// inside a chunk the weight tiles outer, token tiles inner.  CTAs running at the same time
+// thus share a weight tile (read once from HBM) and keep a chunk's token rows in L2 while
+// they sweep the weight tiles, and no chunk mixes two groups' weights.
 __device__ __forceinline__ void decode_tile(const TcParams& p, const int* s_off, const int* s_mt,
                                             int num_mt, int tile_rows, int idx, int& g, int& row0,
                                             int& row_end, int& n_tile) {
-  const int gsz = p.swz * p.n_tiles;
-  const int grp = idx / gsz;
-  const int rem = idx - grp * gsz;
-  const int m_first = grp * p.swz;
-  const int m_cnt = min(p.swz, num_mt - m_first);
-  n_tile = rem / m_cnt;
-  const int mt = m_first + (rem - n_tile * m_cnt);
+  const int nt = p.n_tiles;
+  int mt;  // token tile index inside its group
   if (p.offsets != nullptr) {
-    int lo = 0, hi = p.num_groups - 1;  // last group with s_mt[g] <= mt
+    const int mi = idx / nt;  // the group holding tile idx: s_mt[g] * nt <= idx
+    int lo = 0, hi = p.num_groups - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (s_mt[mid] <= mt) lo = mid; else hi = mid - 1;
+      if (s_mt[mid] <= mi) lo = mid; else hi = mid - 1;
     }
     g = lo;
-    row0 = s_off[g] + (mt - s_mt[g]) * tile_rows;
+    const int m_g = s_mt[g + 1] - s_mt[g];
+    const int local = idx - s_mt[g] * nt;
+    const int chunk = local / (p.swz * nt);
+    const int rem = local - chunk * p.swz * nt;
+    const int cm = min(p.swz, m_g - chunk * p.swz);
+    n_tile = rem / cm;
+    mt = chunk * p.swz + (rem - n_tile * cm);
+    row0 = s_off[g] + mt * tile_rows;
     row_end = s_off[g + 1];
   } else {
     g = 0;
+    const int chunk = idx / (p.swz * nt);
+    const int rem = idx - chunk * p.swz * nt;
+    const int cm = min(p.swz, num_mt - chunk * p.swz);
+    n_tile = rem / cm;
+    mt = chunk * p.swz + (rem - n_tile * cm);
     row0 = mt * tile_rows;
     row_end = p.rows_alloc;
   }
