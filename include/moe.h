@@ -233,6 +233,14 @@ moe_status_t moe_workspace_views(const moe_config_t* cfg, void* ws, float** logi
  * MOE_ERR_CUDA if the stream reports a CUDA error, MOE_OK otherwise. */
 moe_status_t moe_sync_check(moe_stream_t stream);
 
+/* Failure-handling self-test (no counterpart on the pages).  Launches one thread that
+ * waits, through the library's bounded device-side wait, on an mbarrier that nothing
+ * arrives at.  After `limit_us` microseconds (1..1e6) the wait gives up.  The kernel then
+ * stores 2 to *done (1 would mean the wait completed) and records MOE_ERR_TIMEOUT in the
+ * device error word, which the next moe_sync_check() reports and clears.  The kernel
+ * exits normally, so the CUDA context stays usable.  `done` is an int in device memory. */
+moe_status_t moe_debug_wait_timeout(unsigned limit_us, int* done, moe_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char* moe_status_string(moe_status_t status);
 

@@ -18,7 +18,7 @@ from typing import Optional
 __all__ = [
     "MoEConfig", "MoEError", "F32", "BF16", "FLAG_FUSED_COMBINE", "library_path", "load", "workspace_size",
     "route", "permute", "permute_noalloc", "grouped_ffn", "expert_gate_up", "expert_down", "combine", "layer_forward", "workspace_views",
-    "sync_check", "status_string", "version",
+    "sync_check", "debug_wait_timeout", "status_string", "version",
 ]
 
 F32 = 0
@@ -77,6 +77,7 @@ _SIGS = {
     "moe_layer_forward": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "moe_workspace_views": [_CFG, _P] + [ctypes.POINTER(_P)] * 10,
     "moe_sync_check": [_P],
+    "moe_debug_wait_timeout": [ctypes.c_uint, _P, _P],
     "moe_status_string": [ctypes.c_int],
     "moe_version": [],
 }
@@ -202,6 +203,13 @@ def workspace_views(cfg, ws) -> dict:
     _check(load().moe_workspace_views(ctypes.byref(cfg), _ptr(ws), *[ctypes.byref(o) for o in outs]),
            "moe_workspace_views")
     return {n: o.value for n, o in zip(names, outs)}
+
+
+def debug_wait_timeout(limit_us, done, stream=None):
+    """Self-test of the bounded device-side waits: a wait that nothing completes gives up
+    after limit_us and records MOE_ERR_TIMEOUT for the next sync_check()."""
+    _check(load().moe_debug_wait_timeout(limit_us, _ptr(done), _stream(stream)),
+           "moe_debug_wait_timeout")
 
 
 def sync_check(stream=None):

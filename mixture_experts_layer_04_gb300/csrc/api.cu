@@ -320,6 +320,20 @@ bool any_misaligned(std::initializer_list<const void*> ps) {
   return false;
 }
 
+// A wait that is meant to run out: one thread waits on an mbarrier that nothing arrives
+// at, with a short limit, through the same bounded wait every kernel of the library uses.
+__global__ void wait_timeout_probe_kernel(unsigned* err, unsigned long long limit_ns,
+                                          int* done) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);
+  fence_mbar_init();
+  abort_flag = 0;
+  const bool ok = mbar_wait(b, 0, &abort_flag, err, limit_ns);
+  *done = ok ? 1 : 2;
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -586,6 +600,16 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
   // 6. un-permute and weighted combine
   return cuda_status(launch_combine(cfg->dtype, out_perm, inv, w, shared_out, y, y_f32, cfg->T,
                                     cfg->H, cfg->K, s));
+}
+
+moe_status_t moe_debug_wait_timeout(unsigned limit_us, int* done, moe_stream_t stream) {
+  if (done == nullptr || limit_us == 0 || limit_us > 1000000u) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(done)) return MOE_ERR_MISALIGNED;
+  const DeviceInfo* d = nullptr;
+  MOE_TRY(check_device(&d));
+  wait_timeout_probe_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(
+      d->err, static_cast<unsigned long long>(limit_us) * 1000ull, done);
+  return cuda_status(cudaGetLastError());
 }
 
 moe_status_t moe_sync_check(moe_stream_t stream) {

@@ -110,17 +110,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait until the phase of parity `parity` of barrier `bar` has completed.  Gives up
-// when *abort becomes non-zero (another role gave up) or after kWaitLimitNs, in
-// which case it sets *abort and the error word.  Returns true on success.
+// when *abort becomes non-zero (another role gave up) or after `limit_ns` (default
+// kWaitLimitNs), in which case it sets *abort and the error word.  Returns true on success.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          unsigned* err) {
+                                          unsigned* err,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   unsigned long long t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0u) {
       if (*abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         *abort = 1;
         report_error(err, MOE_DEVERR_TIMEOUT);
         return false;
