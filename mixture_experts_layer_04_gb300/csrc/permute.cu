@@ -143,12 +143,27 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
       if (row_w != nullptr) row_w[row] = gate_w[static_cast<size_t>(t) * K + lane];
     }
   }
+  // The token row is read once (bursts of 8 independent 16-byte loads per lane) and
+  // written to each of its K destination rows.
   const uint4* src = x + static_cast<size_t>(t) * row_units;
-  for (int k = 0; k < K; ++k) {
-    const int r = __shfl_sync(0xffffffffu, row, k);
-    if (r < 0) continue;
-    uint4* dst = x_perm + static_cast<size_t>(r) * row_units;
-    for (int i = lane; i < row_units; i += 32) dst[i] = src[i];
+  constexpr int kBurst = 8;
+  for (int i0 = 0; i0 < row_units; i0 += 32 * kBurst) {
+    uint4 v[kBurst];
+#pragma unroll
+    for (int b = 0; b < kBurst; ++b) {
+      const int i = i0 + b * 32 + lane;
+      if (i < row_units) v[b] = __ldg(src + i);
+    }
+    for (int k = 0; k < K; ++k) {
+      const int r = __shfl_sync(0xffffffffu, row, k);
+      if (r < 0) continue;
+      uint4* dst = x_perm + static_cast<size_t>(r) * row_units;
+#pragma unroll
+      for (int b = 0; b < kBurst; ++b) {
+        const int i = i0 + b * 32 + lane;
+        if (i < row_units) dst[i] = v[b];
+      }
+    }
   }
 }
 
