@@ -80,8 +80,6 @@ struct TcCfg {
   static constexpr int kActBytes = kActRows * BK * 2;
   static constexpr int kWgtBytes = kWgtRows * BK * 2;
   static constexpr int kStageBytes = kActBytes + kWgtBytes;
-  static constexpr int kStagesRaw = (192 * 1024) / kStageBytes;
-  static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
   static constexpr int kWgtBox = MODE == kSwiGLU ? kWgtRows / 2 : kWgtRows;  // rows per TMA box
   static constexpr int kColsOut = MODE == kSwiGLU ? kWgtRows / 2 : kWgtRows; // outputs per tile
   static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
@@ -89,6 +87,11 @@ struct TcCfg {
       SWAP ? (MODE == kSwiGLU ? 64 * BN * 4 : 0) : kEpiWarps * 32 * (MODE == kSwiGLU ? 64 : 128);
   static constexpr int kBarBytes = 256;
   static constexpr int kSchedBytes = 2 * (kMaxGroups + 4) * 4 + 32 * 4;
+  // as many stages as shared memory holds (up to 12): the bytes a CTA keeps in flight set
+  // its load rate, which is what bounds the small-tile decode kernels
+  static constexpr int kStagesRaw =
+      (232448 - 1024 - kStgBytes - kBarBytes - kSchedBytes) / kStageBytes;
+  static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
   static constexpr int kSmem = 1024 + kStages * kStageBytes + kStgBytes + kBarBytes + kSchedBytes;
   static_assert((kTmemCols & (kTmemCols - 1)) == 0 && kTmemCols <= 512, "TMEM columns");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M=128");
@@ -300,6 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sStg = sWgt + S * Cfg::kWgtBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + Cfg::kStgBytes);
   // bars: full[S], empty[S], tfull[2], tempty[2], mma_done
+  static_assert(8 * (2 * S + 5) + 8 <= 256, "barrier region");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_off = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(bars) + Cfg::kBarBytes);
