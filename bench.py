@@ -63,6 +63,8 @@ def parse():
     ap.add_argument("--fused-combine", dest="fused", action="store_true", default=None,
                     help="fuse the combine into the down GEMM (MOE_FLAG_FUSED_COMBINE)")
     ap.add_argument("--gather-combine", dest="fused", action="store_false")
+    ap.add_argument("--time-row-gather", action="store_true",
+                    help="also time the row-gather gate/up variant as a stage")
     return ap.parse_args()
 
 
@@ -137,6 +139,21 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def gate_up_kernel(shape, T):
+    """The gate/up kernel the layer launches (mirrors the library's choice): CTA pairs with
+    256-row tiles for large groups (>= 768 rows per expert on average), else single CTAs
+    that gather token rows from x by TMA; decode-sized batches (T <= 128) put the weights
+    on the MMA's 128-row side."""
+    if shape.dtype != "bf16":
+        return "grouped_gemm_simt_kernel<SwiGLU> (moe_expert_gate_up)"
+    if T <= 128:
+        bt = 16 if T <= 16 else 32 if T <= 32 else 64
+        return f"tc_grouped_gemm_kernel<{bt},SwiGLU,swap> (moe_expert_gate_up)"
+    if T * shape.K >= 768 * shape.E:
+        return "tc_pair_gemm_kernel<SwiGLU> (moe_expert_gate_up)"
+    return "tc_grouped_gemm_kernel<256,SwiGLU> (moe_expert_gate_up)"
+
+
 def recorded_traffic(workload, kernel):
     """DRAM bytes per launch of `kernel` on `workload` from a committed ncu summary under
     profiles/, or None when there is none or the kernel sources changed since it was taken
@@ -193,7 +210,7 @@ def algorithmic(shape, T, counts):
     flops = 2 * T * E * H + 6 * H * I * M + 6 * H * Is * T
     byts = T * H * b + E * H * b + 3 * H * I * b * touched + 3 * H * Is * b + T * H * b
     gate_up_flops = 4 * H * I * M
-    gate_up_bytes = M * H * b + 2 * I * H * b * touched + M * I * b
+    gate_up_bytes = T * H * b + 2 * I * H * b * touched + M * I * b  # x rows read once
     return dict(M=M, touched=touched, flops=flops, bytes=byts, gate_up_flops=gate_up_flops,
                 gate_up_bytes=gate_up_bytes)
 
@@ -304,6 +321,11 @@ def run_ours(args, rank, world, local):
     gate_up_times = timed(lambda: moe.expert_gate_up(cfg, x_perm, offsets, inp["w_gate_up"], h, ws,
                                                      stream=stream), max(args.steps, 5))
     stages["gate_up"] = gate_up_times
+    gu_kernel = gate_up_kernel(shape, T)
+    if shape.dtype == "bf16" and args.time_row_gather:
+        # the row-gather variant (not used by the layer), for comparison
+        stages["gate_up_gather"] = timed(lambda: moe.expert_gate_up_gather(
+            cfg, inp["x"], perm, offsets, inp["w_gate_up"], h, ws, stream=stream), nst)
     stages["down"] = timed(lambda: moe.expert_down(cfg, h, offsets, inp["w_down"], out_perm, ws,
                                                    stream=stream), nst)
     shared_out = None
@@ -337,7 +359,7 @@ def run_ours(args, rank, world, local):
                 "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4)}
     roof["traffic"] = recorded_traffic(args.config if args.tokens is None else
                                        f"{args.config}-T{T}", "gate_up")
-    roof["kernel"] = "tc_grouped_gemm_kernel<256,SwiGLU> (moe_expert_gate_up)"
+    roof["kernel"] = gu_kernel
     roof["peak_source"] = peak_kind
 
     # whole-layer roofline: the slower of FLOPs at the bf16 peak and bytes at HBM speed

@@ -181,6 +181,21 @@ moe_status_t moe_expert_gate_up(const moe_config_t* cfg, const void* x_perm,
                                 const int32_t* offsets, const void* w_gate_up, void* h, void* ws,
                                 size_t ws_bytes, moe_stream_t stream);
 
+/* The same gate/up projection with the dispatch row gather folded into its loads: row r
+ * of the groups is token row perm[r] of x, so no permuted copy of x is needed.
+ * Defined by: page section "单机MoE执行流水线" (moving token rows to their experts is
+ * part of the cost at small batches; a fused kernel need not write intermediates back to
+ * device memory).  For every row r of group e:
+ *   h[r] = silu(x[perm[r]] W_g[e]^T) * (x[perm[r]] W_u[e]^T), as moe_expert_gate_up.
+ *   x [T,H] act in; perm [T*K] int32 in (device; entries below offsets[E] are token ids in
+ *   0..T-1, the rest are not read); offsets [E+1] int32 in; w_gate_up [E,2I,H] act;
+ *   h [T*K,I] act out (rows >= offsets[E] untouched); ws as for moe_grouped_ffn.
+ * bf16 only (MOE_ERR_UNSUPPORTED for float32 layers). */
+moe_status_t moe_expert_gate_up_gather(const moe_config_t* cfg, const void* x,
+                                       const int32_t* perm, const int32_t* offsets,
+                                       const void* w_gate_up, void* h, void* ws,
+                                       size_t ws_bytes, moe_stream_t stream);
+
 /* The second GEMM of the grouped FFN alone: the output projection.
  * Defined by: page section "单机MoE执行流水线" (each expert applies its output
  * projection).  For every row r of group e: out_perm[r] = h[r] W_d[e]^T (fp32).

@@ -72,6 +72,7 @@ _SIGS = {
     "moe_permute_noalloc": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P],
     "moe_grouped_ffn": [_CFG, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "moe_expert_gate_up": [_CFG, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+    "moe_expert_gate_up_gather": [_CFG, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "moe_expert_down": [_CFG, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "moe_combine": [_CFG, _P, _P, _P, _P, _P, _P, _P],
     "moe_layer_forward": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
@@ -171,6 +172,14 @@ def expert_gate_up(cfg, x_perm, offsets, w_gate_up, h, ws, ws_bytes=None, stream
     _check(load().moe_expert_gate_up(ctypes.byref(cfg), _ptr(x_perm), _ptr(offsets),
                                      _ptr(w_gate_up), _ptr(h), _ptr(ws), nb, _stream(stream)),
            "moe_expert_gate_up")
+
+
+def expert_gate_up_gather(cfg, x, perm, offsets, w_gate_up, h, ws, ws_bytes=None, stream=None):
+    nb = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check(load().moe_expert_gate_up_gather(ctypes.byref(cfg), _ptr(x), _ptr(perm), _ptr(offsets),
+                                            _ptr(w_gate_up), _ptr(h), _ptr(ws), nb,
+                                            _stream(stream)),
+           "moe_expert_gate_up_gather")
 
 
 def expert_down(cfg, h, offsets, w_down, out_perm, ws, ws_bytes=None, stream=None):

@@ -211,18 +211,22 @@ moe_status_t launch_gemm(const moe_config_t* c, const DeviceInfo* d, const Group
     g.swap_tokens = c->T <= kSwapMaxTokens ? c->T : 0;
     // large groups (>= 768 rows on average) run on CTA pairs with 256-row tiles; smaller,
     // ragged groups keep 128-row tiles (less padding in each group's last tile)
-    g.pair = (g.swap_tokens == 0 && g.rows_alloc >= kPairMinRowsPerGroup * g.G) ? 1 : 0;
+    g.pair = (g.swap_tokens == 0 && g.rows_alloc >= kPairMinRowsPerGroup * g.G &&
+              g.gather_rows == nullptr) ? 1 : 0;
     return cuda_status(launch_grouped_gemm_tc(g, d->err, d->num_sms, s));
   }
   return cuda_status(launch_grouped_gemm_simt(g0, s));
 }
 
-// h = silu(A W_g^T) * (A W_u^T) per group.
+// h = silu(A W_g^T) * (A W_u^T) per group.  With `gather_rows`, row r of the groups is
+// row gather_rows[r] of A (A then has c->T rows).
 moe_status_t run_gate_up(const moe_config_t* c, const DeviceInfo* d, const void* A,
                          int rows_alloc, const void* w_gate_up, int I, void* h, const Groups& gr,
-                         cudaStream_t s) {
+                         cudaStream_t s, const int32_t* gather_rows = nullptr) {
   if (rows_alloc == 0) return MOE_OK;
   GroupedGemm g{};
+  g.gather_rows = gather_rows;
+  g.src_rows = c->T;
   g.mode = kSwiGLU;
   g.dtype = c->dtype;
   g.A = A;
@@ -467,6 +471,27 @@ moe_status_t moe_expert_gate_up(const moe_config_t* cfg, const void* x_perm,
   return run_gate_up(cfg, d, x_perm, cfg->T * cfg->K, w_gate_up, cfg->I, h, gr, s);
 }
 
+moe_status_t moe_expert_gate_up_gather(const moe_config_t* cfg, const void* x,
+                                       const int32_t* perm, const int32_t* offsets,
+                                       const void* w_gate_up, void* h, void* ws, size_t ws_bytes,
+                                       moe_stream_t stream) {
+  MOE_TRY(check_config(cfg));
+  if (cfg->T == 0) return MOE_OK;
+  if (x == nullptr || perm == nullptr || offsets == nullptr || w_gate_up == nullptr ||
+      h == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (any_misaligned({x, perm, offsets, w_gate_up, h})) return MOE_ERR_MISALIGNED;
+  Plan p;
+  MOE_TRY(check_ws(cfg, ws, ws_bytes, &p));
+  const DeviceInfo* d = nullptr;
+  MOE_TRY(check_device(&d));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Groups gr;
+  MOE_TRY(routed_groups(cfg, offsets, ws, p, false, s, &gr));
+  return run_gate_up(cfg, d, x, cfg->T * cfg->K, w_gate_up, cfg->I, h, gr, s, perm);
+}
+
 moe_status_t moe_expert_down(const moe_config_t* cfg, const void* h, const int32_t* offsets,
                              const void* w_down, float* out_perm, void* ws, size_t ws_bytes,
                              moe_stream_t stream) {
@@ -542,6 +567,9 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
   const bool simt = cfg->dtype == MOE_F32;
   // the fused combine needs the tensor-core engine; float32 layers keep the gather combine
   const bool fused = (cfg->flags & MOE_FLAG_FUSED_COMBINE) != 0u && !simt;
+  // The gate/up GEMM reads the permuted copy x_perm: its row gather variant
+  // (moe_expert_gate_up_gather, TMA tile::gather4) is exact but measured 2-3x slower on
+  // GB300 than the copy plus whole-tile TMA loads, so the layer does not use it.
 
   // 1. router scores, top-k, gate drop
   int deferred = 0;

@@ -153,6 +153,19 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint
       : "memory");
 }
 
+// Row gather: four rows r0..r3 (any order, any rows of the tensor) of a 2D map whose box
+// is one row high, each `box width` columns from column c0, land in shared memory as four
+// consecutive box rows at dst (with the map's swizzle, which follows the shared address).
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, uint32_t bar, int c0,
+                                            int r0, int r1, int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(r0), "r"(r1), "r"(r2),
+      "r"(r3)
+      : "memory");
+}
+
 // One bulk (non-tensor) copy global -> shared of `bytes` (multiple of 16, both addresses
 // 16-byte aligned), completing on mbarrier `bar` as transaction bytes.
 __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,

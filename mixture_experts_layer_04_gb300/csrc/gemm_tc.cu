@@ -71,6 +71,7 @@ struct TcParams {
   int n_tiles;
   int up_offset;
   int swz;
+  const int32_t* gather_rows;  // A row r is row gather_rows[r] of the mapped tensor, or null
 };
 
 template <int BN, int MODE, bool SWAP>
@@ -288,7 +289,7 @@ __device__ __forceinline__ void epilogue_rows(const TcParams& p, uint32_t t_row,
   }
 }
 
-template <int BN, int MODE, bool SWAP>
+template <int BN, int MODE, bool SWAP, bool GATHER>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_grouped_gemm_kernel(const __grid_constant__ TcParams p) {
   using Cfg = TcCfg<BN, MODE, SWAP>;
@@ -372,7 +373,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer ----
-    if (elect_one_sync()) {
+    // One elected lane waits for a free stage, arms its barrier and loads the weight and
+    // activation tiles.  With a row gather, the whole warp runs the loop: lane 0 as
+    // above for the weights, and lane l < rows/4 loads activation rows 4l..4l+3 of the
+    // tile, each from its own source row (tile::gather4).
+    constexpr bool gather = GATHER;
+    constexpr int kGatherLanes = kTileRows / 4;
+    static_assert(kGatherLanes <= 32, "one gather4 per lane");
+    if (gather || elect_one_sync()) {
+      const bool leader = !gather || lane == 0;
       int stage = 0;
       uint32_t phase = 0;
       long long issued = 0;
@@ -381,19 +390,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         int g, row0, row_end, n_tile;
         decode_tile(p, s_off, s_mt, num_mt, kTileRows, idx, g, row0, row_end, n_tile);
         const int n0 = n_tile * Cfg::kColsOut;  // first weight row of the tile
+        int src[4] = {0, 0, 0, 0};
+        if (GATHER && lane < kGatherLanes) {
+          // rows past the group's end repeat a row of the tile: computed, never stored
+          const int pad = p.gather_rows[row0];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = row0 + 4 * lane + i;
+            src[i] = r < row_end ? p.gather_rows[r] : pad;
+          }
+        }
         for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
+          bool good = true;
+          if (leader) good = mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err);
+          if constexpr (GATHER) good = __shfl_sync(0xffffffffu, good ? 1 : 0, 0) != 0;
+          if (!good) {
             ok = false;
             break;
           }
           const uint32_t fb = full_bar(stage);
-          mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
           const uint32_t a_dst = smem_u32(sAct + stage * Cfg::kActBytes);
           const uint32_t w_dst = smem_u32(sWgt + stage * Cfg::kWgtBytes);
-          tma_load_2d(a_dst, &p.tmAct, fb, kb * BK, row0);
-          tma_load_3d(w_dst, &p.tmWgt, fb, kb * BK, n0, g);
-          if constexpr (MODE == kSwiGLU)
-            tma_load_3d(w_dst + Cfg::kWgtBox * 128, &p.tmWgt, fb, kb * BK, p.up_offset + n0, g);
+          if (leader) {
+            mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
+            if constexpr (!GATHER) tma_load_2d(a_dst, &p.tmAct, fb, kb * BK, row0);
+            tma_load_3d(w_dst, &p.tmWgt, fb, kb * BK, n0, g);
+            if constexpr (MODE == kSwiGLU)
+              tma_load_3d(w_dst + Cfg::kWgtBox * 128, &p.tmWgt, fb, kb * BK, p.up_offset + n0, g);
+          }
+          if constexpr (GATHER) {
+            __syncwarp();
+            if (lane < kGatherLanes)
+              tma_gather4(a_dst + 512u * lane, &p.tmAct, fb, kb * BK, src[0], src[1], src[2],
+                          src[3]);
+          }
           ++issued;
           if (++stage == S) {
             stage = 0;
@@ -401,18 +431,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // Drain: the most recent load of every stage must have landed before the CTA
-      // may exit (they all have in a normal run; this matters only after an abort).
-      const int n = issued < S ? static_cast<int>(issued) : S;
-      int s = stage;
-      uint32_t ph = phase;
-      volatile int no_abort = 0;
-      for (int j = 0; j < n; ++j) {
-        if (--s < 0) {
-          s = S - 1;
-          ph ^= 1u;
+      // Drain: the most recent load of every stage must have landed before the CTA may
+      // exit (they all have in a normal run; this matters only after an abort).
+      if (leader) {
+        const int n = issued < S ? static_cast<int>(issued) : S;
+        int s = stage;
+        uint32_t ph = phase;
+        volatile int no_abort = 0;
+        for (int j = 0; j < n; ++j) {
+          if (--s < 0) {
+            s = S - 1;
+            ph ^= 1u;
+          }
+          mbar_wait(full_bar(s), ph, &no_abort, p.err);
         }
-        mbar_wait(full_bar(s), ph, &no_abort, p.err);
       }
     }
     __syncwarp();
@@ -830,10 +862,11 @@ bool make_map_3d(CUtensorMap* m, const void* base, uint64_t G, uint64_t rows, ui
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int MODE, bool SWAP>
+template <int BN, int MODE, bool SWAP, bool GATHER = false>
 cudaError_t launch_one(const GroupedGemm& g, unsigned* err, int num_sms, cudaStream_t s) {
   using Cfg = TcCfg<BN, MODE, SWAP>;
-  auto kernel = tc_grouped_gemm_kernel<BN, MODE, SWAP>;
+  auto kernel = tc_grouped_gemm_kernel<BN, MODE, SWAP, GATHER>;
+  if (GATHER != (g.gather_rows != nullptr)) return cudaErrorInvalidValue;
   static int attr_set_dev = -1;  // the attribute is per function and device
   int dev = 0;
   cudaGetDevice(&dev);
@@ -845,9 +878,15 @@ cudaError_t launch_one(const GroupedGemm& g, unsigned* err, int num_sms, cudaStr
   }
   TcParams p;
   memset(&p, 0, sizeof(p));
-  if (!make_map_2d(&p.tmAct, g.A, static_cast<uint64_t>(g.rows_alloc), static_cast<uint64_t>(g.Kd),
-                   Cfg::kActRows))
-    return cudaErrorInvalidValue;
+  // with a row gather the map covers the source rows, one row per box
+  const bool ok_map =
+      g.gather_rows != nullptr
+          ? make_map_2d(&p.tmAct, g.A, static_cast<uint64_t>(g.src_rows),
+                        static_cast<uint64_t>(g.Kd), 1)
+          : make_map_2d(&p.tmAct, g.A, static_cast<uint64_t>(g.rows_alloc),
+                        static_cast<uint64_t>(g.Kd), Cfg::kActRows);
+  if (!ok_map) return cudaErrorInvalidValue;
+  p.gather_rows = g.gather_rows;
   if (!make_map_3d(&p.tmWgt, g.B, static_cast<uint64_t>(g.G), static_cast<uint64_t>(g.Nb),
                    static_cast<uint64_t>(g.Kd), Cfg::kWgtBox))
     return cudaErrorInvalidValue;
@@ -927,6 +966,17 @@ cudaError_t launch_grouped_gemm_tc(const GroupedGemm& g, unsigned* err, int num_
                                    cudaStream_t s) {
   if (g.dtype != kBF16) return cudaErrorInvalidValue;
   if (g.G > kMaxGroups) return cudaErrorInvalidValue;
+  if (g.gather_rows != nullptr && g.src_rows <= 0) return cudaErrorInvalidValue;
+  if (g.gather_rows != nullptr) {  // the row-gather gate/up variant
+    if (g.mode != kSwiGLU) return cudaErrorInvalidValue;
+    if (g.swap_tokens > 0) {
+      const int bt = tc_swap_tokens(g.swap_tokens);
+      if (bt == 16) return launch_one<16, kSwiGLU, true, true>(g, err, num_sms, s);
+      if (bt == 32) return launch_one<32, kSwiGLU, true, true>(g, err, num_sms, s);
+      return launch_one<64, kSwiGLU, true, true>(g, err, num_sms, s);
+    }
+    return launch_one<256, kSwiGLU, false, true>(g, err, num_sms, s);
+  }
   if (g.swap_tokens > 0) {
     const int bt = tc_swap_tokens(g.swap_tokens);
     if (g.mode == kSwiGLU) {

@@ -138,6 +138,10 @@ struct GroupedGemm {
   const float* row_w;        // kScatter only
   // Tensor-core engine, normal order only: run on CTA pairs (cta_group::2, 256-row tiles)
   int pair;
+  // Tensor-core engine, single CTAs: row r of the (grouped) A is row gather_rows[r] of the
+  // src_rows x Kd matrix at A, fetched by TMA row gathers (no permuted copy of A), or null.
+  const int32_t* gather_rows;
+  int src_rows;
 };
 
 cudaError_t launch_grouped_gemm_simt(const GroupedGemm& g, cudaStream_t s);

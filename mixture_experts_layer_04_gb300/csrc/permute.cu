@@ -216,7 +216,15 @@ __global__ void __launch_bounds__(kSmallThreads)
     float* sw = reinterpret_cast<float*>(sids + TK);     // [T*K]
     for (int i = tid; i < T * E; i += blockDim.x) {
       float v = 0.f;
-      for (int sl = 0; sl < rt.S; ++sl) v += rt.partial[static_cast<size_t>(sl) * T * E + i];
+      for (int s0 = 0; s0 < rt.S; s0 += 8) {  // 8 slice loads in flight, summed in order
+        float q[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          q[j] = s0 + j < rt.S ? rt.partial[static_cast<size_t>(s0 + j) * T * E + i] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (s0 + j < rt.S) v += q[j];
+      }
       if (rt.bias != nullptr) v += rt.bias[i % E];
       Ls[i] = v;
       if (blockIdx.x == 0) rt.logits[i] = v;
@@ -290,15 +298,29 @@ __global__ void __launch_bounds__(kSmallThreads)
       if (tid == 0) *num_mtiles = all;
     }
   }
-  // row copies: assignment a -> x_perm[rows[a]] = x[a / K], one warp per assignment
+  // row copies: assignment a -> x_perm[rows[a]] = x[a / K], one warp per assignment,
+  // each lane with 8 independent 16-byte loads in flight before its stores
   const int warp = tid >> 5, lane = tid & 31;
+  constexpr int kBurst = 8;
   for (int a = blockIdx.x * (kSmallThreads / 32) + warp; a < TK;
        a += gridDim.x * (kSmallThreads / 32)) {
     const int r = rows[a];
     if (r < 0) continue;
     const uint4* src = x + static_cast<size_t>(a / K) * row_units;
     uint4* dst = x_perm + static_cast<size_t>(r) * row_units;
-    for (int i = lane; i < row_units; i += 32) dst[i] = src[i];
+    for (int i0 = 0; i0 < row_units; i0 += 32 * kBurst) {
+      uint4 v[kBurst];
+#pragma unroll
+      for (int b = 0; b < kBurst; ++b) {
+        const int i = i0 + b * 32 + lane;
+        if (i < row_units) v[b] = __ldg(src + i);
+      }
+#pragma unroll
+      for (int b = 0; b < kBurst; ++b) {
+        const int i = i0 + b * 32 + lane;
+        if (i < row_units) dst[i] = v[b];
+      }
+    }
   }
 }
 

@@ -224,7 +224,15 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
   float* Ls = Ls_all + warp * E;
   for (int e = lane; e < E; e += 32) {
     float v = 0.f;
-    for (int s = 0; s < S; ++s) v += partial[(static_cast<size_t>(s) * T + t) * E + e];
+    for (int s0 = 0; s0 < S; s0 += 8) {  // 8 slice loads in flight, summed in order
+      float q[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        q[j] = s0 + j < S ? partial[(static_cast<size_t>(s0 + j) * T + t) * E + e] : 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (s0 + j < S) v += q[j];
+    }
     if (bias != nullptr) v += bias[e];
     if (logits_out != nullptr) logits_out[static_cast<size_t>(t) * E + e] = v;
     Ls[e] = v;

@@ -111,6 +111,17 @@ def test_argument_errors_are_host_side(lib):
     assert lib.moe_combine(ctypes.byref(c), _p(A), _p(A), _p(A), None, _p(A + 8), None, None) == MISALIGNED
 
 
+def test_row_gather_gate_up_is_bf16_only(lib):
+    c = cfg(dtype=moe.F32)
+    A = 0x7000_0000_0000
+    need = ws_size(c)[1]
+    assert lib.moe_expert_gate_up_gather(ctypes.byref(c), _p(A), _p(A), _p(A), _p(A), _p(A), _p(A),
+                                         need, None) == UNSUPPORTED
+    cb = cfg()
+    assert lib.moe_expert_gate_up_gather(ctypes.byref(cb), _p(A), None, _p(A), _p(A), _p(A), _p(A),
+                                         ws_size(cb)[1], None) == INVALID
+
+
 def test_zero_tokens_is_a_noop_without_gpu(lib):
     c = cfg(T=0)
     A = 0x7000_0000_0000

@@ -227,6 +227,28 @@ def test_grouped_ffn_stages(moe, T, H_, E, K, I, dtype, skew):
                          what="grouped_ffn")
 
 
+@pytest.mark.parametrize("T,H_,E,K,I,dtype,skew", [c for c in FFN_CASES if c[5] == "bf16"])
+def test_gate_up_row_gather_equals_permuted_copy(moe, T, H_, E, K, I, dtype, skew):
+    """The gate/up GEMM that gathers its rows from x by perm computes, row for row, the
+    same h as the one reading the permuted copy x_perm (the same products in the same
+    order), and reads no entry of perm at or past offsets[E]."""
+    shape, inp, offsets, x_perm, M = _ffn_inputs(T, H_, E, K, I, dtype, skew)
+    _, _, perm, _ = oracle.permute(_skewed_ids(T, E, K, 0.0, skew, seed=1 + T)[0], E)
+    c = _cfg(moe, T, H_, E, K, I=I, dtype=dtype)
+    off = torch.from_numpy(offsets).cuda()
+    perm_d = torch.full((T * K,), -7, dtype=torch.int32)
+    perm_d[:M] = torch.from_numpy(perm[:M])
+    perm_d = perm_d.cuda()
+    ws = torch.empty(moe.workspace_size(c), dtype=torch.uint8, device="cuda")
+    h_copy = torch.full((T * K, I), -5.0, dtype=shape.torch_dtype, device="cuda")
+    h_gath = torch.full((T * K, I), -5.0, dtype=shape.torch_dtype, device="cuda")
+    moe.expert_gate_up(c, x_perm, off, inp["w_gate_up"], h_copy, ws)
+    moe.expert_gate_up_gather(c, inp["x"], perm_d, off, inp["w_gate_up"], h_gath, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(h_gath[:M], h_copy[:M])
+    assert (h_gath[M:] == -5.0).all()
+
+
 @pytest.mark.parametrize("T,H_,E,K,shared,dtype", [
     (1, 64, 4, 2, False, "bf16"), (300, 256, 8, 2, True, "bf16"), (1000, 512, 128, 8, False, "bf16"),
     (257, 128, 16, 16, True, "f32"), (64, 7168, 256, 8, True, "bf16"),
