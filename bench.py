@@ -188,7 +188,7 @@ def kernel_launches_per_step(shape, T):
     wsmem_router = E <= 16 and E * H * b <= 96 * 1024 and T >= 64
     fused_small = T <= 64 and (E * 8 * 4 + (2 * E + 1) * 4 + T * K * 12 + T * E * 4) <= 200 * 1024
     if tc_router:
-        n += 2                            # router GEMM + top-k
+        n += 1 if E <= 256 else 2         # router GEMM (top-k in its epilogue up to 256 experts)
     elif wsmem_router:
         n += 1                            # router with the top-k fused
     else:

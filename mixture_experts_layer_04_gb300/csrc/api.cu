@@ -170,6 +170,15 @@ moe_status_t run_route(const moe_config_t* c, const DeviceInfo* d, const void* x
     g.N_out = c->E;
     g.C = logits;
     g.col_bias = bias;
+    if (c->E <= 256) {
+      // one tile spans all experts: the top-k, softmax and gate drop run in its epilogue
+      g.mode = kTopK;
+      g.topk_k = c->K;
+      g.topk_theta = c->gate_threshold;
+      g.topk_ids = ids;
+      g.topk_w = w;
+      return cuda_status(launch_grouped_gemm_tc(g, d->err, d->num_sms, s));
+    }
     MOE_CUDA(launch_grouped_gemm_tc(g, d->err, d->num_sms, s));
     return cuda_status(
         launch_topk(logits, 1, nullptr, nullptr, ids, w, c->T, c->E, c->K, c->gate_threshold, s));

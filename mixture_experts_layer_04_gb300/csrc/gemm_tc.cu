@@ -45,6 +45,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "topk.cuh"
 
 namespace moe {
 namespace {
@@ -72,6 +73,10 @@ struct TcParams {
   int up_offset;
   int swz;
   const int32_t* gather_rows;  // A row r is row gather_rows[r] of the mapped tensor, or null
+  int topk_k;                  // kTopK: experts kept per row, gate threshold, outputs
+  float topk_theta;
+  int32_t* topk_ids;
+  float* topk_w;
 };
 
 template <int BN, int MODE, bool SWAP>
@@ -287,6 +292,124 @@ __device__ __forceinline__ void epilogue_rows(const TcParams& p, uint32_t t_row,
       __syncwarp();
     }
   }
+}
+
+// Sum of 16 values in the order of a 32-lane xor-butterfly whose lanes 16-31 hold zero
+// (warp_sum), so that the gates below equal the warp top-k's bit for bit.
+__device__ __forceinline__ float butterfly_sum16(const float (&z)[16]) {
+  const float a0 = (z[0] + z[8]) + (z[4] + z[12]), a2 = (z[2] + z[10]) + (z[6] + z[14]);
+  const float a1 = (z[1] + z[9]) + (z[5] + z[13]), a3 = (z[3] + z[11]) + (z[7] + z[15]);
+  return (a0 + a2) + (a1 + a3);
+}
+
+// kTopK epilogue (router logits): each thread owns one token row of the tile, which spans
+// all N_out experts.  The logits (+ bias) are stored as in kPlain, and on the way the
+// thread keeps the 16 best (logit, expert) pairs in registers, sorted by logit descending
+// and expert ascending on ties (the warp top-k's order).  Then the softmax over the K
+// kept logits, the gate drop and the renormalisation, as the warp top-k computes them.
+template <int BN>
+__device__ __forceinline__ void epilogue_topk(const TcParams& p, uint32_t t_row, uint32_t stg,
+                                              int lane, int tile_row0, int row_end) {
+  float* C = static_cast<float*>(p.C);
+  const int K = p.topk_k;
+  uint32_t kk[16];
+  int ki[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    kk[j] = 0u;  // below the key of every non-NaN float
+    ki[j] = -1;
+  }
+  uint32_t thr = 0u;  // key of the K-th best so far
+  const uint32_t kmask = 1u << (K - 1);
+#pragma unroll 1
+  for (int c = 0; c < BN; c += 32) {
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(t_row + c, r);
+    tmem_ld_wait();
+    if (p.col_bias != nullptr) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int col = c + j;
+        const float b = col < p.N_out ? __ldg(p.col_bias + col) : 0.f;
+        r[j] = __float_as_uint(__uint_as_float(r[j]) + b);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      st_shared_v4(stg + stg_off<128>(lane, u), r[4 * u], r[4 * u + 1], r[4 * u + 2],
+                   r[4 * u + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int pass = 0; pass < 8; ++pass) {
+      const int rr = pass * 4 + (lane >> 3), u = lane & 7;
+      const uint4 v = ld_shared_v4(stg + stg_off<128>(rr, u));
+      const int grow = tile_row0 + rr;
+      const int col = c + u * 4;
+      if (grow < row_end && col < p.N_out)
+        *reinterpret_cast<uint4*>(C + static_cast<size_t>(grow) * p.N_out + col) = v;
+    }
+    __syncwarp();
+    // this thread's 32 logits, read back from its own staging row
+#pragma unroll 1
+    for (int u = 0; u < 8; ++u) {
+      const uint4 v4 = ld_shared_v4(stg + stg_off<128>(lane, u));
+      const uint32_t vv[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+      const int col = c + 4 * u + t;
+      const uint32_t key = float_key(__uint_as_float(vv[t]));
+      if (col < p.N_out && key > thr) {  // enters the top K: insertion into the sorted 16
+#pragma unroll
+        for (int q = 15; q >= 1; --q) {  // selects only: every slot stays in a register
+          const bool shift = key > kk[q - 1];
+          const bool here = key > kk[q];
+          kk[q] = shift ? kk[q - 1] : (here ? key : kk[q]);
+          ki[q] = shift ? ki[q - 1] : (here ? col : ki[q]);
+        }
+        const bool first = key > kk[0];
+        kk[0] = first ? key : kk[0];
+        ki[0] = first ? col : ki[0];
+        // the K-th key, picked with a precomputed one-hot mask (no indexed access)
+        uint32_t t_new = 0u;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) t_new |= kk[q] & ((kmask >> q) & 1u ? 0xffffffffu : 0u);
+        thr = t_new;
+      }
+      }
+    }
+  }
+  const int grow = tile_row0 + lane;
+  if (grow >= row_end) return;
+  // keys back to logits (float_key is monotone; -0 came in as +0)
+  float z[16], lv[16];
+#pragma unroll
+  for (int q = 0; q < 16; ++q)
+    lv[q] = __uint_as_float((kk[q] & 0x80000000u) ? (kk[q] & 0x7fffffffu) : ~kk[q]);
+#pragma unroll
+  for (int q = 0; q < 16; ++q) z[q] = q < K ? expf(lv[q] - lv[0]) : 0.f;
+  const float s = butterfly_sum16(z);
+  float w[16];
+#pragma unroll
+  for (int q = 0; q < 16; ++q) w[q] = z[q] / s;
+  if (p.topk_theta > 0.f) {
+#pragma unroll
+    for (int q = 1; q < 16; ++q)
+      if (q < K && w[q] < p.topk_theta) {
+        w[q] = 0.f;
+        ki[q] = -1;
+      }
+    const float s2 = butterfly_sum16(w);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) w[q] = w[q] / s2;
+  }
+  int32_t* ids = p.topk_ids + static_cast<size_t>(grow) * K;
+  float* wo = p.topk_w + static_cast<size_t>(grow) * K;
+#pragma unroll
+  for (int q = 0; q < 16; ++q)
+    if (q < K) {
+      ids[q] = ki[q];
+      wo[q] = w[q];
+    }
 }
 
 template <int BN, int MODE, bool SWAP, bool GATHER>
@@ -519,7 +642,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t stg =
             smem_u32(sStg) + static_cast<uint32_t>((warp - 2) * 32 * (MODE == kSwiGLU ? 64 : 128));
         const int tile_row0 = row0 + quad * 32;  // first global row of this warp's 32 rows
-        epilogue_rows<BN, MODE>(p, t_row, stg, lane, tile_row0, row_end, col0);
+        if constexpr (MODE == kTopK)
+          epilogue_topk<BN>(p, t_row, stg, lane, tile_row0, row_end);
+        else
+          epilogue_rows<BN, MODE>(p, t_row, stg, lane, tile_row0, row_end, col0);
       } else {
         // swapped: lane = weight row of the tile, column j = token row0 + j
         if constexpr (MODE == kSwiGLU) {
@@ -887,6 +1013,10 @@ cudaError_t launch_one(const GroupedGemm& g, unsigned* err, int num_sms, cudaStr
                         static_cast<uint64_t>(g.Kd), Cfg::kActRows);
   if (!ok_map) return cudaErrorInvalidValue;
   p.gather_rows = g.gather_rows;
+  p.topk_k = g.topk_k;
+  p.topk_theta = g.topk_theta;
+  p.topk_ids = g.topk_ids;
+  p.topk_w = g.topk_w;
   if (!make_map_3d(&p.tmWgt, g.B, static_cast<uint64_t>(g.G), static_cast<uint64_t>(g.Nb),
                    static_cast<uint64_t>(g.Kd), Cfg::kWgtBox))
     return cudaErrorInvalidValue;
@@ -967,6 +1097,15 @@ cudaError_t launch_grouped_gemm_tc(const GroupedGemm& g, unsigned* err, int num_
   if (g.dtype != kBF16) return cudaErrorInvalidValue;
   if (g.G > kMaxGroups) return cudaErrorInvalidValue;
   if (g.gather_rows != nullptr && g.src_rows <= 0) return cudaErrorInvalidValue;
+  if (g.mode == kTopK) {  // router logits with the top-k in the epilogue: one tile spans E
+    if (g.swap_tokens > 0 || g.pair || g.gather_rows != nullptr || g.offsets != nullptr ||
+        g.N_out > 256 || g.topk_k < 1 || g.topk_k > 16 || g.topk_ids == nullptr ||
+        g.topk_w == nullptr)
+      return cudaErrorInvalidValue;
+    if (g.N_out <= 64) return launch_one<64, kTopK, false>(g, err, num_sms, s);
+    if (g.N_out <= 128) return launch_one<128, kTopK, false>(g, err, num_sms, s);
+    return launch_one<256, kTopK, false>(g, err, num_sms, s);
+  }
   if (g.gather_rows != nullptr) {  // the row-gather gate/up variant
     if (g.mode != kSwiGLU) return cudaErrorInvalidValue;
     if (g.swap_tokens > 0) {

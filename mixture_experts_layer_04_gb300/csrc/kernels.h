@@ -107,7 +107,9 @@ cudaError_t launch_combine(int dtype, const float* out_perm, const int32_t* inv,
 // A: [rows_alloc, Kd] row-major; B: [G, Nb, Kd] row-major; C: [rows_alloc, N_out].
 //   C[row_token[row], n] += row_w[row] * sum_k A[row, k] * B[g, n, k]  (mode kScatter:
 //   the combine fused into the down projection; fp32 additions at L2, order not fixed)
-enum GemmMode : int { kPlain = 0, kSwiGLU = 1, kScatter = 2 };
+// kTopK: kPlain (the router logits, + col_bias) whose epilogue also takes each row's top-k
+// over all N_out <= 256 columns (one tile spans them) with the softmax and gate drop.
+enum GemmMode : int { kPlain = 0, kSwiGLU = 1, kScatter = 2, kTopK = 3 };
 
 struct GroupedGemm {
   int mode;
@@ -142,6 +144,11 @@ struct GroupedGemm {
   // src_rows x Kd matrix at A, fetched by TMA row gathers (no permuted copy of A), or null.
   const int32_t* gather_rows;
   int src_rows;
+  // kTopK only: K (<= 16), gate threshold, outputs ids [rows, K] and weights [rows, K]
+  int topk_k;
+  float topk_theta;
+  int32_t* topk_ids;
+  float* topk_w;
 };
 
 cudaError_t launch_grouped_gemm_simt(const GroupedGemm& g, cudaStream_t s);

@@ -78,20 +78,37 @@ __global__ void __launch_bounds__(kScanThreads)
   grid_dep_wait();
   grid_dep_trigger();
   const int e = threadIdx.x;
+  constexpr int kChunk = 16;  // counts loaded at once (independent loads in flight)
+  // pass 1: the expert's total over all rank blocks
   int total = 0;
   if (e < E) {
-    for (int b = 0; b < nblocks; ++b) {
-      const int c = block_counts[static_cast<size_t>(b) * E + e];
-      block_counts[static_cast<size_t>(b) * E + e] = total;
-      total += c;
+    for (int b0 = 0; b0 < nblocks; b0 += kChunk) {
+      int c[kChunk];
+#pragma unroll
+      for (int j = 0; j < kChunk; ++j)
+        c[j] = b0 + j < nblocks ? block_counts[static_cast<size_t>(b0 + j) * E + e] : 0;
+#pragma unroll
+      for (int j = 0; j < kChunk; ++j) total += c[j];
     }
   }
   int M = 0;
   const int base = block_exclusive_scan(total, scratch, &M);
+  // pass 2: each block's count becomes its first row of the expert's group
   if (e < E) {
     counts[e] = total;
     offsets[e] = base;
-    for (int b = 0; b < nblocks; ++b) block_counts[static_cast<size_t>(b) * E + e] += base;
+    int run = base;
+    for (int b0 = 0; b0 < nblocks; b0 += kChunk) {
+      int c[kChunk];
+#pragma unroll
+      for (int j = 0; j < kChunk; ++j)
+        c[j] = b0 + j < nblocks ? block_counts[static_cast<size_t>(b0 + j) * E + e] : 0;
+#pragma unroll
+      for (int j = 0; j < kChunk; ++j) {
+        if (b0 + j < nblocks) block_counts[static_cast<size_t>(b0 + j) * E + e] = run;
+        run += c[j];
+      }
+    }
   }
   if (e == 0) offsets[E] = M;
   if (mtile_table != nullptr) {

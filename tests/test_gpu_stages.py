@@ -106,6 +106,46 @@ def test_router_logits_and_selection(moe, T, H_, E, dtype, bias):
     assert amb.mean() < 0.02
 
 
+@pytest.mark.parametrize("T,H_,E,K,theta,dup", [
+    (512, 256, 128, 8, 0.0, False),
+    (300, 512, 256, 16, 0.05, True),    # K = 16, gate drop, duplicated experts (exact ties)
+    (256, 128, 48, 6, 0.1, True),       # E = 48: the 64-column tile masks 16 columns
+    (1000, 256, 32, 1, 0.0, False),
+    (384, 128, 64, 4, 0.2, True),
+    (260, 64, 96, 8, 0.0, "all"),       # every expert has the same weights: all logits tie
+])
+def test_tensor_core_router_topk_equals_warp_topk(moe, T, H_, E, K, theta, dup):
+    """The tensor-core router takes the top-k in its epilogue, one thread per token; given
+    the logits it wrote, the ids and gates equal the warp top-k's (moe_route from logits)
+    bit for bit, ties going to the lower expert id."""
+    shape = synth.MoEShape("r", T=T, H=H_, E=E, K=K, I=64, dtype="bf16", bias="normal", seed=5)
+    inp = synth.make_inputs(shape, device="cuda", weights=False)
+    wr = inp["w_router"].clone()
+    bias = inp["router_bias"]
+    if dup == "all":
+        wr[:] = wr[0]
+        bias = None
+    elif dup:
+        wr[1::3] = wr[0::3][: wr[1::3].shape[0]]   # expert 3j+1 copies expert 3j
+        bias = None
+    c = _cfg(moe, T, H_, E, K, theta=theta)
+    logits = torch.empty(T, E, dtype=torch.float32, device="cuda")
+    ids = torch.full((T, K), -9, dtype=torch.int32, device="cuda")
+    w = torch.full((T, K), -9.0, dtype=torch.float32, device="cuda")
+    moe.route(c, inp["x"], wr, bias, logits, ids, w)
+    ids2 = torch.full((T, K), -9, dtype=torch.int32, device="cuda")
+    w2 = torch.full((T, K), -9.0, dtype=torch.float32, device="cuda")
+    moe.route(c, None, None, None, logits, ids2, w2)
+    torch.cuda.synchronize()
+    assert torch.equal(ids, ids2)
+    assert torch.equal(w, w2)
+    if dup == "all":
+        assert (ids.cpu() == torch.arange(K, dtype=torch.int32)).all()
+    b = bias.cpu().numpy() if bias is not None else None
+    L_ref = oracle.router_logits(H.f64(inp["x"]), H.f64(wr), b)
+    assert np.abs(logits.double().cpu().numpy() - L_ref).max() <= 1e-4 * max(1.0, np.abs(L_ref).max())
+
+
 PERMUTE_CASES = [
     # T, E, K, theta, H, skew
     (1, 4, 2, 0.0, 64, "none"), (255, 8, 2, 0.0, 128, "none"), (257, 8, 2, 0.0, 128, "none"),
