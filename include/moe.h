@@ -237,7 +237,10 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
                                size_t ws_bytes, moe_stream_t stream);
 
 /* Intermediates of the last moe_layer_forward that used `ws` (views into ws; valid
- * until ws is reused).  Any output pointer may be NULL.  Useful to check every stage. */
+ * until ws is reused).  Any output pointer may be NULL.  Useful to check every stage.
+ * x_perm is not written by decode-sized bf16 layers (T <= 64, E <= 256, K <= 16), whose
+ * gate/up GEMM gathers token rows from x through perm instead; out_perm is not written
+ * with MOE_FLAG_FUSED_COMBINE. */
 moe_status_t moe_workspace_views(const moe_config_t* cfg, void* ws, float** logits,
                                  int32_t** topk_ids, float** topk_w, int32_t** counts,
                                  int32_t** offsets, int32_t** perm, int32_t** inv,

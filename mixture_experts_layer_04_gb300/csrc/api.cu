@@ -157,6 +157,10 @@ moe_status_t run_route(const moe_config_t* c, const DeviceInfo* d, const void* x
     return cuda_status(launch_topk(logits, 1, nullptr, nullptr, ids, w, c->T, c->E, c->K,
                                    c->gate_threshold, s));
   }
+  if (route_cluster_ok(c->dtype, c->T, c->H, c->E, c->K))  // decode-sized: one cluster
+    return cuda_status(launch_route_cluster(x, w_router, bias, logits, ids, w, c->gate_threshold,
+                                            c->T, c->H, c->E, c->K, nullptr, nullptr, nullptr,
+                                            nullptr, nullptr, nullptr, d->err, s));
   if (use_tc_router(c)) {
     GroupedGemm g{};
     g.mode = kPlain;
@@ -211,6 +215,9 @@ struct Groups {
 // Decode-sized batches: with at most kSwapMaxTokens tokens no group can have more rows
 // than that, so the tensor-core GEMMs put the weights on the 128-row side of the MMA.
 constexpr int kSwapMaxTokens = 128;
+// Batches routed by one cluster launch with at most this many tokens gather token rows in
+// the gate/up GEMM instead of copying them.
+constexpr int kGatherMaxTokens = 16;
 constexpr int kPairMinRowsPerGroup = 768;
 
 moe_status_t launch_gemm(const moe_config_t* c, const DeviceInfo* d, const GroupedGemm& g0,
@@ -576,34 +583,51 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
   const bool simt = cfg->dtype == MOE_F32;
   // the fused combine needs the tensor-core engine; float32 layers keep the gather combine
   const bool fused = (cfg->flags & MOE_FLAG_FUSED_COMBINE) != 0u && !simt;
-  // The gate/up GEMM reads the permuted copy x_perm: its row gather variant
-  // (moe_expert_gate_up_gather, TMA tile::gather4) is exact but measured 2-3x slower on
-  // GB300 than the copy plus whole-tile TMA loads, so the layer does not use it.
+  // Larger batches: the gate/up GEMM reads the permuted copy x_perm.  Its row-gather
+  // variant (TMA tile::gather4, four 128-byte rows per request) measured about 3x slower
+  // than the copy plus whole-tile TMA loads when every group has hundreds of rows.
 
   // 1. router scores, top-k, gate drop
-  int deferred = 0;
-  float* partial = at<float>(ws, p.partial);
-  MOE_TRY(run_route(cfg, d, x, w_router, router_bias, logits, ids, w, partial, true, &deferred, s));
   // 2. dispatch: stable permutation, inverse map, row gather (+ the SIMT m-tile table);
-  //    for small batches the top-k runs inside the same launch
-  if (deferred > 0) {
-    MOE_CUDA(launch_topk_permute_small(partial, deferred, router_bias, logits, ids, w,
-                                       cfg->gate_threshold, cfg->dtype, x, cfg->T, cfg->H, cfg->E,
-                                       cfg->K, counts, offsets, perm, inv, x_perm,
-                                       simt ? table : nullptr, simt ? num_mt : nullptr, kSimtBM,
-                                       fused ? at<float>(ws, p.row_w) : nullptr, s));
+  //    decode-sized bf16 batches do both in one cluster launch, other small batches run
+  //    the top-k inside the permutation's launch
+  float* row_w = fused ? at<float>(ws, p.row_w) : nullptr;
+  // Decode-sized bf16 batches route and dispatch in one cluster launch, and the gate/up
+  // GEMM then gathers each group's token rows from x itself (few rows per group, so the
+  // gather is cheap next to the weight stream): no permuted copy of x is made.
+  const bool cluster = route_cluster_ok(cfg->dtype, cfg->T, cfg->H, cfg->E, cfg->K);
+  const bool gather = cluster && cfg->T <= kGatherMaxTokens;
+  if (cluster) {
+    MOE_CUDA(launch_route_cluster(x, w_router, router_bias, logits, ids, w, cfg->gate_threshold,
+                                  cfg->T, cfg->H, cfg->E, cfg->K, counts, offsets, perm, inv,
+                                  row_w, gather ? nullptr : x_perm, d->err, s));
   } else {
-    MOE_CUDA(launch_permute(cfg->dtype, x, ids, cfg->T, cfg->H, cfg->E, cfg->K, counts, offsets,
-                            perm, inv, x_perm, at<int32_t>(ws, p.perm_ws), simt ? table : nullptr,
-                            simt ? num_mt : nullptr, kSimtBM, w,
-                            fused ? at<float>(ws, p.row_w) : nullptr, s));
+    int deferred = 0;
+    float* partial = at<float>(ws, p.partial);
+    MOE_TRY(run_route(cfg, d, x, w_router, router_bias, logits, ids, w, partial, true, &deferred,
+                      s));
+    if (deferred > 0) {
+      MOE_CUDA(launch_topk_permute_small(partial, deferred, router_bias, logits, ids, w,
+                                         cfg->gate_threshold, cfg->dtype, x, cfg->T, cfg->H,
+                                         cfg->E, cfg->K, counts, offsets, perm, inv, x_perm,
+                                         simt ? table : nullptr, simt ? num_mt : nullptr, kSimtBM,
+                                         row_w, s));
+    } else {
+      MOE_CUDA(launch_permute(cfg->dtype, x, ids, cfg->T, cfg->H, cfg->E, cfg->K, counts,
+                              offsets, perm, inv, x_perm, at<int32_t>(ws, p.perm_ws),
+                              simt ? table : nullptr, simt ? num_mt : nullptr, kSimtBM, w, row_w,
+                              s));
+    }
   }
   // 3-4. grouped SwiGLU FFN of the routed experts
   Groups gr;
   MOE_TRY(routed_groups(cfg, offsets, ws, p, true, s, &gr));
   void* h = at<void>(ws, p.h);
   const int rows = cfg->T * cfg->K;
-  MOE_TRY(run_gate_up(cfg, d, x_perm, rows, w_gate_up, cfg->I, h, gr, s));
+  if (gather)
+    MOE_TRY(run_gate_up(cfg, d, x, rows, w_gate_up, cfg->I, h, gr, s, perm));
+  else
+    MOE_TRY(run_gate_up(cfg, d, x_perm, rows, w_gate_up, cfg->I, h, gr, s));
   if (fused) {
     // 5'. shared expert written straight into the fp32 sum (or the sum zeroed), then the
     //     down projection adds every routed row, scaled by its gate, into its token's row,

@@ -513,9 +513,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         int g, row0, row_end, n_tile;
         decode_tile(p, s_off, s_mt, num_mt, kTileRows, idx, g, row0, row_end, n_tile);
         const int n0 = n_tile * Cfg::kColsOut;  // first weight row of the tile
+        // With a row gather only the lanes whose four rows start inside the group load
+        // anything: the rest of the tile's rows are never stored, so whatever an earlier
+        // stage left in that part of the buffer is harmless.  Within a lane, rows past
+        // the group's end repeat a row of the tile.
+        const int live_rows = min(row_end - row0, kTileRows);
+        const int gather_lanes = GATHER ? (live_rows + 3) / 4 : 0;
+        const uint32_t stage_tx =
+            GATHER ? static_cast<uint32_t>(Cfg::kWgtBytes + gather_lanes * 512) : Cfg::kStageBytes;
         int src[4] = {0, 0, 0, 0};
-        if (GATHER && lane < kGatherLanes) {
-          // rows past the group's end repeat a row of the tile: computed, never stored
+        if (GATHER && lane < gather_lanes) {
           const int pad = p.gather_rows[row0];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -535,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a_dst = smem_u32(sAct + stage * Cfg::kActBytes);
           const uint32_t w_dst = smem_u32(sWgt + stage * Cfg::kWgtBytes);
           if (leader) {
-            mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
+            mbar_arrive_expect_tx(fb, stage_tx);
             if constexpr (!GATHER) tma_load_2d(a_dst, &p.tmAct, fb, kb * BK, row0);
             tma_load_3d(w_dst, &p.tmWgt, fb, kb * BK, n0, g);
             if constexpr (MODE == kSwiGLU)
@@ -543,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if constexpr (GATHER) {
             __syncwarp();
-            if (lane < kGatherLanes)
+            if (lane < gather_lanes)
               tma_gather4(a_dst + 512u * lane, &p.tmAct, fb, kb * BK, src[0], src[1], src[2],
                           src[3]);
           }
@@ -1085,6 +1092,11 @@ cudaError_t launch_pair(const GroupedGemm& g, unsigned* err, int num_sms, cudaSt
                     p);
 }
 }  // namespace
+
+bool make_tma_2d_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                      uint32_t box_rows) {
+  return make_map_2d(m, base, rows, cols, box_rows);
+}
 
 int tc_swap_tokens(int max_rows_per_group) {
   if (max_rows_per_group <= 16) return 16;

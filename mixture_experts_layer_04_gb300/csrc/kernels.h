@@ -52,6 +52,22 @@ int router_slices(int T, int H, int E, int dtype);
 cudaError_t launch_router_partial(int dtype, const void* x, const void* w_router, float* partial,
                                   int S, int T, int H, int E, cudaStream_t s);
 
+// Decode-sized bf16 batches (T <= 64, E <= 256, K <= 16): router logits on the tensor
+// core, top-k, gate drop and (when `counts` is non-null) the whole dispatch permutation,
+// in one launch of one thread-block cluster (route_cluster.cu).  Token rows are copied
+// into x_perm unless it is null (the gate/up GEMM then gathers them from x).  CTA 0 also
+// sets zero[0..n_zero) to zero (the stream-K flags of the GEMMs that follow), if non-null.
+bool route_cluster_ok(int dtype, int T, int H, int E, int K);
+cudaError_t launch_route_cluster(const void* x, const void* w_router, const float* bias,
+                                 float* logits, int32_t* ids, float* w, float theta, int T, int H,
+                                 int E, int K, int32_t* counts, int32_t* offsets, int32_t* perm,
+                                 int32_t* inv, float* row_w, void* x_perm, unsigned* err,
+                                 cudaStream_t s);
+// 2D TMA map of a row-major bf16 [rows, cols] matrix, box = 64 columns x box_rows rows,
+// 128-byte swizzle (gemm_tc.cu).
+bool make_tma_2d_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                      uint32_t box_rows);
+
 // Top-k, softmax over the kept logits and gate drop, one warp per token.  The logits are
 // the sum of S partial slices [S][T][E] (S = 1: plain logits) plus `bias` (may be null);
 // they are written to `logits_out` when non-null (which may alias `partial` if S == 1).
@@ -150,6 +166,7 @@ struct GroupedGemm {
   int32_t* topk_ids;
   float* topk_w;
 };
+
 
 cudaError_t launch_grouped_gemm_simt(const GroupedGemm& g, cudaStream_t s);
 cudaError_t launch_grouped_gemm_tc(const GroupedGemm& g, unsigned* err, int num_sms,

@@ -33,26 +33,55 @@ __device__ __forceinline__ void warp_topk_softmax(const float* L, int E, int K, 
   float my_v = 0.f;
   int my_e = -1;
   float v0 = 0.f;
-  for (int k = 0; k < K; ++k) {
-    unsigned long long best = 0ull;
-    for (int j = 0, e = lane; e < E; ++j, e += 32) {
-      if (taken & (1u << j)) continue;
-      unsigned long long key = (static_cast<unsigned long long>(float_key(L[e])) << 32) |
-                               static_cast<uint32_t>(~static_cast<uint32_t>(e));
-      best = key > best ? key : best;
-    }
+  if (E <= 256) {
+    // up to 8 candidates per lane, keys kept in registers for all K rounds
+    uint32_t key[8];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
-      best = other > best ? other : best;
+    for (int j = 0; j < 8; ++j) key[j] = lane + 32 * j < E ? float_key(L[lane + 32 * j]) : 0u;
+    for (int k = 0; k < K; ++k) {
+      // this lane's best untaken candidate (the first of equal keys is the lower id), then
+      // the warp's largest key and, among the lanes holding it, the lowest expert id
+      uint32_t kbest = 0u, ebest = 0xffffffffu;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const bool live = lane + 32 * j < E && !(taken & (1u << j));
+        if (live && (key[j] > kbest || ebest == 0xffffffffu)) {
+          kbest = key[j];
+          ebest = static_cast<uint32_t>(lane + 32 * j);
+        }
+      }
+      const uint32_t kmax = __reduce_max_sync(0xffffffffu, ebest != 0xffffffffu ? kbest : 0u);
+      const int e_win = static_cast<int>(__reduce_min_sync(
+          0xffffffffu, (ebest != 0xffffffffu && kbest == kmax) ? ebest : 0xffffffffu));
+      if ((e_win & 31) == lane) taken |= 1u << (e_win >> 5);
+      const float v_win = L[e_win];
+      if (k == 0) v0 = v_win;
+      if (lane == k) {
+        my_v = v_win;
+        my_e = e_win;
+      }
     }
-    const int e_win = static_cast<int>(~static_cast<uint32_t>(best & 0xffffffffull));
-    if ((e_win & 31) == lane) taken |= 1u << (e_win >> 5);
-    const float v_win = L[e_win];
-    if (k == 0) v0 = v_win;
-    if (lane == k) {
-      my_v = v_win;
-      my_e = e_win;
+  } else {
+    for (int k = 0; k < K; ++k) {
+      uint32_t kbest = 0u, ebest = 0xffffffffu;
+      for (int j = 0, e = lane; e < E; ++j, e += 32) {
+        if (taken & (1u << j)) continue;
+        const uint32_t kk = float_key(L[e]);
+        if (kk > kbest || ebest == 0xffffffffu) {
+          kbest = kk;
+          ebest = static_cast<uint32_t>(e);
+        }
+      }
+      const uint32_t kmax = __reduce_max_sync(0xffffffffu, ebest != 0xffffffffu ? kbest : 0u);
+      const int e_win = static_cast<int>(__reduce_min_sync(
+          0xffffffffu, (ebest != 0xffffffffu && kbest == kmax) ? ebest : 0xffffffffu));
+      if ((e_win & 31) == lane) taken |= 1u << (e_win >> 5);
+      const float v_win = L[e_win];
+      if (k == 0) v0 = v_win;
+      if (lane == k) {
+        my_v = v_win;
+        my_e = e_win;
+      }
     }
   }
   float z = (lane < K) ? expf(my_v - v0) : 0.f;

@@ -311,3 +311,70 @@ def test_combine(moe, T, H_, E, K, shared, dtype):
                          s.double().numpy() if shared else None)
     H.assert_close_y(y32.double().cpu().numpy(), ref, max_abs=1e-5, rel_l2=1e-6, what="combine")
     assert torch.equal(y, y32.to(tdt))
+
+
+CLUSTER_CASES = [
+    # T, H, E, K, theta, bias, dup   (bf16, T <= 64, E <= 256: one cluster launch)
+    (1, 2048, 128, 8, 0.0, "normal", False),
+    (64, 2048, 128, 8, 0.0, "normal", False),
+    (33, 256, 40, 6, 0.1, "normal", False),    # E not a multiple of 16; 4 k-blocks, most CTAs none
+    (17, 1024, 256, 16, 0.05, "zipf", False),  # two 128-expert tiles, K = 16, gate drop
+    (64, 7168, 256, 8, 0.05, "zipf", False),   # 7 k-blocks per CTA through the stage ring
+    (8, 64, 8, 2, 0.0, "none", False),         # one k-block for the whole cluster
+    (48, 512, 96, 8, 0.0, "none", True),       # exact ties between duplicated experts
+]
+
+
+@pytest.mark.parametrize("T,H_,E,K,theta,bias,dup", CLUSTER_CASES)
+def test_cluster_route_and_dispatch(moe, T, H_, E, K, theta, bias, dup):
+    """Decode-sized bf16 batches route and dispatch in one cluster launch.  Its logits match
+    the oracle's within fp32 accumulation error; given those logits, its ids and gates equal
+    the warp top-k's (moe_route from logits) bit for bit; counts, offsets, perm and inv
+    equal moe_permute's on the same ids bit for bit; and the layer output, whose gate/up
+    GEMM gathers token rows through perm, matches the oracle."""
+    shape = synth.MoEShape("c", T=T, H=H_, E=E, K=K, I=64, theta=theta, dtype="bf16", bias=bias,
+                           seed=21)
+    inp = synth.make_inputs(shape, device="cuda")
+    if dup:
+        inp["w_router"][1::2] = inp["w_router"][0::2][: inp["w_router"][1::2].shape[0]]
+    run = H.LayerRun(moe, shape, inp)
+    run.run()
+    moe.sync_check()
+    r = run.routing()
+    b = inp["router_bias"].cpu().numpy() if inp["router_bias"] is not None else None
+    L_ref = oracle.router_logits(H.f64(inp["x"]), H.f64(inp["w_router"]), b)
+    assert np.abs(r["logits"] - L_ref).max() <= 1e-4 * max(1.0, np.abs(L_ref).max())
+    # the top-k taken on the cluster's own logits
+    c = _cfg(moe, T, H_, E, K, theta=theta)
+    lg = torch.from_numpy(r["logits"]).cuda()
+    ids2 = torch.empty(T, K, dtype=torch.int32, device="cuda")
+    w2 = torch.empty(T, K, dtype=torch.float32, device="cuda")
+    moe.route(c, None, None, None, lg, ids2, w2)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(r["ids"], ids2.cpu().numpy())
+    np.testing.assert_array_equal(r["w"], w2.cpu().numpy())
+    # the permutation of those ids
+    ws = torch.empty(moe.workspace_size(c), dtype=torch.uint8, device="cuda")
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    perm = torch.full((T * K,), -7, dtype=torch.int32, device="cuda")
+    inv = torch.empty(T * K, dtype=torch.int32, device="cuda")
+    xp = torch.zeros(T * K, H_, dtype=torch.bfloat16, device="cuda")
+    moe.permute(c, inp["x"], ids2, counts, offsets, perm, inv, xp, ws)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(r["counts"], counts.cpu().numpy())
+    np.testing.assert_array_equal(r["offsets"], offsets.cpu().numpy())
+    M = int(r["offsets"][-1])
+    np.testing.assert_array_equal(r["perm"][:M], perm.cpu().numpy()[:M])
+    np.testing.assert_array_equal(r["inv"].reshape(-1), inv.cpu().numpy())
+    # the layer output: the gate/up GEMM gathers each group's rows from x through perm
+    ref = oracle.moe_layer(H.f64(inp["x"]), H.f64(inp["w_router"]), H.f64(inp["w_gate_up"]),
+                           H.f64(inp["w_down"]), K, theta, b)
+    ok = ~H.ambiguous_tokens(ref["logits"], K, theta, ref["w"])
+    H.assert_close_y(run.y32.double().cpu().numpy()[ok], ref["y"][ok])
+    # the routing against the oracle's, on the oracle's logits
+    L32 = L_ref.astype(np.float32)
+    ids_ref, w_ref = oracle.route(L32, K, theta)
+    amb = H.compare_routing(L32, r["ids"], r["w"], ids_ref, w_ref, K, theta)
+    if not dup:  # duplicated experts tie in every token: only validity is checked there
+        assert amb.sum() <= max(1, 0.05 * T)
