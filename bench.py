@@ -61,7 +61,8 @@ def parse():
                     help="replay the layer from a CUDA graph (default: on for T <= 128)")
     ap.add_argument("--no-graph", dest="graph", action="store_false")
     ap.add_argument("--fused-combine", dest="fused", action="store_true", default=None,
-                    help="fuse the combine into the down GEMM (MOE_FLAG_FUSED_COMBINE)")
+                    help="fuse the combine into the down GEMM (MOE_FLAG_FUSED_COMBINE; "
+                         "default for K >= 8)")
     ap.add_argument("--gather-combine", dest="fused", action="store_false")
     ap.add_argument("--time-row-gather", action="store_true",
                     help="also time the row-gather gate/up variant as a stage")
@@ -149,7 +150,8 @@ def gate_up_kernel(shape, T):
     if T <= 128:
         bt = 16 if T <= 16 else 32 if T <= 32 else 64
         return f"tc_grouped_gemm_kernel<{bt},SwiGLU,swap> (moe_expert_gate_up)"
-    if T * shape.K >= 768 * shape.E:
+    rows = T * shape.K // shape.E
+    if rows >= 768 or (rows >= 256 and (shape.H >= 4096 or shape.I >= 4096)):
         return "tc_pair_gemm_kernel<SwiGLU> (moe_expert_gate_up)"
     return "tc_grouped_gemm_kernel<256,SwiGLU> (moe_expert_gate_up)"
 
@@ -187,6 +189,13 @@ def kernel_launches_per_step(shape, T):
     tc_router = shape.dtype == "bf16" and T >= 256 and E >= 32 and E % 16 == 0
     wsmem_router = E <= 16 and E * H * b <= 96 * 1024 and T >= 64
     fused_small = T <= 64 and (E * 8 * 4 + (2 * E + 1) * 4 + T * K * 12 + T * E * 4) <= 200 * 1024
+    cluster = shape.dtype == "bf16" and T <= 64 and E <= 256 and K <= 16
+    if cluster:
+        n += 2                            # routing + permutation in one cluster launch; gate/up
+        n += 1                            # down
+        if shape.I_shared:
+            n += 2
+        return n + 1                      # combine
     if tc_router:
         n += 1 if E <= 256 else 2         # router GEMM (top-k in its epilogue up to 256 experts)
     elif wsmem_router:
@@ -225,7 +234,9 @@ def run_ours(args, rank, world, local):
     T = args.tokens if args.tokens is not None else shape.T
     inp = synth.make_inputs(shape.with_(seed=shape.seed + rank), device=dev, T=T)
     dt = moe.BF16 if shape.dtype == "bf16" else moe.F32
-    fused = bool(args.fused) if args.fused is not None else False
+    # default: the fp32 scatter-add combine fused into the down GEMM when each token has
+    # many (K >= 8) contributions to add, the deterministic gather combine otherwise
+    fused = bool(args.fused) if args.fused is not None else (shape.K >= 8 and shape.dtype == "bf16")
     flags = moe.FLAG_FUSED_COMBINE if fused else 0
     cfg = moe.MoEConfig.make(T, shape.H, shape.E, shape.K, shape.I, shape.I_shared, shape.theta, dt,
                              flags)

@@ -219,16 +219,22 @@ constexpr int kSwapMaxTokens = 128;
 // the gate/up GEMM instead of copying them.
 constexpr int kGatherMaxTokens = 16;
 constexpr int kPairMinRowsPerGroup = 768;
+constexpr int kPairWideDim = 4096;
 
 moe_status_t launch_gemm(const moe_config_t* c, const DeviceInfo* d, const GroupedGemm& g0,
                          cudaStream_t s) {
   if (c->dtype == MOE_BF16) {
     GroupedGemm g = g0;
     g.swap_tokens = c->T <= kSwapMaxTokens ? c->T : 0;
-    // large groups (>= 768 rows on average) run on CTA pairs with 256-row tiles; smaller,
-    // ragged groups keep 128-row tiles (less padding in each group's last tile)
-    g.pair = (g.swap_tokens == 0 && g.rows_alloc >= kPairMinRowsPerGroup * g.G &&
-              g.gather_rows == nullptr) ? 1 : 0;
+    // CTA pairs (256-row tiles, 2/3 of the shared-memory traffic per MMA) pay for the
+    // padding of each group's last tile when groups are large (>= 768 rows on average),
+    // or half that size with a long reduction or a wide output to amortise it; otherwise
+    // single CTAs with 128-row tiles (measured on GB300 with the workloads' groups)
+    const long long rows_per_group = g.rows_alloc / (g.G > 0 ? g.G : 1);
+    const bool big = rows_per_group >= kPairMinRowsPerGroup ||
+                     (rows_per_group >= kPairMinRowsPerGroup / 3 &&
+                      (g.Kd >= kPairWideDim || g.N_out >= kPairWideDim));
+    g.pair = (g.swap_tokens == 0 && big && g.gather_rows == nullptr) ? 1 : 0;
     return cuda_status(launch_grouped_gemm_tc(g, d->err, d->num_sms, s));
   }
   return cuda_status(launch_grouped_gemm_simt(g0, s));

@@ -262,12 +262,12 @@ __device__ __forceinline__ void epilogue_rows(const TcParams& p, uint32_t t_row,
         for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * rw);
       }
       if (p.col_bias != nullptr) {
+        // one coalesced load of the chunk's 32 biases, then broadcast by shuffles
+        const int bc = col0 + c + lane;
+        const float bl = bc < p.N_out ? __ldg(p.col_bias + bc) : 0.f;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int col = col0 + c + j;
-          const float b = col < p.N_out ? __ldg(p.col_bias + col) : 0.f;
-          r[j] = __float_as_uint(__uint_as_float(r[j]) + b);
-        }
+        for (int j = 0; j < 32; ++j)
+          r[j] = __float_as_uint(__uint_as_float(r[j]) + __shfl_sync(0xffffffffu, bl, j));
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u)
@@ -304,18 +304,20 @@ __device__ __forceinline__ float butterfly_sum16(const float (&z)[16]) {
 
 // kTopK epilogue (router logits): each thread owns one token row of the tile, which spans
 // all N_out experts.  The logits (+ bias) are stored as in kPlain, and on the way the
-// thread keeps the 16 best (logit, expert) pairs in registers, sorted by logit descending
-// and expert ascending on ties (the warp top-k's order).  Then the softmax over the K
-// kept logits, the gate drop and the renormalisation, as the warp top-k computes them.
-template <int BN>
+// thread keeps the KS >= K best (logit, expert) pairs in registers, sorted by logit
+// descending and expert ascending on ties (the warp top-k's order); KS is the smallest of
+// 2, 4, 8, 16 that holds K, so the insertion costs no more slots than needed.  Then the
+// softmax over the K kept logits, the gate drop and the renormalisation, as the warp
+// top-k computes them (the same sums in the same order).
+template <int BN, int KS>
 __device__ __forceinline__ void epilogue_topk(const TcParams& p, uint32_t t_row, uint32_t stg,
                                               int lane, int tile_row0, int row_end) {
   float* C = static_cast<float*>(p.C);
   const int K = p.topk_k;
-  uint32_t kk[16];
-  int ki[16];
+  uint32_t kk[KS];
+  int ki[KS];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
+  for (int j = 0; j < KS; ++j) {
     kk[j] = 0u;  // below the key of every non-NaN float
     ki[j] = -1;
   }
@@ -327,12 +329,11 @@ __device__ __forceinline__ void epilogue_topk(const TcParams& p, uint32_t t_row,
     tmem_ld_32x32b_x32(t_row + c, r);
     tmem_ld_wait();
     if (p.col_bias != nullptr) {
+      // one coalesced load of the chunk's 32 biases, then broadcast by shuffles
+      const float bl = c + lane < p.N_out ? __ldg(p.col_bias + c + lane) : 0.f;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int col = c + j;
-        const float b = col < p.N_out ? __ldg(p.col_bias + col) : 0.f;
-        r[j] = __float_as_uint(__uint_as_float(r[j]) + b);
-      }
+      for (int j = 0; j < 32; ++j)
+        r[j] = __float_as_uint(__uint_as_float(r[j]) + __shfl_sync(0xffffffffu, bl, j));
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u)
@@ -356,44 +357,48 @@ __device__ __forceinline__ void epilogue_topk(const TcParams& p, uint32_t t_row,
       const uint32_t vv[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
-      const int col = c + 4 * u + t;
-      const uint32_t key = float_key(__uint_as_float(vv[t]));
-      if (col < p.N_out && key > thr) {  // enters the top K: insertion into the sorted 16
+        const int col = c + 4 * u + t;
+        const uint32_t key = float_key(__uint_as_float(vv[t]));
+        if (col < p.N_out && key > thr) {  // enters the top K: insertion into the sorted KS
 #pragma unroll
-        for (int q = 15; q >= 1; --q) {  // selects only: every slot stays in a register
-          const bool shift = key > kk[q - 1];
-          const bool here = key > kk[q];
-          kk[q] = shift ? kk[q - 1] : (here ? key : kk[q]);
-          ki[q] = shift ? ki[q - 1] : (here ? col : ki[q]);
+          for (int q = KS - 1; q >= 1; --q) {  // selects only: every slot stays in a register
+            const bool shift = key > kk[q - 1];
+            const bool here = key > kk[q];
+            kk[q] = shift ? kk[q - 1] : (here ? key : kk[q]);
+            ki[q] = shift ? ki[q - 1] : (here ? col : ki[q]);
+          }
+          const bool first = key > kk[0];
+          kk[0] = first ? key : kk[0];
+          ki[0] = first ? col : ki[0];
+          if (K == KS) {
+            thr = kk[KS - 1];
+          } else {  // the K-th key, picked with a one-hot mask (no indexed access)
+            uint32_t t_new = 0u;
+#pragma unroll
+            for (int q = 0; q < KS; ++q) t_new |= kk[q] & ((kmask >> q) & 1u ? 0xffffffffu : 0u);
+            thr = t_new;
+          }
         }
-        const bool first = key > kk[0];
-        kk[0] = first ? key : kk[0];
-        ki[0] = first ? col : ki[0];
-        // the K-th key, picked with a precomputed one-hot mask (no indexed access)
-        uint32_t t_new = 0u;
-#pragma unroll
-        for (int q = 0; q < 16; ++q) t_new |= kk[q] & ((kmask >> q) & 1u ? 0xffffffffu : 0u);
-        thr = t_new;
-      }
       }
     }
   }
   const int grow = tile_row0 + lane;
   if (grow >= row_end) return;
-  // keys back to logits (float_key is monotone; -0 came in as +0)
-  float z[16], lv[16];
+  // keys back to logits (float_key is monotone; -0 came in as +0); the sums below run
+  // over 16 terms (zeros past K) in the warp top-k's butterfly order
+  float z[16], lv[KS];
 #pragma unroll
-  for (int q = 0; q < 16; ++q)
+  for (int q = 0; q < KS; ++q)
     lv[q] = __uint_as_float((kk[q] & 0x80000000u) ? (kk[q] & 0x7fffffffu) : ~kk[q]);
 #pragma unroll
-  for (int q = 0; q < 16; ++q) z[q] = q < K ? expf(lv[q] - lv[0]) : 0.f;
+  for (int q = 0; q < 16; ++q) z[q] = (q < KS && q < K) ? expf(lv[q < KS ? q : 0] - lv[0]) : 0.f;
   const float s = butterfly_sum16(z);
   float w[16];
 #pragma unroll
   for (int q = 0; q < 16; ++q) w[q] = z[q] / s;
   if (p.topk_theta > 0.f) {
 #pragma unroll
-    for (int q = 1; q < 16; ++q)
+    for (int q = 1; q < KS; ++q)
       if (q < K && w[q] < p.topk_theta) {
         w[q] = 0.f;
         ki[q] = -1;
@@ -405,7 +410,7 @@ __device__ __forceinline__ void epilogue_topk(const TcParams& p, uint32_t t_row,
   int32_t* ids = p.topk_ids + static_cast<size_t>(grow) * K;
   float* wo = p.topk_w + static_cast<size_t>(grow) * K;
 #pragma unroll
-  for (int q = 0; q < 16; ++q)
+  for (int q = 0; q < KS; ++q)
     if (q < K) {
       ids[q] = ki[q];
       wo[q] = w[q];
@@ -649,9 +654,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t stg =
             smem_u32(sStg) + static_cast<uint32_t>((warp - 2) * 32 * (MODE == kSwiGLU ? 64 : 128));
         const int tile_row0 = row0 + quad * 32;  // first global row of this warp's 32 rows
-        if constexpr (MODE == kTopK)
-          epilogue_topk<BN>(p, t_row, stg, lane, tile_row0, row_end);
-        else
+        if constexpr (MODE == kTopK) {
+          if (p.topk_k <= 2)
+            epilogue_topk<BN, 2>(p, t_row, stg, lane, tile_row0, row_end);
+          else if (p.topk_k <= 4)
+            epilogue_topk<BN, 4>(p, t_row, stg, lane, tile_row0, row_end);
+          else if (p.topk_k <= 8)
+            epilogue_topk<BN, 8>(p, t_row, stg, lane, tile_row0, row_end);
+          else
+            epilogue_topk<BN, 16>(p, t_row, stg, lane, tile_row0, row_end);
+        } else
           epilogue_rows<BN, MODE>(p, t_row, stg, lane, tile_row0, row_end, col0);
       } else {
         // swapped: lane = weight row of the tile, column j = token row0 + j
