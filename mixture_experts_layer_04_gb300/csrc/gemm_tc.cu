@@ -185,6 +185,20 @@ __device__ __forceinline__ void red_add_f32(float* p, float v) {
 
 // Barrier among the four epilogue warps only (named barrier 1, 128 threads).
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Barrier of the four epilogue warps that also returns, to every one of them, whether
+// any thread passed `pred` true: a decision to leave the tile loop taken by all or none
+// (a plain barrier followed by separate reads of the abort flag could split the warps
+// if the flag is set in between, and the next barrier would then never fill).
+__device__ __forceinline__ bool epi_bar_any(bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred p, 1, 128, q;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(out)
+      : "r"(pred ? 1u : 0u)
+      : "memory");
+  return out != 0u;
+}
 
 // Reads NC (16 or 32) consecutive columns of this warp's 32 TMEM lanes into v[0..NC).
 template <int NC>
@@ -641,8 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool ready = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.err);
       if constexpr (SWAP && MODE == kSwiGLU) {
         // the four epilogue warps meet at named barriers below: leave together or not at all
-        epi_bar();
-        if (*abort_flag) break;
+        if (epi_bar_any(!ready || *abort_flag != 0)) break;
       } else if (!ready) {
         break;
       }

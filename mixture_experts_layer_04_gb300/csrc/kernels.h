@@ -55,8 +55,7 @@ cudaError_t launch_router_partial(int dtype, const void* x, const void* w_router
 // Decode-sized bf16 batches (T <= 64, E <= 256, K <= 16): router logits on the tensor
 // core, top-k, gate drop and (when `counts` is non-null) the whole dispatch permutation,
 // in one launch of one thread-block cluster (route_cluster.cu).  Token rows are copied
-// into x_perm unless it is null (the gate/up GEMM then gathers them from x).  CTA 0 also
-// sets zero[0..n_zero) to zero (the stream-K flags of the GEMMs that follow), if non-null.
+// into x_perm unless it is null (the gate/up GEMM then gathers them from x).
 bool route_cluster_ok(int dtype, int T, int H, int E, int K);
 cudaError_t launch_route_cluster(const void* x, const void* w_router, const float* bias,
                                  float* logits, int32_t* ids, float* w, float theta, int T, int H,

@@ -80,6 +80,14 @@ SMALL = [
                        seed=6),
         synth.MoEShape("f32_shared", T=100, H=128, E=6, K=2, I=64, I_shared=128, theta=0.2,
                        dtype="f32", bias="normal", seed=2),
+        # decode-sized batches (one-cluster routing, swapped GEMMs): every token-tile width
+        # (16, 32, 64), a row gather and a copy of x, ragged I, a shared expert
+        synth.MoEShape("decode_t1_tiny", T=1, H=256, E=8, K=2, I=64, seed=7),
+        synth.MoEShape("decode_t3_ragged", T=3, H=1024, E=16, K=4, I=320, bias="normal", seed=8),
+        synth.MoEShape("decode_t24", T=24, H=512, E=32, K=8, I=192, theta=0.05, bias="zipf",
+                       seed=10),
+        synth.MoEShape("decode_t64", T=64, H=2048, E=64, K=4, I=128, I_shared=64, bias="normal",
+                       seed=11),
 ]
 
 
@@ -192,6 +200,25 @@ def test_deterministic(moe):
     a.run()
     torch.cuda.synchronize()
     assert torch.equal(a.y, b.y) and torch.equal(a.y32, b.y32)
+
+
+@pytest.mark.parametrize("T", [1, 8, 64])
+def test_deterministic_decode(moe, T):
+    """Decode-sized layers (one-cluster routing, swapped GEMMs) are bitwise repeatable."""
+    shape = synth.WORKLOADS["qwen_decode"]
+    inp = synth.make_inputs(shape, device="cuda", T=T)
+    for flags in (0, moe.FLAG_FUSED_COMBINE):
+        a = H.LayerRun(moe, shape, inp, flags=flags)
+        b = H.LayerRun(moe, shape, inp, flags=flags)
+        a.run()
+        b.run()
+        a.run()
+        torch.cuda.synchronize()
+        moe.sync_check()
+        if flags == 0:
+            assert torch.equal(a.y, b.y) and torch.equal(a.y32, b.y32)
+        else:  # the fused combine adds rows at L2 in no fixed order
+            assert (a.y32 - b.y32).abs().max().item() <= 1e-5 * max(1.0, a.y32.abs().max().item())
 
 
 @pytest.mark.parametrize("case", ["T0", "T1", "K_eq_E", "one_expert", "empty_experts"])
