@@ -364,29 +364,34 @@ __global__ void __launch_bounds__(kRcThreads, 1)
       }
     }
   }
-  // row copies: warp (c, w) reads token row t = c*8 + w (+ multiples of the cluster's
-  // warps) once, in bursts of 8 independent 16-byte loads per lane, and writes it to each
-  // of the token's K rows
+  // row copies: the T*K kept assignments are dealt to all warps of the cluster, two at a
+  // time per warp (both rows' loads in flight, then both rows' stores), so every SM of the
+  // cluster shares the stores; each lane moves 16-byte units in bursts of 4 per row
   if (p.x_perm != nullptr) {
     const int row_units = p.H / 8;
-    constexpr int kBurst = 8;
-    for (int t = c * kRcWarps + warp; t < p.T; t += nc * kRcWarps) {
-      const uint4* src = p.x + static_cast<size_t>(t) * row_units;
+    constexpr int kBurst = 4;
+    const int nw = nc * kRcWarps;
+    for (int a0 = c * kRcWarps + warp; a0 < TK; a0 += 2 * nw) {
+      const int a1 = a0 + nw;
+      const int r0 = rows[a0], r1 = a1 < TK ? rows[a1] : -1;
+      const uint4* s0 = p.x + static_cast<size_t>(a0 / p.K) * row_units;
+      const uint4* s1 = p.x + static_cast<size_t>((a1 < TK ? a1 : a0) / p.K) * row_units;
       for (int i0 = 0; i0 < row_units; i0 += 32 * kBurst) {
-        uint4 v[kBurst];
+        uint4 v0[kBurst], v1[kBurst];
 #pragma unroll
         for (int b = 0; b < kBurst; ++b) {
           const int i = i0 + b * 32 + lane;
-          if (i < row_units) v[b] = __ldg(src + i);
+          if (i < row_units) {
+            if (r0 >= 0) v0[b] = __ldg(s0 + i);
+            if (r1 >= 0) v1[b] = __ldg(s1 + i);
+          }
         }
-        for (int k = 0; k < p.K; ++k) {
-          const int r = rows[t * p.K + k];
-          if (r < 0) continue;
-          uint4* dst = p.x_perm + static_cast<size_t>(r) * row_units;
 #pragma unroll
-          for (int b = 0; b < kBurst; ++b) {
-            const int i = i0 + b * 32 + lane;
-            if (i < row_units) dst[i] = v[b];
+        for (int b = 0; b < kBurst; ++b) {
+          const int i = i0 + b * 32 + lane;
+          if (i < row_units) {
+            if (r0 >= 0) p.x_perm[static_cast<size_t>(r0) * row_units + i] = v0[b];
+            if (r1 >= 0) p.x_perm[static_cast<size_t>(r1) * row_units + i] = v1[b];
           }
         }
       }
