@@ -58,6 +58,13 @@ constexpr int kMaxGroups = 1024;
 
 struct TcParams {
   CUtensorMap tmAct;  // [rows_alloc, Kd] activations (token rows)
+  // CTA pairs only, for tail tiles in swapped order: the activations in boxes of 16, 32
+  // and 64 rows, and (SwiGLU) the weights as [G][2][I][Kd] in boxes of 64 gate rows plus
+  // the 64 matching up rows
+  CUtensorMap tmActS16;
+  CUtensorMap tmActS32;
+  CUtensorMap tmActS64;
+  CUtensorMap tmWgtS;
   CUtensorMap tmWgt;  // [G, Nb, Kd] weights
   void* C;
   const float* col_bias;
@@ -764,6 +771,81 @@ __global__ void __launch_bounds__(kThreads, 1)
 //   * both CTAs' epilogue warps arrive on the even CTA's tmem-empty barrier (count 8);
 //   * a cluster barrier after initialisation and before TMEM release keeps every
 //     remote arrive and shared-memory read inside the peer's lifetime.
+// A group's last tile holds r < 256 rows.  Padded to 256 token rows it costs a full pair
+// step (512 MMA rows x 256 columns per k-block); in swapped order (the tile's 256 weight
+// rows on the MMA's M side, 128 per CTA, and its r token rows, rounded up to N, a multiple
+// of 32, as the MMA's N split 2 x N/2 between the CTAs) a k-block moves 16 KB + 64 N bytes
+// per CTA instead of 32 KB.  Tails up to kPairTailMaxN rows are run that way.
+constexpr int kPairTailMaxN = 192;
+
+__device__ __forceinline__ int pair_tail_n(int row0, int row_end) {
+  const int r = row_end - row0;
+  if (r >= 256) return 0;
+  const int n = (r + 31) / 32 * 32;
+  return n <= kPairTailMaxN ? n : 0;
+}
+
+// Epilogue of a swapped pair tail (see pair_tail_n) in one CTA of the pair: TMEM lane L
+// (quad * 32 + lane) is weight row L of this CTA's 128, accumulator column j is token row
+// row0 + j (j < tn).  SwiGLU: lanes 0-63 hold gate rows n0 + 64 rank + L, lanes 64-127 the
+// matching up rows, whose values reach the gate lanes through `stg` (64 x 32 floats per
+// round).  Plain / scatter: lane L is output column n0 + 128 rank + L.
+template <int MODE>
+__device__ __forceinline__ void epilogue_pair_tail(const TcParams& p, uint32_t t_row, uint8_t* stg,
+                                                   int quad, int lane, int rank, int tn, int row0,
+                                                   int row_end, int n0) {
+  const int L = quad * 32 + lane;
+  if constexpr (MODE == kSwiGLU) {
+    float* xchg = reinterpret_cast<float*>(stg);  // [64][32], rotated by row
+    __nv_bfloat16* C = static_cast<__nv_bfloat16*>(p.C);
+    const int col = n0 + 64 * rank + (L & 63);
+#pragma unroll 1
+    for (int c = 0; c < tn; c += 32) {
+      float v[32];
+      if (quad >= 2) {
+        const int r = L - 64;
+        tmem_ld_cols<32>(t_row + c, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) xchg[r * 32 + ((j + r) & 31)] = v[j];
+      }
+      epi_bar();
+      if (quad < 2) {
+        tmem_ld_cols<32>(t_row + c, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int tok = row0 + c + j;
+          if (tok < row_end && col < p.N_out) {
+            const float u = xchg[L * 32 + ((j + L) & 31)];
+            C[static_cast<size_t>(tok) * p.N_out + col] = __float2bfloat16_rn(silu_f(v[j]) * u);
+          }
+        }
+      }
+      epi_bar();
+    }
+  } else {
+    float* C = static_cast<float*>(p.C);
+    const int col = n0 + 128 * rank + L;
+    const float b = (p.col_bias != nullptr && col < p.N_out) ? __ldg(p.col_bias + col) : 0.f;
+#pragma unroll 1
+    for (int c = 0; c < tn; c += 32) {
+      float v[32];
+      tmem_ld_cols<32>(t_row + c, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int tok = row0 + c + j;
+        if (tok < row_end && col < p.N_out) {
+          if constexpr (MODE == kScatter) {
+            red_add_f32(C + static_cast<size_t>(__ldg(p.row_token + tok)) * p.N_out + col,
+                        __ldg(p.row_w + tok) * v[j]);
+          } else {
+            C[static_cast<size_t>(tok) * p.N_out + col] = v[j] + b;
+          }
+        }
+      }
+    }
+  }
+}
+
 template <int MODE>
 struct TcPairCfg {
   static constexpr int kABytes = 128 * BK * 2;  // this CTA's 128 rows of A
@@ -824,6 +906,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fence_mbar_init();
     tma_prefetch_desc(&p.tmAct);
     tma_prefetch_desc(&p.tmWgt);
+    tma_prefetch_desc(&p.tmActS16);
+    tma_prefetch_desc(&p.tmActS32);
+    tma_prefetch_desc(&p.tmActS64);
+    if constexpr (MODE == kSwiGLU) tma_prefetch_desc(&p.tmWgtS);
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(tmem_slot), Cfg::kTmemCols);
@@ -876,15 +962,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int a_row = row0 + static_cast<int>(rank) * 128;
         const int b_row = MODE == kSwiGLU ? (rank == 0 ? n0 : p.up_offset + n0)
                                           : n0 + static_cast<int>(rank) * 128;
+        // swapped tail: sA takes this CTA's 128 weight rows, sB its N/2 token rows
+        const int tn = pair_tail_n(row0, row_end);
+        const int t_row = row0 + static_cast<int>(rank) * (tn / 2);
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
             ok = false;
             break;
           }
           const uint32_t fb_leader = mapa_shared(full_bar(stage), 0);
+          const uint32_t a_dst = smem_u32(sA + stage * Cfg::kABytes);
+          const uint32_t b_dst = smem_u32(sB + stage * Cfg::kBBytes);
+          if (tn > 0) {
+            if (rank == 0)
+              mbar_arrive_expect_tx(full_bar(stage), 2u * (Cfg::kABytes + tn * 64));
+            if constexpr (MODE == kSwiGLU)  // gate rows w0.. then the matching up rows
+              tma_load_4d_pair(a_dst, &p.tmWgtS, fb_leader, kb * BK,
+                               n0 + static_cast<int>(rank) * 64, 0, g);
+            else
+              tma_load_3d_pair(a_dst, &p.tmWgt, fb_leader, kb * BK, b_row, g);
+            // this CTA's tn/2 token rows in boxes of 64, 32 and 16 rows
+            int rr = 0;
+            for (; rr + 64 <= tn / 2; rr += 64)
+              tma_load_2d_pair(b_dst + 128u * rr, &p.tmActS64, fb_leader, kb * BK, t_row + rr);
+            if (rr + 32 <= tn / 2) {
+              tma_load_2d_pair(b_dst + 128u * rr, &p.tmActS32, fb_leader, kb * BK, t_row + rr);
+              rr += 32;
+            }
+            if (rr < tn / 2)
+              tma_load_2d_pair(b_dst + 128u * rr, &p.tmActS16, fb_leader, kb * BK, t_row + rr);
+            ++issued;
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * Cfg::kStageBytes);
-          tma_load_2d_pair(smem_u32(sA + stage * Cfg::kABytes), &p.tmAct, fb_leader, kb * BK, a_row);
-          tma_load_3d_pair(smem_u32(sB + stage * Cfg::kBBytes), &p.tmWgt, fb_leader, kb * BK, b_row, g);
+          tma_load_2d_pair(a_dst, &p.tmAct, fb_leader, kb * BK, a_row);
+          tma_load_3d_pair(b_dst, &p.tmWgt, fb_leader, kb * BK, b_row, g);
           ++issued;
           if (++stage == S) {
             stage = 0;
@@ -919,6 +1035,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int idx = pair; idx < total && ok; idx += npairs, ++local) {
         const int acc = local & 1;
         const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
+        int g, row0, row_end, n_tile;
+        decode_tile(p, s_off, s_mt, num_mt, kTileRows, idx, g, row0, row_end, n_tile);
+        const int tn = pair_tail_n(row0, row_end);
+        const uint32_t idesc_t = tn > 0 ? idesc_bf16_f32(256, tn) : idesc;
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.err)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -933,7 +1053,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             tc_mma_bf16_pair(d_tmem, smem_desc_sw128(a_base + kk * 32),
-                             smem_desc_sw128(b_base + kk * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
+                             smem_desc_sw128(b_base + kk * 32), idesc_t, (kb | kk) != 0 ? 1u : 0u);
           tc_commit_pair(empty_bar(stage), 0x3);
           if (++stage == S) {
             stage = 0;
@@ -960,12 +1080,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       decode_tile(p, s_off, s_mt, num_mt, kTileRows, idx, g, row0, row_end, n_tile);
       const int acc = local & 1;
       const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
-      if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.err)) break;
+      const bool ready = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.err);
+      // swapped tails meet at named barriers: the four epilogue warps leave together
+      if (epi_bar_any(!ready || *abort_flag != 0)) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                              static_cast<uint32_t>(acc * BN);
-      const int tile_row0 = row0 + static_cast<int>(rank) * 128 + quad * 32;
-      epilogue_rows<BN, MODE>(p, t_row, stg, lane, tile_row0, row_end, n_tile * Cfg::kColsOut);
+      const int tn = pair_tail_n(row0, row_end);
+      if (tn > 0) {
+        epilogue_pair_tail<MODE>(p, t_row, sStg, quad, lane, static_cast<int>(rank), tn, row0,
+                                 row_end, n_tile * Cfg::kColsOut);
+      } else {
+        const int tile_row0 = row0 + static_cast<int>(rank) * 128 + quad * 32;
+        epilogue_rows<BN, MODE>(p, t_row, stg, lane, tile_row0, row_end, n_tile * Cfg::kColsOut);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
@@ -1016,6 +1144,21 @@ bool make_map_3d(CUtensorMap* m, const void* base, uint64_t G, uint64_t rows, ui
   cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 4D bf16 map of [G][2][half][cols] (two stacked blocks of `half` rows per group), box =
+// 1 x 2 x 64 rows x 64 columns: rows r..r+63 of both blocks in one load.
+bool make_map_4d_halves(CUtensorMap* m, const void* base, uint64_t G, uint64_t half,
+                        uint64_t cols) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[4] = {cols, half, 2, G};
+  cuuint64_t strides[3] = {cols * 2, half * cols * 2, 2 * half * cols * 2};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(BK), 64, 2, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -1095,6 +1238,20 @@ cudaError_t launch_pair(const GroupedGemm& g, unsigned* err, int num_sms, cudaSt
   if (!make_map_3d(&p.tmWgt, g.B, static_cast<uint64_t>(g.G), static_cast<uint64_t>(g.Nb),
                    static_cast<uint64_t>(g.Kd), 128))
     return cudaErrorInvalidValue;
+  if (!make_map_2d(&p.tmActS16, g.A, static_cast<uint64_t>(g.rows_alloc),
+                   static_cast<uint64_t>(g.Kd), 16) ||
+      !make_map_2d(&p.tmActS32, g.A, static_cast<uint64_t>(g.rows_alloc),
+                   static_cast<uint64_t>(g.Kd), 32) ||
+      !make_map_2d(&p.tmActS64, g.A, static_cast<uint64_t>(g.rows_alloc),
+                   static_cast<uint64_t>(g.Kd), 64))
+    return cudaErrorInvalidValue;
+  if (MODE == kSwiGLU) {
+    // [G][2][I][Kd]: the gate block then the up block of each expert
+    if (g.up_offset * 2 != g.Nb || g.up_offset % 64 != 0 ||
+        !make_map_4d_halves(&p.tmWgtS, g.B, static_cast<uint64_t>(g.G),
+                            static_cast<uint64_t>(g.up_offset), static_cast<uint64_t>(g.Kd)))
+      return cudaErrorInvalidValue;
+  }
   p.C = g.C;
   p.col_bias = g.col_bias;
   p.offsets = g.offsets;

@@ -267,6 +267,50 @@ def test_grouped_ffn_stages(moe, T, H_, E, K, I, dtype, skew):
                          what="grouped_ffn")
 
 
+# Groups of >= 768 rows on average run on CTA pairs (256-row tiles).  A group's last tile
+# with r < 256 rows runs in swapped order when r rounds up to at most 192 token columns,
+# else padded; these sizes give tails of 1, 33, 31, 192, 255 (padded), 0, 96 and 160 rows
+# and one empty group.
+PAIR_GROUPS = [769, 801, 1055, 1216, 0, 1279, 1024, 864, 928]
+
+
+@pytest.mark.parametrize("H_,I", [(256, 128), (512, 320)])
+def test_pair_tiles_with_swapped_tails(moe, H_, I):
+    sizes = np.array(PAIR_GROUPS)
+    E, K = len(sizes), 2
+    M = int(sizes.sum())
+    T = (M + 255) // K  # a few spare rows after the last group
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    shape = synth.MoEShape("pair", T=T, H=H_, E=E, K=K, I=I, seed=12)
+    inp = synth.make_inputs(shape, device="cuda")
+    gen = torch.Generator().manual_seed(13)
+    x_perm = torch.full((T * K, H_), float("nan"), dtype=torch.bfloat16, device="cuda")
+    x_perm[:M] = torch.randn(M, H_, generator=gen).to(torch.bfloat16).cuda()
+    c = _cfg(moe, T, H_, E, K, I=I, dtype="bf16")
+    off = torch.from_numpy(offsets).cuda()
+    ws = torch.empty(moe.workspace_size(c), dtype=torch.uint8, device="cuda")
+    h = torch.full((T * K, I), -5.0, dtype=torch.bfloat16, device="cuda")
+    moe.expert_gate_up(c, x_perm, off, inp["w_gate_up"], h, ws)
+    out = torch.full((T * K, H_), -5.0, dtype=torch.float32, device="cuda")
+    moe.expert_down(c, h, off, inp["w_down"], out, ws)
+    torch.cuda.synchronize()
+    moe.sync_check()
+    assert (h[M:] == -5.0).all() and (out[M:] == -5.0).all()
+    xp = H.f64(x_perm[:M])
+    h_gpu = H.f64(h[:M])
+    h_ref = np.zeros((M, I))
+    o_of_hgpu = np.zeros((M, H_))
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 > r0:
+            h_ref[r0:r1] = oracle.expert_gate_up(xp[r0:r1], H.f64(inp["w_gate_up"][e]))
+            o_of_hgpu[r0:r1] = oracle.expert_down(h_gpu[r0:r1], H.f64(inp["w_down"][e]))
+    assert np.isfinite(h_gpu).all()
+    assert (np.abs(h_gpu - h_ref) <= 2.0 ** -8 * np.abs(h_ref) + 1e-4).all()
+    H.assert_close_y(out[:M].double().cpu().numpy(), o_of_hgpu, max_abs=1e-3, rel_l2=1e-5,
+                     what="down")
+
+
 @pytest.mark.parametrize("T,H_,E,K,I,dtype,skew", [c for c in FFN_CASES if c[5] == "bf16"])
 def test_gate_up_row_gather_equals_permuted_copy(moe, T, H_, E, K, I, dtype, skew):
     """The gate/up GEMM that gathers its rows from x by perm computes, row for row, the
