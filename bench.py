@@ -142,16 +142,16 @@ class ClockSampler:
 
 def gate_up_kernel(shape, T):
     """The gate/up kernel the layer launches (mirrors the library's choice): CTA pairs with
-    256-row tiles for large groups (>= 768 rows per expert on average), else single CTAs
-    that gather token rows from x by TMA; decode-sized batches (T <= 128) put the weights
-    on the MMA's 128-row side."""
+    256-row tiles for groups of >= 384 rows per expert on average (the gate/up GEMM's
+    threshold), else single CTAs with 128-row tiles; decode-sized batches (T <= 128) put
+    the weights on the MMA's 128-row side."""
     if shape.dtype != "bf16":
         return "grouped_gemm_simt_kernel<SwiGLU> (moe_expert_gate_up)"
     if T <= 128:
         bt = 16 if T <= 16 else 32 if T <= 32 else 64
         return f"tc_grouped_gemm_kernel<{bt},SwiGLU,swap> (moe_expert_gate_up)"
     rows = T * shape.K // shape.E
-    if rows >= 768 or (rows >= 256 and (shape.H >= 4096 or shape.I >= 4096)):
+    if rows >= 384 or (rows >= 256 and (shape.H >= 4096 or shape.I >= 4096)):
         return "tc_pair_gemm_kernel<SwiGLU> (moe_expert_gate_up)"
     return "tc_grouped_gemm_kernel<256,SwiGLU> (moe_expert_gate_up)"
 
