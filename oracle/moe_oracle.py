@@ -52,6 +52,8 @@ __all__ = [
     "topk_softmax",
     "gate_drop",
     "route",
+    "capacity",
+    "route_capacity",
     "permute",
     "silu",
     "swiglu_ffn",
@@ -137,6 +139,59 @@ def route(logits32, K, theta=0.0):
     """Routing = top-k softmax followed by the gate drop (P1 §2.2, steps 2 and 3)."""
     ids, w = topk_softmax(logits32, K)
     return gate_drop(ids, w, theta)
+
+
+def capacity(T, K, E, factor_tenths=12):
+    """Per-expert capacity of a batch: ceil(T * K / E * 1.2).
+
+    P1 §3.2, trap 2: capacity = (batch_size * seq_len * k) / num_experts * 1.2, the
+    batch's assignments spread evenly with a 1.2 safety factor.  Reading: T = batch_size
+    * seq_len tokens, rounded up to a whole number of rows, computed exactly in integers.
+    """
+    return (factor_tenths * T * K + 10 * E - 1) // (10 * E)
+
+
+def route_capacity(logits32, K, theta=0.0, cap=None):
+    """Routing with a per-expert capacity (P1 §3.2, trap 2).
+
+    The page inserts a capacity check into routing: once an expert has been chosen
+    `cap` times, its logit is set to -inf and the token chooses again.  Reading: tokens
+    are routed one after another in token order.  For token t, an expert is available
+    when fewer than `cap` of the assignments kept so far (tokens before t, after their
+    gate drop) went to it.  The token then takes the top-k of the available experts only
+    (logit descending, ties to the lower id), with a softmax over those and the gate drop
+    of `gate_drop`.  Its kept assignments then count against the experts' capacity.  If
+    fewer than K experts are available, the missing slots hold id -1 and gate 0.
+
+    Returns ids [T, K] int32 and w [T, K] float64, as `route`.
+    """
+    L = np.asarray(logits32, dtype=np.float32).astype(np.float64)
+    T, E = L.shape
+    if not 1 <= K <= E:
+        raise ValueError("need 1 <= K <= E")
+    if cap is None:
+        cap = capacity(T, K, E)
+    count = np.zeros(E, dtype=np.int64)
+    ids = np.full((T, K), -1, dtype=np.int32)
+    w = np.zeros((T, K), dtype=np.float64)
+    experts = np.arange(E)
+    for t in range(T):
+        avail = experts[count < cap]
+        if len(avail) == 0:
+            continue
+        order = avail[np.lexsort((avail, -L[t, avail]))]
+        top = order[:K]
+        z = np.exp(L[t, top] - L[t, top[0]])
+        row_ids = np.full(K, -1, dtype=np.int32)
+        row_w = np.zeros(K)
+        row_ids[:len(top)] = top
+        row_w[:len(top)] = z / z.sum()
+        row_ids, row_w = gate_drop(row_ids[None, :], row_w[None, :], theta)
+        ids[t], w[t] = row_ids[0], row_w[0]
+        for e in ids[t]:
+            if e >= 0:
+                count[e] += 1
+    return ids, w
 
 
 def permute(ids, E):
