@@ -64,6 +64,8 @@ def parse():
                     help="fuse the combine into the down GEMM (MOE_FLAG_FUSED_COMBINE; "
                          "default for K >= 8)")
     ap.add_argument("--gather-combine", dest="fused", action="store_false")
+    ap.add_argument("--capacity", action="store_true",
+                    help="capacity-limited routing (MOE_FLAG_CAPACITY: ceil(1.2 T K / E) per expert)")
     ap.add_argument("--time-row-gather", action="store_true",
                     help="also time the row-gather gate/up variant as a stage")
     return ap.parse_args()
@@ -178,7 +180,7 @@ def recorded_traffic(workload, kernel):
     return None
 
 
-def kernel_launches_per_step(shape, T):
+def kernel_launches_per_step(shape, T, capacity=False):
     """Kernels this library launches for one moe_layer_forward (the count is exact: it
     mirrors the launch sequence of the C ABI for this config)."""
     if T == 0:
@@ -189,7 +191,9 @@ def kernel_launches_per_step(shape, T):
     tc_router = shape.dtype == "bf16" and T >= 256 and E >= 32 and E % 16 == 0
     wsmem_router = E <= 16 and E * H * b <= 96 * 1024 and T >= 64
     fused_small = T <= 64 and (E * 8 * 4 + (2 * E + 1) * 4 + T * K * 12 + T * E * 4) <= 200 * 1024
-    cluster = shape.dtype == "bf16" and T <= 64 and E <= 256 and K <= 16
+    cluster = shape.dtype == "bf16" and T <= 64 and E <= 256 and K <= 16 and not capacity
+    if capacity:
+        fused_small = False           # the top-k is not deferred into the permutation
     if cluster:
         n += 2                            # routing + permutation in one cluster launch; gate/up
         n += 1                            # down
@@ -202,6 +206,8 @@ def kernel_launches_per_step(shape, T):
         n += 1                            # router with the top-k fused
     else:
         n += 1 if fused_small else 2      # partial logits (+ top-k unless fused below)
+    if capacity:
+        n += 1                            # the capacity sweep over the router's choices
     n += 1 if T <= 256 else 3             # one-launch permutation, or rank + scan + scatter
     n += 2                                # grouped gate/up, grouped down
     if shape.I_shared:
@@ -237,7 +243,7 @@ def run_ours(args, rank, world, local):
     # default: the fp32 scatter-add combine fused into the down GEMM when each token has
     # many (K >= 8) contributions to add, the deterministic gather combine otherwise
     fused = bool(args.fused) if args.fused is not None else (shape.K >= 8 and shape.dtype == "bf16")
-    flags = moe.FLAG_FUSED_COMBINE if fused else 0
+    flags = (moe.FLAG_FUSED_COMBINE if fused else 0) | (moe.FLAG_CAPACITY if args.capacity else 0)
     cfg = moe.MoEConfig.make(T, shape.H, shape.E, shape.K, shape.I, shape.I_shared, shape.theta, dt,
                              flags)
     ws = torch.empty(moe.workspace_size(cfg), dtype=torch.uint8, device=dev)
@@ -415,7 +421,9 @@ def run_ours(args, rank, world, local):
         "data": "synthetic (seeded; x~N(0,1), W_r~N(0,1/H), expert W~N(0,0.02))",
         "config": {"workload": args.config, "T": T, "H": shape.H, "E": shape.E, "K": shape.K,
                    "I": shape.I, "I_shared": shape.I_shared, "theta": shape.theta,
-                   "router_bias": shape.bias, "l2": "flushed between steps: 512 MiB write, then 512 MiB read of another buffer",
+                   "router_bias": shape.bias,
+                   "routing": "capacity ceil(1.2 T K / E) per expert" if args.capacity else "top-k",
+                   "l2": "flushed between steps: 512 MiB write, then 512 MiB read of another buffer",
                    "parallelism": "replicas" if world > 1 else "single-gpu",
                    "cuda_graph": bool(use_graph),
                    "combine": "fused scatter-add (fp32, order not fixed)" if fused else "gather (deterministic)",
@@ -429,7 +437,7 @@ def run_ours(args, rank, world, local):
                 "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
                 "d2h_bytes_per_step": y_host.numel() * y_host.element_size()},
-        "gpu_launches": kernel_launches_per_step(shape, T) * args.steps,
+        "gpu_launches": kernel_launches_per_step(shape, T, args.capacity) * args.steps,
         "clocks": clk.summary(),
         "wall_s_timed_region": round(t_wall, 3),
     }

@@ -70,7 +70,16 @@ enum {
    * order, so y and y_f32 are correct to fp32 rounding but not bitwise reproducible from
    * run to run.  Without this flag (default) the combine gathers in slot order and every
    * output is deterministic.  Float32 layers ignore the flag. */
-  MOE_FLAG_FUSED_COMBINE = 1u
+  MOE_FLAG_FUSED_COMBINE = 1u,
+  /* moe_route and moe_layer_forward: capacity-limited routing ("MoE大模型的智能调度…" §3.2,
+   * trap 2).  Each expert takes at most cap = ceil(1.2 * T * K / E) kept assignments.
+   * Tokens are routed in token order: an expert that earlier tokens have filled is
+   * unavailable (its logit counts as -inf), and the token takes its top-k of the available
+   * experts, with the softmax over them and the gate drop as usual; dropped assignments do
+   * not use capacity.  If fewer than K experts are available the missing slots hold -1 / 0
+   * (a suffix, like dropped slots).  E <= 1024.  The result is deterministic and equals
+   * the token-by-token rule; it runs as one extra single-CTA launch after the router. */
+  MOE_FLAG_CAPACITY = 2u
 };
 
 typedef struct {
@@ -107,7 +116,8 @@ moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes);
  *               expert id; a dropped slot holds -1 (dropped slots form a suffix).
  *   topk_w      [T,K] float out: softmax over the K kept logits, after the drop the
  *               survivors renormalised to sum 1; dropped slots hold 0.
- * The selection is taken on float32 logits. */
+ * The selection is taken on float32 logits.  With MOE_FLAG_CAPACITY the choices are
+ * capacity-limited (see the flag). */
 moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* w_router,
                        const float* router_bias, float* logits, int32_t* topk_ids,
                        float* topk_w, moe_stream_t stream);

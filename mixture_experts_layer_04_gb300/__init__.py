@@ -16,7 +16,7 @@ import os
 from typing import Optional
 
 __all__ = [
-    "MoEConfig", "MoEError", "F32", "BF16", "FLAG_FUSED_COMBINE", "library_path", "load", "workspace_size",
+    "MoEConfig", "MoEError", "F32", "BF16", "FLAG_FUSED_COMBINE", "FLAG_CAPACITY", "library_path", "load", "workspace_size",
     "route", "permute", "permute_noalloc", "grouped_ffn", "expert_gate_up", "expert_down", "combine", "layer_forward", "workspace_views",
     "sync_check", "debug_wait_timeout", "status_string", "version",
 ]
@@ -26,6 +26,7 @@ BF16 = 1
 # moe_config_t.flags: fuse the combine into the down projection (bf16 layers; y is then
 # correct to fp32 rounding but not bitwise reproducible run to run)
 FLAG_FUSED_COMBINE = 1
+FLAG_CAPACITY = 2
 
 _STATUS = {
     0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",

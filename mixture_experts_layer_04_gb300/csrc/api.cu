@@ -53,7 +53,8 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 moe_status_t check_config(const moe_config_t* c) {
   if (c == nullptr) return MOE_ERR_INVALID_ARG;
-  if ((c->flags & ~static_cast<uint32_t>(MOE_FLAG_FUSED_COMBINE)) != 0u) return MOE_ERR_INVALID_ARG;
+  if ((c->flags & ~static_cast<uint32_t>(MOE_FLAG_FUSED_COMBINE | MOE_FLAG_CAPACITY)) != 0u)
+    return MOE_ERR_INVALID_ARG;
   if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if (c->T < 0 || c->H <= 0 || c->E <= 0 || c->K <= 0 || c->I <= 0 || c->I_shared < 0)
     return MOE_ERR_INVALID_ARG;
@@ -429,8 +430,13 @@ moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* w_rou
   if (cfg->T == 0) return MOE_OK;
   const DeviceInfo* d = nullptr;
   MOE_TRY(check_device(&d));
-  return run_route(cfg, d, x, w_router, router_bias, logits, topk_ids, topk_w, nullptr, false,
-                   nullptr, static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MOE_TRY(run_route(cfg, d, x, w_router, router_bias, logits, topk_ids, topk_w, nullptr, false,
+                    nullptr, s));
+  if ((cfg->flags & MOE_FLAG_CAPACITY) == 0u) return MOE_OK;
+  return cuda_status(launch_capacity_route(logits, topk_ids, topk_w, cfg->T, cfg->E, cfg->K,
+                                           cfg->gate_threshold,
+                                           capacity_limit(cfg->T, cfg->K, cfg->E), d->err, s));
 }
 
 moe_status_t moe_permute(const moe_config_t* cfg, const void* x, const int32_t* topk_ids,
@@ -606,7 +612,11 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
   // Decode-sized bf16 batches route and dispatch in one cluster launch, and the gate/up
   // GEMM then gathers each group's token rows from x itself (few rows per group, so the
   // gather is cheap next to the weight stream): no permuted copy of x is made.
-  const bool cluster = route_cluster_ok(cfg->dtype, cfg->T, cfg->H, cfg->E, cfg->K);
+  // capacity-limited routing rewrites the router's choices before the dispatch, so the
+  // one-launch routing + dispatch of small batches does not apply
+  const bool capacity = (cfg->flags & MOE_FLAG_CAPACITY) != 0u;
+  const bool cluster =
+      !capacity && route_cluster_ok(cfg->dtype, cfg->T, cfg->H, cfg->E, cfg->K);
   const bool gather = cluster && cfg->T <= kGatherMaxTokens;
   if (cluster) {
     MOE_CUDA(launch_route_cluster(x, w_router, router_bias, logits, ids, w, cfg->gate_threshold,
@@ -615,8 +625,11 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
   } else {
     int deferred = 0;
     float* partial = at<float>(ws, p.partial);
-    MOE_TRY(run_route(cfg, d, x, w_router, router_bias, logits, ids, w, partial, true, &deferred,
-                      s));
+    MOE_TRY(run_route(cfg, d, x, w_router, router_bias, logits, ids, w, partial, !capacity,
+                      &deferred, s));
+    if (capacity)
+      MOE_CUDA(launch_capacity_route(logits, ids, w, cfg->T, cfg->E, cfg->K, cfg->gate_threshold,
+                                     capacity_limit(cfg->T, cfg->K, cfg->E), d->err, s));
     if (deferred > 0) {
       MOE_CUDA(launch_topk_permute_small(partial, deferred, router_bias, logits, ids, w,
                                          cfg->gate_threshold, cfg->dtype, x, cfg->T, cfg->H,

@@ -62,6 +62,12 @@ cudaError_t launch_route_cluster(const void* x, const void* w_router, const floa
                                  int E, int K, int32_t* counts, int32_t* offsets, int32_t* perm,
                                  int32_t* inv, float* row_w, void* x_perm, unsigned* err,
                                  cudaStream_t s);
+// Capacity-limited routing (capacity.cu): ceil(1.2 T K / E) kept assignments per expert, and
+// the in-place rewrite of the router's choices ids/w [T,K] (from logits [T,E]) into the
+// token-by-token capacity routing.  E <= 1024, K <= 16; one CTA.
+int capacity_limit(int T, int K, int E);
+cudaError_t launch_capacity_route(const float* logits, int32_t* ids, float* w, int T, int E, int K,
+                                  float theta, int cap, unsigned* err, cudaStream_t s);
 // 2D TMA map of a row-major bf16 [rows, cols] matrix, box = 64 columns x box_rows rows,
 // 128-byte swizzle (gemm_tc.cu).
 bool make_tma_2d_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,

@@ -5,6 +5,7 @@ reference legs may import this package.  It shares no code with the CUDA library
 """
 
 from .moe_oracle import (  # noqa: F401
+    capacity,
     combine,
     expert_down,
     expert_gate_up,
@@ -14,6 +15,7 @@ from .moe_oracle import (  # noqa: F401
     moe_layer_tokens,
     permute,
     route,
+    route_capacity,
     router_logits,
     silu,
     swiglu_ffn,

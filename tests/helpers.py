@@ -150,3 +150,25 @@ class ExpertSlices:
 
     def __getitem__(self, e):
         return f64(self.w[int(e)])
+
+
+def capacity_gate_margin(L, K, theta, ids):
+    """Smallest |pre-drop gate - theta| over slots >= 1 in the token-by-token capacity
+    routing whose result is `ids`: the replay recovers each token's available top-k."""
+    if theta <= 0:
+        return np.inf
+    L = L.astype(np.float64)
+    T, E = L.shape
+    cap = oracle.capacity(T, K, E)
+    count = np.zeros(E, dtype=np.int64)
+    m = np.inf
+    for t in range(T):
+        avail = np.nonzero(count < cap)[0]
+        top = avail[np.lexsort((avail, -L[t, avail]))][:K]
+        if len(top) > 1:
+            z = np.exp(L[t, top] - L[t, top[0]])
+            m = min(m, float(np.abs(z[1:] / z.sum() - theta).min()))
+        for e in ids[t]:
+            if e >= 0:
+                count[e] += 1
+    return m

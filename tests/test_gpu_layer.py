@@ -221,6 +221,48 @@ def test_deterministic_decode(moe, T):
             assert (a.y32 - b.y32).abs().max().item() <= 1e-5 * max(1.0, a.y32.abs().max().item())
 
 
+@pytest.mark.parametrize("shape", [
+    synth.MoEShape("cap_qwen_small", T=1024, H=256, E=128, K=8, I=128, bias="normal", seed=21),
+    # no gate drop here: with it, one near-threshold gate decided differently from the
+    # layer's own logits would reroute later tokens (the route-level capacity tests cover
+    # the drop, on given logits with every gate clear of the threshold)
+    synth.MoEShape("cap_shared_zipf", T=600, H=512, E=64, K=8, I=256, I_shared=256,
+                   bias="zipf", seed=22),
+    synth.MoEShape("cap_decode", T=8, H=512, E=32, K=4, I=128, bias="zipf", seed=23),
+], ids=lambda s: s.name)
+def test_layer_with_capacity_routing(moe, shape):
+    """MOE_FLAG_CAPACITY through the whole layer.  The oracle routes from the layer's own
+    fp32 logits (checked against the oracle's separately), so both take the same integer
+    decisions; the rest of the layer is compared within the usual tolerance."""
+    inp = synth.make_inputs(shape, device="cuda")
+    run = H.LayerRun(moe, shape, inp, flags=moe.FLAG_CAPACITY)
+    run.run()
+    torch.cuda.synchronize()
+    moe.sync_check()
+    r = run.routing()
+    bias = _bias_np(inp)
+    x64 = H.f64(inp["x"])
+    L_ref = oracle.router_logits(x64, H.f64(inp["w_router"]), bias)
+    assert np.abs(r["logits"] - L_ref).max() <= 1e-4 * max(1, np.abs(L_ref).max())
+    L32 = r["logits"].astype(np.float32)
+    ids_ref, w_ref = oracle.route_capacity(L32, shape.K, shape.theta)
+    assert H.capacity_gate_margin(L32, shape.K, shape.theta, ids_ref) > 1e-5
+    np.testing.assert_array_equal(r["ids"], ids_ref)
+    np.testing.assert_allclose(r["w"], w_ref, rtol=0, atol=1e-5)
+    counts_ref, offsets_ref, perm_ref, inv_ref = oracle.permute(ids_ref, shape.E)
+    assert counts_ref.max() <= oracle.capacity(shape.T, shape.K, shape.E)
+    np.testing.assert_array_equal(r["offsets"], offsets_ref)
+    out_ref = oracle.grouped_ffn(x64[perm_ref], offsets_ref, H.ExpertSlices(inp["w_gate_up"]),
+                                 H.ExpertSlices(inp["w_down"]))
+    shared_ref = None
+    if shape.I_shared:
+        shared_ref = oracle.swiglu_ffn(x64, H.f64(inp["w_shared_gate_up"]),
+                                       H.f64(inp["w_shared_down"]))
+    y_ref = oracle.combine(out_ref, inv_ref, w_ref, shared_ref)
+    H.assert_close_y(run.y32.double().cpu().numpy(), y_ref, **_tol(shape))
+    assert torch.equal(run.y, run.y32.to(shape.torch_dtype))
+
+
 @pytest.mark.parametrize("case", ["T0", "T1", "K_eq_E", "one_expert", "empty_experts"])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_edge_cases(moe, case, dtype):

@@ -72,6 +72,48 @@ def test_route_from_logits_bit_exact(moe, T, E, K, theta, ties):
     assert torch.equal(Lg.cpu(), L)              # logits are an input here: untouched
 
 
+def _skewed_logits(T, E, skew, seed):
+    L = synth.random_logits(T, E, seed=seed)
+    if skew == "normal":
+        L = L + torch.randn(E, generator=torch.Generator().manual_seed(seed)) * 1.0
+    elif skew == "zipf":
+        r = torch.randperm(E, generator=torch.Generator().manual_seed(seed)).double() + 1
+        L = L + (-1.1 * torch.log(r)).float()
+    elif skew == "one":
+        L[:, E // 2] += 50.0
+    return L
+
+
+CAPACITY_CASES = [
+    # T, E, K, theta, skew
+    (1, 8, 2, 0.0, "none"), (37, 16, 4, 0.0, "one"), (300, 8, 2, 0.1, "zipf"),
+    (1000, 64, 8, 0.0, "normal"), (5000, 128, 8, 0.0, "zipf"), (2048, 256, 8, 0.05, "zipf"),
+    (600, 1024, 16, 0.0, "normal"), (700, 4, 2, 0.0, "one"),
+]
+
+
+@pytest.mark.parametrize("T,E,K,theta,skew", CAPACITY_CASES)
+def test_capacity_route_equals_oracle(moe, T, E, K, theta, skew):
+    L = _skewed_logits(T, E, skew, seed=T + 3 * E)
+    c = moe.MoEConfig.make(T, 64, E, K, 64, 0, theta, moe.BF16, moe.FLAG_CAPACITY)
+    Lg = L.cuda()
+    ids = torch.full((T, K), -9, dtype=torch.int32, device="cuda")
+    w = torch.full((T, K), -9.0, dtype=torch.float32, device="cuda")
+    moe.route(c, None, None, None, Lg, ids, w)
+    torch.cuda.synchronize()
+    moe.sync_check()
+    ids_ref, w_ref = oracle.route_capacity(L.numpy(), K, theta)
+    # the gate drop is an fp32 decision on the GPU and fp64 in the oracle: these inputs
+    # keep every gate clear of the threshold, so both take the same decisions
+    assert H.capacity_gate_margin(L.numpy(), K, theta, ids_ref) > 1e-5
+    np.testing.assert_array_equal(ids.cpu().numpy(), ids_ref)
+    np.testing.assert_allclose(w.cpu().numpy(), w_ref, rtol=0, atol=1e-5)
+    counts = np.bincount(ids_ref[ids_ref >= 0], minlength=E)
+    assert counts.max() <= oracle.capacity(T, K, E)
+    if skew != "none":  # the capacity binds: the result differs from plain routing
+        assert not np.array_equal(ids_ref, oracle.route(L.numpy(), K, theta)[0])
+
+
 ROUTER_CASES = [
     # T, H, E, dtype, bias   (bf16 with T >= 256 and E % 16 == 0 uses the tensor cores)
     (1024, 512, 128, "bf16", "normal"),
