@@ -97,7 +97,9 @@ __global__ void __launch_bounds__(kCapThreads, 1)
   uint32_t* mask = reinterpret_cast<uint32_t*>(fb + E);     // [E][kCapWords]
   int32_t* bid = reinterpret_cast<int32_t*>(mask + E * kCapWords);  // [kCapBlock * K]
   float* bw = reinterpret_cast<float*>(bid + kCapBlock * K);        // [kCapBlock * K]
-  __shared__ int s_lo, s_changed;
+  int* chg = reinterpret_cast<int*>(bw + kCapBlock * K);           // [3 * E]: e, old, new fb
+  __shared__ int s_nchg;
+  __shared__ int s_dirty[kCapBlock];
 
   grid_dep_wait();  // the router's logits and choices
   grid_dep_trigger();
@@ -121,18 +123,15 @@ __global__ void __launch_bounds__(kCapThreads, 1)
           const int e = lane < K ? bid[tl * K + lane] : -1;
           dirty = theta > 0.f || __any_sync(0xffffffffu, e >= 0 && cnt[e] >= cap);
         } else {
-          dirty = tl > s_lo;
+          dirty = s_dirty[tl] != 0;
         }
         if (dirty)
           masked_topk(logits + static_cast<size_t>(t0 + tl) * E, E, K, theta, tl, cnt, fb, cap,
                       bid + tl * K, bw + tl * K);
       }
-      __syncthreads();  // every warp has read s_lo and written its tokens' choices
+      __syncthreads();  // every warp has read the dirty flags and written its tokens' choices
       for (int i = tid; i < E * kCapWords; i += kCapThreads) mask[i] = 0u;
-      if (tid == 0) {
-        s_changed = 0;
-        s_lo = kNone;
-      }
+      if (tid == 0) s_nchg = 0;
       __syncthreads();
       // 2. which block tokens hold each expert
       for (int i = tid; i < nb * K; i += kCapThreads) {
@@ -158,13 +157,48 @@ __global__ void __launch_bounds__(kCapThreads, 1)
           }
         }
         if (f != fb[e]) {
-          atomicOr(&s_changed, 1);
-          atomicMin(&s_lo, min(f, fb[e]));
+          const int j = atomicAdd(&s_nchg, 1);
+          chg[3 * j] = e;
+          chg[3 * j + 1] = fb[e];
+          chg[3 * j + 2] = f;
           fb[e] = f;
         }
       }
       __syncthreads();
-      if (!s_changed) break;
+      const int nchg = s_nchg;
+      if (nchg == 0) break;
+      // 4. which tokens must choose again: e's last free place moved from a to b.  Earlier
+      //    (b < a): tokens in (b, a] lose e, which matters to those holding it.  Later
+      //    (b > a): tokens in (a, b] gain e, which matters if its logit ties or beats the
+      //    token's weakest choice or the token has an empty slot (a dropped slot hides a
+      //    choice, so it counts as empty).
+      for (int tl = tid; tl < nb; tl += kCapThreads) {
+        const float* Lt = logits + static_cast<size_t>(t0 + tl) * E;
+        float weakest = 0.f;
+        bool has_empty = false;
+        for (int k = 0; k < K; ++k) {
+          const int e = bid[tl * K + k];
+          if (e < 0) {
+            has_empty = true;
+          } else {
+            const float v = Lt[e];
+            weakest = k == 0 ? v : fminf(weakest, v);
+          }
+        }
+        int d = 0;
+        for (int j = 0; j < nchg && !d; ++j) {
+          const int e = chg[3 * j], a = chg[3 * j + 1], b = chg[3 * j + 2];
+          if (b < a) {
+            if (tl > b && tl <= a) {
+              for (int k = 0; k < K; ++k) d |= bid[tl * K + k] == e;
+            }
+          } else if (tl > a && tl <= b) {
+            d = has_empty || Lt[e] >= weakest;
+          }
+        }
+        s_dirty[tl] = d;
+      }
+      __syncthreads();
       if (pass > nb + 1) {  // cannot happen: each pass fixes at least one more token
         if (tid == 0) report_error(err, MOE_DEVERR_BOUNDS);
         break;
@@ -195,7 +229,7 @@ cudaError_t launch_capacity_route(const float* logits, int32_t* ids, float* w, i
                                   float theta, int cap, unsigned* err, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   if (E < 1 || E > 1024 || K < 1 || K > 16) return cudaErrorInvalidValue;
-  const size_t smem = static_cast<size_t>(E) * (2 * 4 + kCapWords * 4) +
+  const size_t smem = static_cast<size_t>(E) * (2 * 4 + kCapWords * 4 + 3 * 4) +
                       static_cast<size_t>(kCapBlock) * K * 8;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -203,7 +237,7 @@ cudaError_t launch_capacity_route(const float* logits, int32_t* ids, float* w, i
   static int attr_dev = -1;
   if (attr_dev != dev) {
     e = cudaFuncSetAttribute(capacity_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kCapBlock * 16 * 8 + 1024 * (8 + kCapWords * 4)));
+                             static_cast<int>(kCapBlock * 16 * 8 + 1024 * (8 + kCapWords * 4 + 12)));
     if (e != cudaSuccess) return e;
     attr_dev = dev;
   }
