@@ -36,26 +36,36 @@ __device__ __forceinline__ int nth_set_bit(uint32_t v, int n) {
   return __ffs(v) - 1;
 }
 
-// One warp: token `tl` of the block (logits row L) takes its top-k among the available experts
-// (count < cap and fb >= tl), with the softmax and gate drop of the warp top-k (same sums in
-// the same order), and writes its K slots to ids/w (missing slots -1 / 0).
-__device__ void masked_topk(const float* __restrict__ L, int E, int K, float theta, int tl,
-                            const int* cnt, const int* fb, int cap, int32_t* ids, float* w) {
+// Inverse of float_key (the key of -0 gives +0, which the softmax cannot tell apart).
+__device__ __forceinline__ float key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+template <int NJ>  // candidates per lane: experts lane + 32 j, j < NJ (E <= 32 NJ)
+__device__ __forceinline__ void masked_topk_t(const float* __restrict__ L, int E, int K,
+                                              float theta, int tl, const int* cnt, const int* fb, int cap,
+                                              int32_t* ids, float* w) {
   const int lane = threadIdx.x & 31;
+  uint32_t key[NJ];
   uint32_t live = 0u;  // bit j: expert lane + 32 j is available
-  for (int j = 0, e = lane; e < E; ++j, e += 32)
-    if (cnt[e] < cap && fb[e] >= tl) live |= 1u << j;
-  uint32_t taken = 0u;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    const int e = lane + 32 * j;
+    key[j] = 0u;
+    if (e < E && cnt[e] < cap && fb[e] >= tl) {
+      key[j] = float_key(L[e]);
+      live |= 1u << j;
+    }
+  }
   float my_v = 0.f, v0 = 0.f;
   int my_e = -1, nsel = 0;
   for (int k = 0; k < K; ++k) {
     uint32_t kbest = 0u, ebest = 0xffffffffu;
-    for (int j = 0, e = lane; e < E; ++j, e += 32) {
-      if (!((live >> j) & 1u) || ((taken >> j) & 1u)) continue;
-      const uint32_t kk = float_key(L[e]);
-      if (kk > kbest || ebest == 0xffffffffu) {
-        kbest = kk;
-        ebest = static_cast<uint32_t>(e);
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      if (((live >> j) & 1u) && (key[j] > kbest || ebest == 0xffffffffu)) {
+        kbest = key[j];
+        ebest = static_cast<uint32_t>(lane + 32 * j);
       }
     }
     const bool has = ebest != 0xffffffffu;
@@ -63,8 +73,8 @@ __device__ void masked_topk(const float* __restrict__ L, int E, int K, float the
     const uint32_t kmax = __reduce_max_sync(0xffffffffu, has ? kbest : 0u);
     const int e_win = static_cast<int>(
         __reduce_min_sync(0xffffffffu, (has && kbest == kmax) ? ebest : 0xffffffffu));
-    if ((e_win & 31) == lane) taken |= 1u << (e_win >> 5);
-    const float v_win = L[e_win];
+    if ((e_win & 31) == lane) live &= ~(1u << (e_win >> 5));
+    const float v_win = key_float(kmax);
     if (k == 0) v0 = v_win;
     if (lane == k) {
       my_v = v_win;
@@ -85,6 +95,21 @@ __device__ void masked_topk(const float* __restrict__ L, int E, int K, float the
     ids[lane] = lane < nsel ? my_e : -1;
     w[lane] = lane < nsel ? g : 0.f;
   }
+}
+
+// One warp: token `tl` of the block (logits row L) takes its top-k among the available experts
+// (count < cap and fb >= tl), with the softmax and gate drop of the warp top-k (same sums in
+// the same order), and writes its K slots to ids/w (dropped or missing slots -1 / 0).  The
+// candidates' keys are loaded once and kept in registers.
+__device__ __forceinline__ void masked_topk(const float* __restrict__ L, int E, int K, float theta,
+                                            int tl, const int* cnt, const int* fb, int cap,
+                                            int32_t* ids, float* w) {
+  if (E <= 128)
+    masked_topk_t<4>(L, E, K, theta, tl, cnt, fb, cap, ids, w);
+  else if (E <= 256)
+    masked_topk_t<8>(L, E, K, theta, tl, cnt, fb, cap, ids, w);
+  else
+    masked_topk_t<32>(L, E, K, theta, tl, cnt, fb, cap, ids, w);
 }
 
 __global__ void __launch_bounds__(kCapThreads, 1)
