@@ -9,11 +9,14 @@ from .moe_oracle import (  # noqa: F401
     combine,
     expert_down,
     expert_gate_up,
+    expert_gate_up_fp8,
     gate_drop,
     grouped_ffn,
     moe_layer,
     moe_layer_tokens,
     permute,
+    quantize_e4m3,
+    quantize_rows_fp8,
     route,
     route_capacity,
     router_logits,

@@ -55,6 +55,9 @@ __all__ = [
     "capacity",
     "route_capacity",
     "permute",
+    "quantize_e4m3",
+    "quantize_rows_fp8",
+    "expert_gate_up_fp8",
     "silu",
     "swiglu_ffn",
     "expert_gate_up",
@@ -252,6 +255,55 @@ def expert_gate_up(x_rows, w_gate_up):
     wgu = np.asarray(w_gate_up, dtype=np.float64)
     I = wgu.shape[0] // 2
     return silu(x @ wgu[:I].T) * (x @ wgu[I:].T)
+
+
+E4M3_MAX = 448.0
+
+
+def quantize_e4m3(v32):
+    """Round float32 values to the nearest FP8 E4M3 value (1 sign, 4 exponent bits with
+    bias 7, 3 mantissa bits, no infinities; largest finite 448, smallest subnormal 2^-9),
+    ties to even, saturating: anything beyond 448 in magnitude becomes +-448.
+
+    Low-precision experts: P1 §4.1 quantises the resident experts' weights to 8 bits
+    (INT8) to save memory.  Reading: the 8-bit format that the target's tensor cores run at
+    full rate, FP8 E4M3, with one scale per row.  Returns float64 values that are exactly
+    representable in E4M3.
+    """
+    v = np.asarray(v32, dtype=np.float32).astype(np.float64)
+    a = np.abs(v)
+    out = np.zeros_like(a)
+    nz = a > 0
+    e = np.floor(np.log2(np.where(nz, a, 1.0)))
+    e = np.maximum(e, -6.0)               # below 2^-6 the spacing stays 2^-9 (subnormals)
+    quantum = np.exp2(e - 3.0)            # 3 mantissa bits
+    q = np.round(a / quantum) * quantum   # np.round: halves to even, exact for these powers of 2
+    q = np.minimum(q, E4M3_MAX)
+    out[nz] = q[nz]
+    return np.copysign(out, v)
+
+
+def quantize_rows_fp8(a):
+    """Per-row E4M3 quantisation of a [rows, cols] matrix: scale = amax(|row|) / 448 in
+    float32 (1 for an all-zero row) and codes = E4M3(row / scale), the division in float32
+    (the precision the kernels take this decision in).  Returns (codes as float64 values,
+    scales as float32), with row ~= codes * scale."""
+    a32 = np.asarray(a, dtype=np.float32)
+    amax = np.abs(a32).max(axis=1)
+    scale = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    codes = quantize_e4m3((a32 / scale[:, None]).astype(np.float32))
+    return codes, scale
+
+
+def expert_gate_up_fp8(x_codes, x_scale, w_codes, w_scale):
+    """The gate/up half of the expert FFN on E4M3 operands: every dot product of codes is
+    exact in float64, then scaled by the token row's and the weight row's scales;
+    h = silu(g) * u as in `expert_gate_up`.  w rows 0..I-1 are the gate, I..2I-1 the up."""
+    acc = (np.asarray(x_codes, dtype=np.float64) @ np.asarray(w_codes, dtype=np.float64).T)
+    acc = acc * np.asarray(x_scale, dtype=np.float64)[:, None] * \
+        np.asarray(w_scale, dtype=np.float64)[None, :]
+    I = acc.shape[1] // 2
+    return silu(acc[:, :I]) * acc[:, I:]
 
 
 def expert_down(h_rows, w_down):
