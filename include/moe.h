@@ -206,6 +206,33 @@ moe_status_t moe_expert_gate_up_gather(const moe_config_t* cfg, const void* x,
                                        const void* w_gate_up, void* h, void* ws,
                                        size_t ws_bytes, moe_stream_t stream);
 
+/* Per-row FP8 (E4M3) quantisation, for low-precision experts.
+ * Defined by: "MoE大模型的智能调度…" §4.1 (the resident experts' weights are quantised to 8
+ * bits to save memory).  Reading: E4M3, the 8-bit format the tensor cores run at full rate,
+ * one float32 scale per row.  For every row r:
+ *   scales[r] = max_c |in[r,c]| / 448 (1 for an all-zero row), float32;
+ *   codes[r,c] = E4M3(in[r,c] / scales[r]) (float32 division, round to nearest even,
+ *   saturating at +-448), one byte each.
+ *   in [rows, cols] bf16 (device); codes [rows, cols] uint8 out; scales [rows] float out.
+ *   cols % 8 == 0; rows >= 0.  Expert weights quantise as rows = E*2I (gate/up, per output
+ *   channel); token rows as rows = T*K (the permuted x). */
+moe_status_t moe_quantize_fp8(const void* in, int64_t rows, int32_t cols, uint8_t* codes,
+                              float* scales, moe_stream_t stream);
+
+/* The gate/up projection on FP8 operands: moe_expert_gate_up with E4M3 codes and per-row
+ * scales (see moe_quantize_fp8) in place of the bf16 activations and weights.
+ * Defined by: page section "单机MoE执行流水线" (each expert's gate/up GEMM) and
+ * "MoE大模型的智能调度…" §4.1 (8-bit expert weights).  For every row r of group e:
+ *   g[r,n] = xs[r] * ws[e,n] * sum_k xq[r,k] wq[e,n,k] (fp32 accumulation of exact
+ *   products), u likewise with the up rows I+n, h[r,n] = silu(g) * u rounded once to bf16.
+ *   x_codes [T*K,H] uint8, x_scales [T*K] float; offsets [E+1] int32; w_codes [E,2I,H]
+ *   uint8, w_scales [E,2I] float; h [T*K,I] bf16 out (rows >= offsets[E] untouched);
+ *   ws as for moe_grouped_ffn.  bf16 layers only, H % 128 == 0 (else MOE_ERR_UNSUPPORTED). */
+moe_status_t moe_expert_gate_up_fp8(const moe_config_t* cfg, const uint8_t* x_codes,
+                                    const float* x_scales, const int32_t* offsets,
+                                    const uint8_t* w_codes, const float* w_scales, void* h,
+                                    void* ws, size_t ws_bytes, moe_stream_t stream);
+
 /* The second GEMM of the grouped FFN alone: the output projection.
  * Defined by: page section "单机MoE执行流水线" (each expert applies its output
  * projection).  For every row r of group e: out_perm[r] = h[r] W_d[e]^T (fp32).

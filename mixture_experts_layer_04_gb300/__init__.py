@@ -17,7 +17,7 @@ from typing import Optional
 
 __all__ = [
     "MoEConfig", "MoEError", "F32", "BF16", "FLAG_FUSED_COMBINE", "FLAG_CAPACITY", "library_path", "load", "workspace_size",
-    "route", "permute", "permute_noalloc", "grouped_ffn", "expert_gate_up", "expert_down", "combine", "layer_forward", "workspace_views",
+    "route", "permute", "permute_noalloc", "grouped_ffn", "expert_gate_up", "expert_gate_up_gather", "quantize_fp8", "expert_gate_up_fp8", "expert_down", "combine", "layer_forward", "workspace_views",
     "sync_check", "debug_wait_timeout", "status_string", "version",
 ]
 
@@ -74,6 +74,8 @@ _SIGS = {
     "moe_grouped_ffn": [_CFG, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "moe_expert_gate_up": [_CFG, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "moe_expert_gate_up_gather": [_CFG, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+    "moe_quantize_fp8": [_P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P],
+    "moe_expert_gate_up_fp8": [_CFG, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "moe_expert_down": [_CFG, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "moe_combine": [_CFG, _P, _P, _P, _P, _P, _P, _P],
     "moe_layer_forward": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
@@ -181,6 +183,22 @@ def expert_gate_up_gather(cfg, x, perm, offsets, w_gate_up, h, ws, ws_bytes=None
                                             _ptr(w_gate_up), _ptr(h), _ptr(ws), nb,
                                             _stream(stream)),
            "moe_expert_gate_up_gather")
+
+
+def quantize_fp8(x, codes, scales, stream=None):
+    """Per-row E4M3 codes and float32 scales of a bf16 [rows, cols] tensor."""
+    rows, cols = x.shape[0], x.numel() // max(1, x.shape[0])
+    _check(load().moe_quantize_fp8(_ptr(x), rows, cols, _ptr(codes), _ptr(scales), _stream(stream)),
+           "moe_quantize_fp8")
+
+
+def expert_gate_up_fp8(cfg, x_codes, x_scales, offsets, w_codes, w_scales, h, ws, ws_bytes=None,
+                       stream=None):
+    nb = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check(load().moe_expert_gate_up_fp8(ctypes.byref(cfg), _ptr(x_codes), _ptr(x_scales),
+                                         _ptr(offsets), _ptr(w_codes), _ptr(w_scales), _ptr(h),
+                                         _ptr(ws), nb, _stream(stream)),
+           "moe_expert_gate_up_fp8")
 
 
 def expert_down(cfg, h, offsets, w_down, out_perm, ws, ws_bytes=None, stream=None):

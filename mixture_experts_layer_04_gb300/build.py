@@ -24,7 +24,7 @@ LIB_NAME = "libmoe_gb300.so"
 LIB_PATH = os.path.join(BUILD, LIB_NAME)
 
 SOURCES = ["api.cu", "route.cu", "permute.cu", "combine.cu", "gemm_simt.cu", "gemm_tc.cu",
-           "permute_noalloc.cu", "route_cluster.cu", "capacity.cu"]
+           "permute_noalloc.cu", "route_cluster.cu", "capacity.cu", "quant.cu"]
 GENCODE = "-gencode=arch=compute_103a,code=sm_103a"
 NVCC_FLAGS = [
     GENCODE, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",

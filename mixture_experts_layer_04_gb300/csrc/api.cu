@@ -504,6 +504,51 @@ moe_status_t moe_expert_gate_up(const moe_config_t* cfg, const void* x_perm,
   return run_gate_up(cfg, d, x_perm, cfg->T * cfg->K, w_gate_up, cfg->I, h, gr, s);
 }
 
+moe_status_t moe_quantize_fp8(const void* in, int64_t rows, int32_t cols, uint8_t* codes,
+                              float* scales, moe_stream_t stream) {
+  if (rows < 0 || cols <= 0 || cols % 8 != 0) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (in == nullptr || codes == nullptr || scales == nullptr) return MOE_ERR_INVALID_ARG;
+  if (any_misaligned({in, codes})) return MOE_ERR_MISALIGNED;
+  const DeviceInfo* d = nullptr;
+  MOE_TRY(check_device(&d));
+  return cuda_status(launch_quantize_fp8(in, rows, cols, codes, scales,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_expert_gate_up_fp8(const moe_config_t* cfg, const uint8_t* x_codes,
+                                    const float* x_scales, const int32_t* offsets,
+                                    const uint8_t* w_codes, const float* w_scales, void* h,
+                                    void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_config(cfg));
+  if (cfg->T == 0) return MOE_OK;
+  if (cfg->dtype != MOE_BF16 || cfg->H % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (x_codes == nullptr || x_scales == nullptr || offsets == nullptr || w_codes == nullptr ||
+      w_scales == nullptr || h == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (any_misaligned({x_codes, offsets, w_codes, h})) return MOE_ERR_MISALIGNED;
+  Plan p;
+  MOE_TRY(check_ws(cfg, ws, ws_bytes, &p));
+  const DeviceInfo* d = nullptr;
+  MOE_TRY(check_device(&d));
+  GroupedGemm g{};
+  g.mode = kSwiGLU;
+  g.dtype = cfg->dtype;
+  g.A = x_codes;
+  g.rows_alloc = cfg->T * cfg->K;
+  g.Kd = cfg->H;
+  g.B = w_codes;
+  g.G = cfg->E;
+  g.Nb = 2 * cfg->I;
+  g.N_out = cfg->I;
+  g.up_offset = cfg->I;
+  g.C = h;
+  g.offsets = offsets;
+  g.swap_tokens = cfg->T <= kSwapMaxTokens ? cfg->T : 0;
+  return cuda_status(launch_gate_up_fp8(g, x_scales, w_scales, d->err, d->num_sms,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
 moe_status_t moe_expert_gate_up_gather(const moe_config_t* cfg, const void* x,
                                        const int32_t* perm, const int32_t* offsets,
                                        const void* w_gate_up, void* h, void* ws, size_t ws_bytes,

@@ -84,6 +84,11 @@ struct TcParams {
   float topk_theta;
   int32_t* topk_ids;
   float* topk_w;
+  // FP8 gate/up (E4M3 operands): per A row and per B row ([G][b_rows]) scales, applied to
+  // the accumulators before the SwiGLU; null for bf16
+  const float* a_scale;
+  const float* b_scale;
+  int b_rows;
 };
 
 template <int BN, int MODE, bool SWAP>
@@ -231,15 +236,33 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[32]) {
 // half).  `stg` is this warp's staging buffer in shared memory.
 template <int BN, int MODE>
 __device__ __forceinline__ void epilogue_rows(const TcParams& p, uint32_t t_row, uint32_t stg,
-                                              int lane, int tile_row0, int row_end, int col0) {
+                                              int lane, int tile_row0, int row_end, int col0,
+                                              int group = 0) {
   if constexpr (MODE == kSwiGLU) {
     __nv_bfloat16* C = static_cast<__nv_bfloat16*>(p.C);
+    // FP8 operands: this thread's token-row scale, and the group's weight-row scales
+    float sa = 1.f;
+    const float* sb = nullptr;
+    if (p.a_scale != nullptr) {
+      sa = tile_row0 + lane < row_end ? __ldg(p.a_scale + tile_row0 + lane) : 0.f;
+      sb = p.b_scale + static_cast<size_t>(group) * p.b_rows;
+    }
 #pragma unroll 1
     for (int c = 0; c < BN / 2; c += 32) {
       uint32_t gr[32], ur[32];
       tmem_ld_32x32b_x32(t_row + c, gr);
       tmem_ld_32x32b_x32(t_row + BN / 2 + c, ur);
       tmem_ld_wait();
+      if (sb != nullptr) {
+        const int cl = col0 + c + lane;  // one coalesced load per chunk, then broadcast
+        const float sg = cl < p.N_out ? __ldg(sb + cl) : 0.f;
+        const float su = cl < p.N_out ? __ldg(sb + p.up_offset + cl) : 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          gr[j] = __float_as_uint(__uint_as_float(gr[j]) * (sa * __shfl_sync(0xffffffffu, sg, j)));
+          ur[j] = __float_as_uint(__uint_as_float(ur[j]) * (sa * __shfl_sync(0xffffffffu, su, j)));
+        }
+      }
       uint32_t pk[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
@@ -438,11 +461,12 @@ __device__ __forceinline__ void epilogue_topk(const TcParams& p, uint32_t t_row,
     }
 }
 
-template <int BN, int MODE, bool SWAP, bool GATHER>
+template <int BN, int MODE, bool SWAP, bool GATHER, bool F8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_grouped_gemm_kernel(const __grid_constant__ TcParams p) {
   using Cfg = TcCfg<BN, MODE, SWAP>;
   constexpr int S = Cfg::kStages;
+  constexpr int kKStep = F8 ? 128 : BK;  // elements per 128-byte k-step
   constexpr int kTileRows = Cfg::kActRows;
   constexpr int kNC = BN < 32 ? BN : 32;  // TMEM columns per load in the swapped epilogue
   extern __shared__ uint8_t smem_raw[];
@@ -569,15 +593,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t w_dst = smem_u32(sWgt + stage * Cfg::kWgtBytes);
           if (leader) {
             mbar_arrive_expect_tx(fb, stage_tx);
-            if constexpr (!GATHER) tma_load_2d(a_dst, &p.tmAct, fb, kb * BK, row0);
-            tma_load_3d(w_dst, &p.tmWgt, fb, kb * BK, n0, g);
+            if constexpr (!GATHER) tma_load_2d(a_dst, &p.tmAct, fb, kb * kKStep, row0);
+            tma_load_3d(w_dst, &p.tmWgt, fb, kb * kKStep, n0, g);
             if constexpr (MODE == kSwiGLU)
-              tma_load_3d(w_dst + Cfg::kWgtBox * 128, &p.tmWgt, fb, kb * BK, p.up_offset + n0, g);
+              tma_load_3d(w_dst + Cfg::kWgtBox * 128, &p.tmWgt, fb, kb * kKStep, p.up_offset + n0, g);
           }
           if constexpr (GATHER) {
             __syncwarp();
             if (lane < gather_lanes)
-              tma_gather4(a_dst + 512u * lane, &p.tmAct, fb, kb * BK, src[0], src[1], src[2],
+              tma_gather4(a_dst + 512u * lane, &p.tmAct, fb, kb * kKStep, src[0], src[1], src[2],
                           src[3]);
           }
           ++issued;
@@ -607,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA ----
     if (elect_one_sync()) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, BN);
+      constexpr uint32_t idesc = F8 ? idesc_e4m3_f32(128, BN) : idesc_bf16_f32(128, BN);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
@@ -632,7 +656,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t ad = smem_desc_sw128(a_base + kk * 32);
             const uint64_t bd = smem_desc_sw128(b_base + kk * 32);
-            tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            if constexpr (F8)
+              tc_mma_e4m3(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            else
+              tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           tc_commit(empty_bar(stage));
           if (++stage == S) {
@@ -684,19 +711,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           else
             epilogue_topk<BN, 16>(p, t_row, stg, lane, tile_row0, row_end);
         } else
-          epilogue_rows<BN, MODE>(p, t_row, stg, lane, tile_row0, row_end, col0);
+          epilogue_rows<BN, MODE>(p, t_row, stg, lane, tile_row0, row_end, col0, g);
       } else {
         // swapped: lane = weight row of the tile, column j = token row0 + j
         if constexpr (MODE == kSwiGLU) {
           // lanes 0-63: gate rows (quads 0, 1); lanes 64-127: up rows (quads 2, 3).
           // xchg[r][j] holds up row r for token j, rotated by r to spread the banks.
           float* xchg = reinterpret_cast<float*>(sStg);
+          // FP8 operands: this lane's weight-row scale; token-row scales per column below
+          float sw = 1.f;
+          if (p.a_scale != nullptr) {
+            const int wr = quad < 2 ? col0 + quad * 32 + lane
+                                    : p.up_offset + col0 + (quad - 2) * 32 + lane;
+            sw = col0 + (quad & 1) * 32 + lane < p.N_out
+                     ? __ldg(p.b_scale + static_cast<size_t>(g) * p.b_rows + wr)
+                     : 0.f;
+          }
           if (quad >= 2) {
             const int r = (quad - 2) * 32 + lane;
 #pragma unroll 1
             for (int c = 0; c < BN; c += kNC) {
               float v[32];
               tmem_ld_cols<kNC>(t_row + c, v);
+              if (p.a_scale != nullptr) {
+                const float sx = row0 + c + lane < row_end ? __ldg(p.a_scale + row0 + c + lane) : 0.f;
+#pragma unroll
+                for (int j = 0; j < kNC; ++j) v[j] *= sw * __shfl_sync(0xffffffffu, sx, j);
+              }
 #pragma unroll
               for (int j = 0; j < kNC; ++j) xchg[r * BN + ((c + j + r) % BN)] = v[j];
             }
@@ -710,6 +751,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < BN; c += kNC) {
               float v[32];
               tmem_ld_cols<kNC>(t_row + c, v);
+              if (p.a_scale != nullptr) {
+                const float sx = row0 + c + lane < row_end ? __ldg(p.a_scale + row0 + c + lane) : 0.f;
+#pragma unroll
+                for (int j = 0; j < kNC; ++j) v[j] *= sw * __shfl_sync(0xffffffffu, sx, j);
+              }
 #pragma unroll
               for (int j = 0; j < kNC; ++j) {
                 const int tok = row0 + c + j;
@@ -1148,6 +1194,33 @@ bool make_map_3d(CUtensorMap* m, const void* base, uint64_t G, uint64_t rows, ui
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2D / 3D maps of FP8 (one byte per element) matrices: box = 128 columns (128 bytes, one
+// swizzle row, the same smem layout as 64 bf16 columns) x box_rows rows.
+bool make_map_2d_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                    uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+bool make_map_3d_u8(CUtensorMap* m, const void* base, uint64_t G, uint64_t rows, uint64_t cols,
+                    uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {cols, rows, G};
+  cuuint64_t strides[2] = {cols, rows * cols};
+  cuuint32_t box[3] = {128, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 4D bf16 map of [G][2][half][cols] (two stacked blocks of `half` rows per group), box =
 // 1 x 2 x 64 rows x 64 columns: rows r..r+63 of both blocks in one load.
 bool make_map_4d_halves(CUtensorMap* m, const void* base, uint64_t G, uint64_t half,
@@ -1163,10 +1236,11 @@ bool make_map_4d_halves(CUtensorMap* m, const void* base, uint64_t G, uint64_t h
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int MODE, bool SWAP, bool GATHER = false>
-cudaError_t launch_one(const GroupedGemm& g, unsigned* err, int num_sms, cudaStream_t s) {
+template <int BN, int MODE, bool SWAP, bool GATHER = false, bool F8 = false>
+cudaError_t launch_one(const GroupedGemm& g, unsigned* err, int num_sms, cudaStream_t s,
+                       const float* a_scale = nullptr, const float* b_scale = nullptr) {
   using Cfg = TcCfg<BN, MODE, SWAP>;
-  auto kernel = tc_grouped_gemm_kernel<BN, MODE, SWAP, GATHER>;
+  auto kernel = tc_grouped_gemm_kernel<BN, MODE, SWAP, GATHER, F8>;
   if (GATHER != (g.gather_rows != nullptr)) return cudaErrorInvalidValue;
   static int attr_set_dev = -1;  // the attribute is per function and device
   int dev = 0;
@@ -1181,7 +1255,9 @@ cudaError_t launch_one(const GroupedGemm& g, unsigned* err, int num_sms, cudaStr
   memset(&p, 0, sizeof(p));
   // with a row gather the map covers the source rows, one row per box
   const bool ok_map =
-      g.gather_rows != nullptr
+      F8 ? make_map_2d_u8(&p.tmAct, g.A, static_cast<uint64_t>(g.rows_alloc),
+                          static_cast<uint64_t>(g.Kd), Cfg::kActRows)
+      : g.gather_rows != nullptr
           ? make_map_2d(&p.tmAct, g.A, static_cast<uint64_t>(g.src_rows),
                         static_cast<uint64_t>(g.Kd), 1)
           : make_map_2d(&p.tmAct, g.A, static_cast<uint64_t>(g.rows_alloc),
@@ -1192,9 +1268,14 @@ cudaError_t launch_one(const GroupedGemm& g, unsigned* err, int num_sms, cudaStr
   p.topk_theta = g.topk_theta;
   p.topk_ids = g.topk_ids;
   p.topk_w = g.topk_w;
-  if (!make_map_3d(&p.tmWgt, g.B, static_cast<uint64_t>(g.G), static_cast<uint64_t>(g.Nb),
-                   static_cast<uint64_t>(g.Kd), Cfg::kWgtBox))
+  if (F8 ? !make_map_3d_u8(&p.tmWgt, g.B, static_cast<uint64_t>(g.G), static_cast<uint64_t>(g.Nb),
+                           static_cast<uint64_t>(g.Kd), Cfg::kWgtBox)
+         : !make_map_3d(&p.tmWgt, g.B, static_cast<uint64_t>(g.G), static_cast<uint64_t>(g.Nb),
+                        static_cast<uint64_t>(g.Kd), Cfg::kWgtBox))
     return cudaErrorInvalidValue;
+  p.a_scale = a_scale;
+  p.b_scale = b_scale;
+  p.b_rows = g.Nb;
   p.C = g.C;
   p.col_bias = g.col_bias;
   p.offsets = g.offsets;
@@ -1203,7 +1284,7 @@ cudaError_t launch_one(const GroupedGemm& g, unsigned* err, int num_sms, cudaStr
   p.num_groups = g.G;
   p.err = err;
   p.rows_alloc = g.rows_alloc;
-  p.num_kb = g.Kd / BK;
+  p.num_kb = F8 ? g.Kd / 128 : g.Kd / BK;  // 128-byte k-steps either way
   p.N_out = g.N_out;
   p.n_tiles = (g.N_out + Cfg::kColsOut - 1) / Cfg::kColsOut;
   p.up_offset = g.up_offset;
@@ -1284,6 +1365,20 @@ int tc_swap_tokens(int max_rows_per_group) {
   if (max_rows_per_group <= 16) return 16;
   if (max_rows_per_group <= 32) return 32;
   return 64;
+}
+
+cudaError_t launch_gate_up_fp8(const GroupedGemm& g, const float* a_scale, const float* b_scale,
+                               unsigned* err, int num_sms, cudaStream_t s) {
+  if (g.mode != kSwiGLU || g.G > kMaxGroups || g.Kd % 128 != 0 || a_scale == nullptr ||
+      b_scale == nullptr || g.gather_rows != nullptr)
+    return cudaErrorInvalidValue;
+  if (g.swap_tokens > 0) {
+    const int bt = tc_swap_tokens(g.swap_tokens);
+    if (bt == 16) return launch_one<16, kSwiGLU, true, false, true>(g, err, num_sms, s, a_scale, b_scale);
+    if (bt == 32) return launch_one<32, kSwiGLU, true, false, true>(g, err, num_sms, s, a_scale, b_scale);
+    return launch_one<64, kSwiGLU, true, false, true>(g, err, num_sms, s, a_scale, b_scale);
+  }
+  return launch_one<256, kSwiGLU, false, false, true>(g, err, num_sms, s, a_scale, b_scale);
 }
 
 cudaError_t launch_grouped_gemm_tc(const GroupedGemm& g, unsigned* err, int num_sms,

@@ -174,6 +174,14 @@ struct GroupedGemm {
 
 
 cudaError_t launch_grouped_gemm_simt(const GroupedGemm& g, cudaStream_t s);
+// FP8 (E4M3) per-row quantisation of a bf16 [rows, cols] matrix (quant.cu); cols % 8 == 0.
+cudaError_t launch_quantize_fp8(const void* in, long long rows, int cols, uint8_t* codes,
+                                float* scales, cudaStream_t s);
+// The gate/up GEMM on E4M3 operands (A [rows_alloc, Kd] and B [G, Nb, Kd] codes, Kd % 128
+// == 0) with per-row scales a_scale [rows_alloc] and b_scale [G, Nb]; single CTAs (swapped
+// for decode-sized batches), bf16 h.
+cudaError_t launch_gate_up_fp8(const GroupedGemm& g, const float* a_scale, const float* b_scale,
+                               unsigned* err, int num_sms, cudaStream_t s);
 cudaError_t launch_grouped_gemm_tc(const GroupedGemm& g, unsigned* err, int num_sms,
                                    cudaStream_t s);
 

@@ -353,6 +353,80 @@ def test_pair_tiles_with_swapped_tails(moe, H_, I):
                      what="down")
 
 
+def _e4m3_bytes(values):
+    """The E4M3 bit patterns of float64 values that are exact E4M3 numbers."""
+    return torch.from_numpy(np.asarray(values, dtype=np.float32)).to(torch.float8_e4m3fn).view(
+        torch.uint8).numpy()
+
+
+def test_quantize_fp8_bit_exact(moe):
+    gen = torch.Generator().manual_seed(31)
+    a = torch.randn(300, 384, generator=gen) * torch.rand(300, 1, generator=gen) * 20
+    a[7] = 0.0                      # an all-zero row: scale 1
+    a[11, 5] = 1e4                  # one large value: the rest of the row goes subnormal
+    a[13] = 1e-6 * torch.randn(384, generator=gen)
+    x = a.to(torch.bfloat16).cuda()
+    codes = torch.full((300, 384), 0x55, dtype=torch.uint8, device="cuda")
+    scales = torch.full((300,), -1.0, dtype=torch.float32, device="cuda")
+    moe.quantize_fp8(x, codes, scales)
+    torch.cuda.synchronize()
+    ref_codes, ref_scales = oracle.quantize_rows_fp8(x.float().cpu().numpy())
+    np.testing.assert_array_equal(scales.cpu().numpy(), ref_scales)
+    np.testing.assert_array_equal(codes.cpu().numpy(), _e4m3_bytes(ref_codes))
+
+
+FP8_CASES = [
+    # T, H, E, K, I, skew   (T <= 128: the decode-sized, swapped tiles)
+    (300, 256, 8, 2, 128, "none"), (1000, 512, 64, 4, 192, "normal"), (129, 384, 16, 8, 320, "empties"),
+    (64, 256, 16, 8, 128, "normal"), (8, 512, 32, 4, 128, "none"), (1, 256, 8, 2, 64, "none"),
+]
+
+
+@pytest.mark.parametrize("T,H_,E,K,I,skew", FP8_CASES)
+def test_gate_up_fp8_equals_oracle(moe, T, H_, E, K, I, skew):
+    """E4M3 activations and weights with per-row scales, quantised on the GPU (bit-exact
+    against the oracle's quantiser), then the FP8 gate/up against the oracle's FP8 gate/up
+    on the same codes: fp32 accumulation of exact products, h rounded once to bf16."""
+    shape, inp, offsets, x_perm, M = _ffn_inputs(T, H_, E, K, I, "bf16", skew)
+    x_perm[M:] = 0
+    c = _cfg(moe, T, H_, E, K, I=I, dtype="bf16")
+    ws = torch.empty(moe.workspace_size(c), dtype=torch.uint8, device="cuda")
+    xq = torch.empty(T * K, H_, dtype=torch.uint8, device="cuda")
+    xs = torch.empty(T * K, dtype=torch.float32, device="cuda")
+    moe.quantize_fp8(x_perm, xq, xs)
+    wq = torch.empty(E, 2 * I, H_, dtype=torch.uint8, device="cuda")
+    wsc = torch.empty(E, 2 * I, dtype=torch.float32, device="cuda")
+    moe.quantize_fp8(inp["w_gate_up"].reshape(E * 2 * I, H_), wq, wsc)
+    h = torch.full((T * K, I), -5.0, dtype=torch.bfloat16, device="cuda")
+    moe.expert_gate_up_fp8(c, xq, xs, torch.from_numpy(offsets).cuda(), wq, wsc, h, ws)
+    torch.cuda.synchronize()
+    moe.sync_check()
+    assert (h[M:] == -5.0).all()
+    xc, xsc = oracle.quantize_rows_fp8(x_perm[:M].float().cpu().numpy())
+    np.testing.assert_array_equal(xq[:M].cpu().numpy(), _e4m3_bytes(xc))
+    np.testing.assert_array_equal(xs[:M].cpu().numpy(), xsc)
+    wc, wsr = oracle.quantize_rows_fp8(inp["w_gate_up"].reshape(E * 2 * I, H_).float().cpu().numpy())
+    np.testing.assert_array_equal(wq.reshape(E * 2 * I, H_).cpu().numpy(), _e4m3_bytes(wc))
+    wc, wsr = wc.reshape(E, 2 * I, H_), wsr.reshape(E, 2 * I)
+    h_gpu = H.f64(h[:M])
+    h_ref = np.zeros((M, I))
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 > r0:
+            h_ref[r0:r1] = oracle.expert_gate_up_fp8(xc[r0:r1], xsc[r0:r1], wc[e], wsr[e])
+    # h is rounded once to bf16: half an ulp (2^-9 relative) plus fp32 accumulation
+    assert (np.abs(h_gpu - h_ref) <= 2.0 ** -8 * np.abs(h_ref) + 1e-4).all()
+    # and FP8 stays close to the bf16 gate/up (E4M3 keeps 3 mantissa bits)
+    h_bf16 = np.zeros((M, I))
+    xp = H.f64(x_perm[:M])
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 > r0:
+            h_bf16[r0:r1] = oracle.expert_gate_up(xp[r0:r1], H.f64(inp["w_gate_up"][e]))
+    rel = np.linalg.norm(h_gpu - h_bf16) / max(np.linalg.norm(h_bf16), 1e-30)
+    assert rel < 0.1
+
+
 @pytest.mark.parametrize("T,H_,E,K,I,dtype,skew", [c for c in FFN_CASES if c[5] == "bf16"])
 def test_gate_up_row_gather_equals_permuted_copy(moe, T, H_, E, K, I, dtype, skew):
     """The gate/up GEMM that gathers its rows from x by perm computes, row for row, the
