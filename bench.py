@@ -64,6 +64,9 @@ def parse():
                     help="fuse the combine into the down GEMM (MOE_FLAG_FUSED_COMBINE; "
                          "default for K >= 8)")
     ap.add_argument("--gather-combine", dest="fused", action="store_false")
+    ap.add_argument("--fp8", action="store_true",
+                    help="also time the FP8 (E4M3) gate/up: the token-row quantiser and the "
+                         "kind::f8f6f4 grouped GEMM (the layer itself stays bf16)")
     ap.add_argument("--capacity", action="store_true",
                     help="capacity-limited routing (MOE_FLAG_CAPACITY: ceil(1.2 T K / E) per expert)")
     ap.add_argument("--time-row-gather", action="store_true",
@@ -343,6 +346,18 @@ def run_ours(args, rank, world, local):
         # the row-gather variant (not used by the layer), for comparison
         stages["gate_up_gather"] = timed(lambda: moe.expert_gate_up_gather(
             cfg, inp["x"], perm, offsets, inp["w_gate_up"], h, ws, stream=stream), nst)
+    fp8 = None
+    if args.fp8 and shape.dtype == "bf16" and H_ % 128 == 0:
+        # weights quantised once (outside the timing), token rows per step
+        wq = torch.empty(E, 2 * shape.I, H_, dtype=torch.uint8, device=dev)
+        wsc = torch.empty(E, 2 * shape.I, dtype=torch.float32, device=dev)
+        moe.quantize_fp8(inp["w_gate_up"].reshape(E * 2 * shape.I, H_), wq, wsc, stream=stream)
+        xq = torch.empty(T * K, H_, dtype=torch.uint8, device=dev)
+        xs = torch.empty(T * K, dtype=torch.float32, device=dev)
+        stages["quantize_x_fp8"] = timed(lambda: moe.quantize_fp8(x_perm, xq, xs, stream=stream), nst)
+        fp8 = timed(lambda: moe.expert_gate_up_fp8(cfg, xq, xs, offsets, wq, wsc, h, ws,
+                                                  stream=stream), max(args.steps, 5))
+        stages["gate_up_fp8"] = fp8
     stages["down"] = timed(lambda: moe.expert_down(cfg, h, offsets, inp["w_down"], out_perm, ws,
                                                    stream=stream), nst)
     shared_out = None
@@ -378,6 +393,26 @@ def run_ours(args, rank, world, local):
                                        f"{args.config}-T{T}", "gate_up")
     roof["kernel"] = gu_kernel
     roof["peak_source"] = peak_kind
+
+    # the FP8 gate/up variant (--fp8): E4M3 operands; the FP8 tensor peak is the measured
+    # bf16 peak times the nominal FP8/bf16 ratio (4.5 / 2.25 PFLOP/s)
+    fp8_roof = None
+    if fp8 is not None:
+        f8_s = statistics.mean(fp8) / 1e3
+        if decode:
+            f8_bytes = (T * H_ + 2 * shape.I * H_ * alg["touched"] + alg["M"] * shape.I * 2 +
+                        4 * (T * K + 2 * shape.I * alg["touched"]))
+            a8 = f8_bytes / f8_s / 1e9
+            fp8_roof = {"bound": "hbm", "achieved": round(a8, 1), "peak": peaks["hbm_gbs"],
+                        "unit": "GB/s", "frac": round(a8 / peaks["hbm_gbs"], 4)}
+        else:
+            pk8 = 2.0 * peaks["bf16_tflops"]
+            a8 = alg["gate_up_flops"] / f8_s / 1e12
+            fp8_roof = {"bound": "tensor", "achieved": round(a8, 1), "peak": round(pk8, 1),
+                        "unit": "TFLOP/s", "frac": round(a8 / pk8, 4),
+                        "peak_note": "2 x measured bf16 (nominal fp8/bf16 ratio)"}
+        fp8_roof["us"] = round(f8_s * 1e6, 2)
+        fp8_roof["kernel"] = "tc_grouped_gemm_kernel<...,SwiGLU,F8> (moe_expert_gate_up_fp8)"
 
     # whole-layer roofline: the slower of FLOPs at the bf16 peak and bytes at HBM speed
     t_roof = max(alg["flops"] / (peaks["bf16_tflops"] * 1e12), alg["bytes"] / (peaks["hbm_gbs"] * 1e9))
@@ -430,6 +465,7 @@ def run_ours(args, rank, world, local):
                    "kept_assignments": alg["M"], "experts_touched": alg["touched"],
                    "group_rows_max": int(counts.max()), "empty_experts": int((counts == 0).sum())},
         "roofline": roof,
+        **({"fp8_gate_up": fp8_roof} if fp8_roof is not None else {}),
         "layer_roofline": {"t_roofline_us": round(t_roof * 1e6, 2), "frac": round(layer_frac, 4),
                            "flops": alg["flops"], "bytes": alg["bytes"], "peaks": peak_kind},
         "stages_us": stages_us,
