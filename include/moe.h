@@ -233,6 +233,21 @@ moe_status_t moe_expert_gate_up_fp8(const moe_config_t* cfg, const uint8_t* x_co
                                     const uint8_t* w_codes, const float* w_scales, void* h,
                                     void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* The output projection on FP8 operands: moe_expert_down with E4M3 codes and per-row
+ * scales (see moe_quantize_fp8): h quantised per row (T*K rows of I), W_d per output
+ * channel (E*H rows of I).  For every row r of group e:
+ *   out_perm[r,n] = hs[r] * ws[e,n] * sum_k hq[r,k] wq[e,n,k] (fp32 accumulation).
+ *   h_codes [T*K,I] uint8, h_scales [T*K] float; offsets [E+1] int32; w_codes [E,H,I]
+ *   uint8, w_scales [E,H] float; out_perm [T*K,H] float out (rows >= offsets[E]
+ *   untouched); ws as for moe_grouped_ffn.  bf16 layers only, I % 128 == 0 (else
+ *   MOE_ERR_UNSUPPORTED).
+ * Defined by: page section "单机MoE执行流水线" (each expert's output projection) and
+ * "MoE大模型的智能调度…" §4.1 (8-bit expert weights). */
+moe_status_t moe_expert_down_fp8(const moe_config_t* cfg, const uint8_t* h_codes,
+                                 const float* h_scales, const int32_t* offsets,
+                                 const uint8_t* w_codes, const float* w_scales, float* out_perm,
+                                 void* ws, size_t ws_bytes, moe_stream_t stream);
+
 /* The second GEMM of the grouped FFN alone: the output projection.
  * Defined by: page section "单机MoE执行流水线" (each expert applies its output
  * projection).  For every row r of group e: out_perm[r] = h[r] W_d[e]^T (fp32).

@@ -17,7 +17,7 @@ from typing import Optional
 
 __all__ = [
     "MoEConfig", "MoEError", "F32", "BF16", "FLAG_FUSED_COMBINE", "FLAG_CAPACITY", "library_path", "load", "workspace_size",
-    "route", "permute", "permute_noalloc", "grouped_ffn", "expert_gate_up", "expert_gate_up_gather", "quantize_fp8", "expert_gate_up_fp8", "expert_down", "combine", "layer_forward", "workspace_views",
+    "route", "permute", "permute_noalloc", "grouped_ffn", "expert_gate_up", "expert_gate_up_gather", "quantize_fp8", "expert_gate_up_fp8", "expert_down_fp8", "expert_down", "combine", "layer_forward", "workspace_views",
     "sync_check", "debug_wait_timeout", "status_string", "version",
 ]
 
@@ -76,6 +76,7 @@ _SIGS = {
     "moe_expert_gate_up_gather": [_CFG, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "moe_quantize_fp8": [_P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P],
     "moe_expert_gate_up_fp8": [_CFG, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+    "moe_expert_down_fp8": [_CFG, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "moe_expert_down": [_CFG, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "moe_combine": [_CFG, _P, _P, _P, _P, _P, _P, _P],
     "moe_layer_forward": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
@@ -199,6 +200,15 @@ def expert_gate_up_fp8(cfg, x_codes, x_scales, offsets, w_codes, w_scales, h, ws
                                          _ptr(offsets), _ptr(w_codes), _ptr(w_scales), _ptr(h),
                                          _ptr(ws), nb, _stream(stream)),
            "moe_expert_gate_up_fp8")
+
+
+def expert_down_fp8(cfg, h_codes, h_scales, offsets, w_codes, w_scales, out_perm, ws,
+                    ws_bytes=None, stream=None):
+    nb = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check(load().moe_expert_down_fp8(ctypes.byref(cfg), _ptr(h_codes), _ptr(h_scales),
+                                      _ptr(offsets), _ptr(w_codes), _ptr(w_scales),
+                                      _ptr(out_perm), _ptr(ws), nb, _stream(stream)),
+           "moe_expert_down_fp8")
 
 
 def expert_down(cfg, h, offsets, w_down, out_perm, ws, ws_bytes=None, stream=None):

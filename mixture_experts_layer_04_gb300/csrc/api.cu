@@ -549,6 +549,38 @@ moe_status_t moe_expert_gate_up_fp8(const moe_config_t* cfg, const uint8_t* x_co
                                         static_cast<cudaStream_t>(stream)));
 }
 
+moe_status_t moe_expert_down_fp8(const moe_config_t* cfg, const uint8_t* h_codes,
+                                 const float* h_scales, const int32_t* offsets,
+                                 const uint8_t* w_codes, const float* w_scales, float* out_perm,
+                                 void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_config(cfg));
+  if (cfg->T == 0) return MOE_OK;
+  if (cfg->dtype != MOE_BF16 || cfg->I % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (h_codes == nullptr || h_scales == nullptr || offsets == nullptr || w_codes == nullptr ||
+      w_scales == nullptr || out_perm == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (any_misaligned({h_codes, offsets, w_codes, out_perm})) return MOE_ERR_MISALIGNED;
+  Plan p;
+  MOE_TRY(check_ws(cfg, ws, ws_bytes, &p));
+  const DeviceInfo* d = nullptr;
+  MOE_TRY(check_device(&d));
+  GroupedGemm g{};
+  g.mode = kPlain;
+  g.dtype = cfg->dtype;
+  g.A = h_codes;
+  g.rows_alloc = cfg->T * cfg->K;
+  g.Kd = cfg->I;
+  g.B = w_codes;
+  g.G = cfg->E;
+  g.Nb = cfg->H;
+  g.N_out = cfg->H;
+  g.C = out_perm;
+  g.offsets = offsets;
+  g.swap_tokens = cfg->T <= kSwapMaxTokens ? cfg->T : 0;
+  return cuda_status(launch_down_fp8(g, h_scales, w_scales, d->err, d->num_sms,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
 moe_status_t moe_expert_gate_up_gather(const moe_config_t* cfg, const void* x,
                                        const int32_t* perm, const int32_t* offsets,
                                        const void* w_gate_up, void* h, void* ws, size_t ws_bytes,

@@ -296,11 +296,25 @@ __device__ __forceinline__ void epilogue_rows(const TcParams& p, uint32_t t_row,
       const int grow = tile_row0 + lane;
       rw = grow < row_end ? __ldg(p.row_w + grow) : 0.f;
     }
+    // FP8 operands: this thread's row scale and the group's output-channel scales
+    const float* sb = nullptr;
+    if (p.a_scale != nullptr) {
+      rw *= tile_row0 + lane < row_end ? __ldg(p.a_scale + tile_row0 + lane) : 0.f;
+      sb = p.b_scale + static_cast<size_t>(group) * p.b_rows;
+    }
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       uint32_t r[32];
       tmem_ld_32x32b_x32(t_row + c, r);
       tmem_ld_wait();
+      if (sb != nullptr) {
+        const int cl = col0 + c + lane;
+        const float sc = cl < p.N_out ? __ldg(sb + cl) : 0.f;
+        const float rs = MODE == kScatter ? 1.f : rw;  // kScatter applies rw below
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          r[j] = __float_as_uint(__uint_as_float(r[j]) * (rs * __shfl_sync(0xffffffffu, sc, j)));
+      }
       if constexpr (MODE == kScatter) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * rw);
@@ -772,10 +786,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           float* C = static_cast<float*>(p.C);
           const int col = col0 + quad * 32 + lane;
           const float b = (p.col_bias != nullptr && col < p.N_out) ? __ldg(p.col_bias + col) : 0.f;
+          // FP8 operands: this lane's output-channel scale; token-row scales per column
+          const float sw = (p.a_scale != nullptr && col < p.N_out)
+                               ? __ldg(p.b_scale + static_cast<size_t>(g) * p.b_rows + col)
+                               : 1.f;
 #pragma unroll 1
           for (int c = 0; c < BN; c += kNC) {
             float v[32];
             tmem_ld_cols<kNC>(t_row + c, v);
+            if (p.a_scale != nullptr) {
+              const float sx = row0 + c + lane < row_end ? __ldg(p.a_scale + row0 + c + lane) : 0.f;
+#pragma unroll
+              for (int j = 0; j < kNC; ++j) v[j] *= sw * __shfl_sync(0xffffffffu, sx, j);
+            }
 #pragma unroll
             for (int j = 0; j < kNC; ++j) {
               const int row = row0 + c + j;
@@ -1379,6 +1402,27 @@ cudaError_t launch_gate_up_fp8(const GroupedGemm& g, const float* a_scale, const
     return launch_one<64, kSwiGLU, true, false, true>(g, err, num_sms, s, a_scale, b_scale);
   }
   return launch_one<256, kSwiGLU, false, false, true>(g, err, num_sms, s, a_scale, b_scale);
+}
+
+cudaError_t launch_down_fp8(const GroupedGemm& g, const float* a_scale, const float* b_scale,
+                            unsigned* err, int num_sms, cudaStream_t s) {
+  if ((g.mode != kPlain && g.mode != kScatter) || g.G > kMaxGroups || g.Kd % 128 != 0 ||
+      a_scale == nullptr || b_scale == nullptr || g.gather_rows != nullptr)
+    return cudaErrorInvalidValue;
+  if (g.swap_tokens > 0) {
+    const int bt = tc_swap_tokens(g.swap_tokens);
+    if (g.mode == kScatter) {
+      if (bt == 16) return launch_one<16, kScatter, true, false, true>(g, err, num_sms, s, a_scale, b_scale);
+      if (bt == 32) return launch_one<32, kScatter, true, false, true>(g, err, num_sms, s, a_scale, b_scale);
+      return launch_one<64, kScatter, true, false, true>(g, err, num_sms, s, a_scale, b_scale);
+    }
+    if (bt == 16) return launch_one<16, kPlain, true, false, true>(g, err, num_sms, s, a_scale, b_scale);
+    if (bt == 32) return launch_one<32, kPlain, true, false, true>(g, err, num_sms, s, a_scale, b_scale);
+    return launch_one<64, kPlain, true, false, true>(g, err, num_sms, s, a_scale, b_scale);
+  }
+  if (g.mode == kScatter)
+    return launch_one<256, kScatter, false, false, true>(g, err, num_sms, s, a_scale, b_scale);
+  return launch_one<256, kPlain, false, false, true>(g, err, num_sms, s, a_scale, b_scale);
 }
 
 cudaError_t launch_grouped_gemm_tc(const GroupedGemm& g, unsigned* err, int num_sms,

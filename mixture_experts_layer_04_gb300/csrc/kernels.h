@@ -182,6 +182,10 @@ cudaError_t launch_quantize_fp8(const void* in, long long rows, int cols, uint8_
 // for decode-sized batches), bf16 h.
 cudaError_t launch_gate_up_fp8(const GroupedGemm& g, const float* a_scale, const float* b_scale,
                                unsigned* err, int num_sms, cudaStream_t s);
+// The down projection (kPlain, or kScatter for the fused combine) on E4M3 operands: h codes
+// [rows_alloc, Kd] with a_scale per row, W_d codes [G, Nb, Kd] with b_scale per output channel.
+cudaError_t launch_down_fp8(const GroupedGemm& g, const float* a_scale, const float* b_scale,
+                            unsigned* err, int num_sms, cudaStream_t s);
 cudaError_t launch_grouped_gemm_tc(const GroupedGemm& g, unsigned* err, int num_sms,
                                    cudaStream_t s);
 

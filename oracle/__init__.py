@@ -8,6 +8,7 @@ from .moe_oracle import (  # noqa: F401
     capacity,
     combine,
     expert_down,
+    expert_down_fp8,
     expert_gate_up,
     expert_gate_up_fp8,
     gate_drop,

@@ -58,6 +58,7 @@ __all__ = [
     "quantize_e4m3",
     "quantize_rows_fp8",
     "expert_gate_up_fp8",
+    "expert_down_fp8",
     "silu",
     "swiglu_ffn",
     "expert_gate_up",
@@ -304,6 +305,15 @@ def expert_gate_up_fp8(x_codes, x_scale, w_codes, w_scale):
         np.asarray(w_scale, dtype=np.float64)[None, :]
     I = acc.shape[1] // 2
     return silu(acc[:, :I]) * acc[:, I:]
+
+
+def expert_down_fp8(h_codes, h_scale, w_codes, w_scale):
+    """The output projection on E4M3 operands: o[r, n] = h_scale[r] * w_scale[n] *
+    sum_k hq[r, k] wq[n, k], the code dot products exact in float64 (W_d rows = output
+    channels, one scale each)."""
+    acc = np.asarray(h_codes, dtype=np.float64) @ np.asarray(w_codes, dtype=np.float64).T
+    return acc * np.asarray(h_scale, dtype=np.float64)[:, None] * \
+        np.asarray(w_scale, dtype=np.float64)[None, :]
 
 
 def expert_down(h_rows, w_down):

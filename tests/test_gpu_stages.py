@@ -427,6 +427,49 @@ def test_gate_up_fp8_equals_oracle(moe, T, H_, E, K, I, skew):
     assert rel < 0.1
 
 
+FP8_DOWN_CASES = [
+    # T, H, E, K, I, skew   (I % 128 == 0: the down projection's reduction is I)
+    (300, 256, 8, 2, 128, "none"), (1000, 512, 64, 4, 256, "normal"), (129, 384, 16, 8, 384, "empties"),
+    (64, 256, 16, 8, 128, "normal"), (8, 512, 32, 4, 128, "none"), (1, 256, 8, 2, 128, "none"),
+]
+
+
+@pytest.mark.parametrize("T,H_,E,K,I,skew", FP8_DOWN_CASES)
+def test_down_fp8_equals_oracle(moe, T, H_, E, K, I, skew):
+    """E4M3 h rows and W_d output channels with per-row scales, quantised on the GPU
+    (bit-exact against the oracle), then the FP8 down projection against the oracle's on
+    the same codes (fp32 accumulation of exact products)."""
+    shape, inp, offsets, _, M = _ffn_inputs(T, H_, E, K, I, "bf16", skew)
+    c = _cfg(moe, T, H_, E, K, I=I, dtype="bf16")
+    ws = torch.empty(moe.workspace_size(c), dtype=torch.uint8, device="cuda")
+    gen = torch.Generator().manual_seed(T + I)
+    h = torch.zeros(T * K, I, dtype=torch.bfloat16, device="cuda")
+    h[:M] = (torch.randn(M, I, generator=gen) * 0.05).to(torch.bfloat16).cuda()
+    hq = torch.empty(T * K, I, dtype=torch.uint8, device="cuda")
+    hs = torch.empty(T * K, dtype=torch.float32, device="cuda")
+    moe.quantize_fp8(h, hq, hs)
+    wq = torch.empty(E, H_, I, dtype=torch.uint8, device="cuda")
+    wsc = torch.empty(E, H_, dtype=torch.float32, device="cuda")
+    moe.quantize_fp8(inp["w_down"].reshape(E * H_, I), wq, wsc)
+    out = torch.full((T * K, H_), -5.0, dtype=torch.float32, device="cuda")
+    moe.expert_down_fp8(c, hq, hs, torch.from_numpy(offsets).cuda(), wq, wsc, out, ws)
+    torch.cuda.synchronize()
+    moe.sync_check()
+    assert (out[M:] == -5.0).all()
+    hc, hsc = oracle.quantize_rows_fp8(h[:M].float().cpu().numpy())
+    np.testing.assert_array_equal(hq[:M].cpu().numpy(), _e4m3_bytes(hc))
+    np.testing.assert_array_equal(hs[:M].cpu().numpy(), hsc)
+    wc, wsr = oracle.quantize_rows_fp8(inp["w_down"].reshape(E * H_, I).float().cpu().numpy())
+    wc, wsr = wc.reshape(E, H_, I), wsr.reshape(E, H_)
+    o_ref = np.zeros((M, H_))
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 > r0:
+            o_ref[r0:r1] = oracle.expert_down_fp8(hc[r0:r1], hsc[r0:r1], wc[e], wsr[e])
+    H.assert_close_y(out[:M].double().cpu().numpy(), o_ref, max_abs=1e-4, rel_l2=1e-5,
+                     what="down_fp8")
+
+
 @pytest.mark.parametrize("T,H_,E,K,I,dtype,skew", [c for c in FFN_CASES if c[5] == "bf16"])
 def test_gate_up_row_gather_equals_permuted_copy(moe, T, H_, E, K, I, dtype, skew):
     """The gate/up GEMM that gathers its rows from x by perm computes, row for row, the

@@ -72,3 +72,16 @@ def test_fp8_gate_up_reduces_to_plain_on_exact_operands():
     u = (x @ w[24:].T) * sx[:, None] * sw[None, 24:]
     np.testing.assert_allclose(oracle.expert_gate_up_fp8(x, sx, w, sw), oracle.silu(g) * u,
                                rtol=1e-12)
+
+
+def test_fp8_down_reduces_to_plain_on_exact_operands():
+    rng = np.random.default_rng(4)
+    h = oracle.quantize_e4m3((rng.standard_normal((30, 96)) * 2).astype(np.float32))
+    w = oracle.quantize_e4m3((rng.standard_normal((40, 96)) * 2).astype(np.float32))
+    np.testing.assert_allclose(
+        oracle.expert_down_fp8(h, np.ones(30, np.float32), w, np.ones(40, np.float32)),
+        oracle.expert_down(h, w), rtol=1e-15, atol=0)
+    sh = rng.uniform(0.5, 2, 30).astype(np.float32)
+    sw = rng.uniform(0.5, 2, 40).astype(np.float32)
+    np.testing.assert_allclose(oracle.expert_down_fp8(h, sh, w, sw),
+                               (h @ w.T) * sh[:, None] * sw[None, :], rtol=1e-12)
