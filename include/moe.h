@@ -79,7 +79,11 @@ enum {
    * not use capacity.  If fewer than K experts are available the missing slots hold -1 / 0
    * (a suffix, like dropped slots).  E <= 1024.  The result is deterministic and equals
    * the token-by-token rule; it runs as one extra single-CTA launch after the router. */
-  MOE_FLAG_CAPACITY = 2u
+  MOE_FLAG_CAPACITY = 2u,
+  /* moe_workspace_size and moe_layer_forward_fp8: the routed experts run on FP8 (E4M3)
+   * codes (see moe_layer_forward_fp8); the workspace then also holds the codes and scales
+   * of x and h.  moe_layer_forward rejects this flag. */
+  MOE_FLAG_FP8 = 4u
 };
 
 typedef struct {
@@ -205,6 +209,26 @@ moe_status_t moe_expert_gate_up_gather(const moe_config_t* cfg, const void* x,
                                        const int32_t* perm, const int32_t* offsets,
                                        const void* w_gate_up, void* h, void* ws,
                                        size_t ws_bytes, moe_stream_t stream);
+
+/* The whole layer with FP8 (E4M3) routed experts, as moe_layer_forward otherwise: routing
+ * (capacity-limited with MOE_FLAG_CAPACITY), then x quantised per token row, the dispatch
+ * of the one-byte rows, the FP8 gate/up (moe_expert_gate_up_fp8) to bf16 h, h quantised
+ * per row, the FP8 down projection (moe_expert_down_fp8), the bf16 shared expert and the
+ * gather combine.
+ * Defined by: page section "单机MoE执行流水线" (the layer's stages) and
+ * "MoE大模型的智能调度…" §4.1 (8-bit expert weights).
+ *   w_gate_up_codes [E,2I,H] uint8 and w_gate_up_scales [E,2I] float, w_down_codes [E,H,I]
+ *   uint8 and w_down_scales [E,H] float, from moe_quantize_fp8 of the bf16 weights (rows =
+ *   output channels); the other arguments as moe_layer_forward.
+ * cfg->flags must include MOE_FLAG_FP8 (the workspace size depends on it) and must not
+ * include MOE_FLAG_FUSED_COMBINE; bf16 layers with H % 128 == 0 and I % 128 == 0 (else
+ * MOE_ERR_UNSUPPORTED). */
+moe_status_t moe_layer_forward_fp8(const moe_config_t* cfg, const void* x, const void* w_router,
+                                   const float* router_bias, const uint8_t* w_gate_up_codes,
+                                   const float* w_gate_up_scales, const uint8_t* w_down_codes,
+                                   const float* w_down_scales, const void* w_shared_gate_up,
+                                   const void* w_shared_down, void* y, float* y_f32, void* ws,
+                                   size_t ws_bytes, moe_stream_t stream);
 
 /* Per-row FP8 (E4M3) quantisation, for low-precision experts.
  * Defined by: "MoE大模型的智能调度…" §4.1 (the resident experts' weights are quantised to 8

@@ -16,8 +16,8 @@ import os
 from typing import Optional
 
 __all__ = [
-    "MoEConfig", "MoEError", "F32", "BF16", "FLAG_FUSED_COMBINE", "FLAG_CAPACITY", "library_path", "load", "workspace_size",
-    "route", "permute", "permute_noalloc", "grouped_ffn", "expert_gate_up", "expert_gate_up_gather", "quantize_fp8", "expert_gate_up_fp8", "expert_down_fp8", "expert_down", "combine", "layer_forward", "workspace_views",
+    "MoEConfig", "MoEError", "F32", "BF16", "FLAG_FUSED_COMBINE", "FLAG_CAPACITY", "FLAG_FP8", "library_path", "load", "workspace_size",
+    "route", "permute", "permute_noalloc", "grouped_ffn", "expert_gate_up", "expert_gate_up_gather", "quantize_fp8", "expert_gate_up_fp8", "expert_down_fp8", "layer_forward_fp8", "expert_down", "combine", "layer_forward", "workspace_views",
     "sync_check", "debug_wait_timeout", "status_string", "version",
 ]
 
@@ -27,6 +27,7 @@ BF16 = 1
 # correct to fp32 rounding but not bitwise reproducible run to run)
 FLAG_FUSED_COMBINE = 1
 FLAG_CAPACITY = 2
+FLAG_FP8 = 4
 
 _STATUS = {
     0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
@@ -77,6 +78,8 @@ _SIGS = {
     "moe_quantize_fp8": [_P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P],
     "moe_expert_gate_up_fp8": [_CFG, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "moe_expert_down_fp8": [_CFG, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+    "moe_layer_forward_fp8": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                              ctypes.c_size_t, _P],
     "moe_expert_down": [_CFG, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "moe_combine": [_CFG, _P, _P, _P, _P, _P, _P, _P],
     "moe_layer_forward": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
@@ -209,6 +212,17 @@ def expert_down_fp8(cfg, h_codes, h_scales, offsets, w_codes, w_scales, out_perm
                                       _ptr(offsets), _ptr(w_codes), _ptr(w_scales),
                                       _ptr(out_perm), _ptr(ws), nb, _stream(stream)),
            "moe_expert_down_fp8")
+
+
+def layer_forward_fp8(cfg, x, w_router, router_bias, w_gate_up_codes, w_gate_up_scales,
+                      w_down_codes, w_down_scales, w_shared_gate_up, w_shared_down, y, y_f32, ws,
+                      ws_bytes=None, stream=None):
+    nb = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check(load().moe_layer_forward_fp8(
+        ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(router_bias), _ptr(w_gate_up_codes),
+        _ptr(w_gate_up_scales), _ptr(w_down_codes), _ptr(w_down_scales), _ptr(w_shared_gate_up),
+        _ptr(w_shared_down), _ptr(y), _ptr(y_f32), _ptr(ws), nb, _stream(stream)),
+        "moe_layer_forward_fp8")
 
 
 def expert_down(cfg, h, offsets, w_down, out_perm, ws, ws_bytes=None, stream=None):

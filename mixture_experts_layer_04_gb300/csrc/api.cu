@@ -53,7 +53,8 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 moe_status_t check_config(const moe_config_t* c) {
   if (c == nullptr) return MOE_ERR_INVALID_ARG;
-  if ((c->flags & ~static_cast<uint32_t>(MOE_FLAG_FUSED_COMBINE | MOE_FLAG_CAPACITY)) != 0u)
+  if ((c->flags & ~static_cast<uint32_t>(MOE_FLAG_FUSED_COMBINE | MOE_FLAG_CAPACITY |
+                                         MOE_FLAG_FP8)) != 0u)
     return MOE_ERR_INVALID_ARG;
   if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if (c->T < 0 || c->H <= 0 || c->E <= 0 || c->K <= 0 || c->I <= 0 || c->I_shared < 0)
@@ -73,7 +74,7 @@ bool use_tc_router(const moe_config_t* c) {
 // Workspace plan: every region 256-byte aligned.
 struct Plan {
   size_t logits, partial, ids, w, counts, offsets, perm, inv, perm_ws, table, num_mt, x_perm, h,
-      out_perm, row_w, y32,
+      out_perm, row_w, y32, x_codes, x_scales, xs_perm, h_codes, h_scales,
       shared_h, shared_out, total;
 };
 
@@ -114,6 +115,14 @@ Plan make_plan(const moe_config_t* c) {
   const bool fused = (c->flags & MOE_FLAG_FUSED_COMBINE) != 0u;
   p.row_w = take(fused ? T * K * 4 : 0);
   p.y32 = take(fused ? T * H * 4 : 0);
+  // FP8 experts (moe_layer_forward_fp8): x's codes and scales, the scales in row order, and
+  // h's codes and scales (the permuted codes reuse x_perm)
+  const bool fp8 = (c->flags & MOE_FLAG_FP8) != 0u;
+  p.x_codes = take(fp8 ? T * H : 0);
+  p.x_scales = take(fp8 ? T * 4 : 0);
+  p.xs_perm = take(fp8 ? T * K * 4 : 0);
+  p.h_codes = take(fp8 ? T * K * I : 0);
+  p.h_scales = take(fp8 ? T * K * 4 : 0);
   p.total = o;
   return p;
 }
@@ -639,12 +648,113 @@ moe_status_t moe_combine(const moe_config_t* cfg, const float* out_perm, const i
                                     cfg->T, cfg->H, cfg->K, static_cast<cudaStream_t>(stream)));
 }
 
+moe_status_t moe_layer_forward_fp8(const moe_config_t* cfg, const void* x, const void* w_router,
+                                   const float* router_bias, const uint8_t* w_gate_up_codes,
+                                   const float* w_gate_up_scales, const uint8_t* w_down_codes,
+                                   const float* w_down_scales, const void* w_shared_gate_up,
+                                   const void* w_shared_down, void* y, float* y_f32, void* ws,
+                                   size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_config(cfg));
+  if ((cfg->flags & MOE_FLAG_FP8) == 0u || (cfg->flags & MOE_FLAG_FUSED_COMBINE) != 0u)
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->T == 0) return MOE_OK;
+  if (cfg->dtype != MOE_BF16 || cfg->H % 128 != 0 || cfg->I % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (x == nullptr || w_router == nullptr || w_gate_up_codes == nullptr ||
+      w_gate_up_scales == nullptr || w_down_codes == nullptr || w_down_scales == nullptr ||
+      y == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  const bool shared = cfg->I_shared > 0;
+  if (shared != (w_shared_gate_up != nullptr) || shared != (w_shared_down != nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (any_misaligned({x, w_router, w_gate_up_codes, w_down_codes, y, w_shared_gate_up,
+                      w_shared_down, y_f32}))
+    return MOE_ERR_MISALIGNED;
+  const Plan p = make_plan(cfg);
+  if (ws == nullptr || ws_bytes < p.total) return MOE_ERR_WORKSPACE;
+  if (!aligned16(ws)) return MOE_ERR_MISALIGNED;
+  const DeviceInfo* d = nullptr;
+  MOE_TRY(check_device(&d));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int T = cfg->T, H = cfg->H, E = cfg->E, K = cfg->K, I = cfg->I;
+  float* logits = at<float>(ws, p.logits);
+  int32_t* ids = at<int32_t>(ws, p.ids);
+  float* w = at<float>(ws, p.w);
+  int32_t* counts = at<int32_t>(ws, p.counts);
+  int32_t* offsets = at<int32_t>(ws, p.offsets);
+  int32_t* perm = at<int32_t>(ws, p.perm);
+  int32_t* inv = at<int32_t>(ws, p.inv);
+  uint8_t* x_codes = at<uint8_t>(ws, p.x_codes);
+  float* x_scales = at<float>(ws, p.x_scales);
+  float* xs_perm = at<float>(ws, p.xs_perm);
+  uint8_t* xq_perm = at<uint8_t>(ws, p.x_perm);
+  void* h = at<void>(ws, p.h);
+  uint8_t* h_codes = at<uint8_t>(ws, p.h_codes);
+  float* h_scales = at<float>(ws, p.h_scales);
+  float* out_perm = at<float>(ws, p.out_perm);
+  // 1. routing (capacity-limited with MOE_FLAG_CAPACITY)
+  MOE_TRY(run_route(cfg, d, x, w_router, router_bias, logits, ids, w, at<float>(ws, p.partial),
+                    false, nullptr, s));
+  if ((cfg->flags & MOE_FLAG_CAPACITY) != 0u)
+    MOE_CUDA(launch_capacity_route(logits, ids, w, T, E, K, cfg->gate_threshold,
+                                   capacity_limit(T, K, E), d->err, s));
+  // 2. x's rows to E4M3 codes, then the dispatch moves the one-byte rows (as rows of H/2
+  //    bf16 units) and the scales follow the permutation
+  MOE_CUDA(launch_quantize_fp8(x, T, H, x_codes, x_scales, s));
+  MOE_CUDA(launch_permute(MOE_BF16, x_codes, ids, T, H / 2, E, K, counts, offsets, perm, inv,
+                          xq_perm, at<int32_t>(ws, p.perm_ws), nullptr, nullptr, kSimtBM, w,
+                          nullptr, s));
+  MOE_CUDA(launch_gather_scales(x_scales, perm, offsets + E, xs_perm, T * K, s));
+  // 3. FP8 gate/up -> bf16 h -> E4M3 h -> FP8 down
+  GroupedGemm g{};
+  g.mode = kSwiGLU;
+  g.dtype = MOE_BF16;
+  g.A = xq_perm;
+  g.rows_alloc = T * K;
+  g.Kd = H;
+  g.B = w_gate_up_codes;
+  g.G = E;
+  g.Nb = 2 * I;
+  g.N_out = I;
+  g.up_offset = I;
+  g.C = h;
+  g.offsets = offsets;
+  g.swap_tokens = T <= kSwapMaxTokens ? T : 0;
+  MOE_CUDA(launch_gate_up_fp8(g, xs_perm, w_gate_up_scales, d->err, d->num_sms, s));
+  MOE_CUDA(launch_quantize_fp8(h, static_cast<long long>(T) * K, I, h_codes, h_scales, s));
+  GroupedGemm gd{};
+  gd.mode = kPlain;
+  gd.dtype = MOE_BF16;
+  gd.A = h_codes;
+  gd.rows_alloc = T * K;
+  gd.Kd = I;
+  gd.B = w_down_codes;
+  gd.G = E;
+  gd.Nb = H;
+  gd.N_out = H;
+  gd.C = out_perm;
+  gd.offsets = offsets;
+  gd.swap_tokens = g.swap_tokens;
+  MOE_CUDA(launch_down_fp8(gd, h_scales, w_down_scales, d->err, d->num_sms, s));
+  // 4. shared expert (bf16), 5. combine
+  float* shared_out = nullptr;
+  if (shared) {
+    shared_out = at<float>(ws, p.shared_out);
+    Groups one{};
+    one.G = 1;
+    void* hs = at<void>(ws, p.shared_h);
+    MOE_TRY(run_gate_up(cfg, d, x, T, w_shared_gate_up, cfg->I_shared, hs, one, s));
+    MOE_TRY(run_down(cfg, d, hs, T, w_shared_down, cfg->I_shared, shared_out, one, s));
+  }
+  return cuda_status(launch_combine(cfg->dtype, out_perm, inv, w, shared_out, y, y_f32, T, H, K, s));
+}
+
 moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const void* w_router,
                                const float* router_bias, const void* w_gate_up,
                                const void* w_down, const void* w_shared_gate_up,
                                const void* w_shared_down, void* y, float* y_f32, void* ws,
                                size_t ws_bytes, moe_stream_t stream) {
   MOE_TRY(check_config(cfg));
+  if ((cfg->flags & MOE_FLAG_FP8) != 0u) return MOE_ERR_INVALID_ARG;  // moe_layer_forward_fp8
   if (cfg->T == 0) return MOE_OK;
   if (x == nullptr || w_router == nullptr || w_gate_up == nullptr || w_down == nullptr ||
       y == nullptr)

@@ -177,6 +177,9 @@ cudaError_t launch_grouped_gemm_simt(const GroupedGemm& g, cudaStream_t s);
 // FP8 (E4M3) per-row quantisation of a bf16 [rows, cols] matrix (quant.cu); cols % 8 == 0.
 cudaError_t launch_quantize_fp8(const void* in, long long rows, int cols, uint8_t* codes,
                                 float* scales, cudaStream_t s);
+// dst[r] = src[perm[r]] for r < offsets_end[0] (device), 0 for r < n beyond it (quant.cu).
+cudaError_t launch_gather_scales(const float* src, const int32_t* perm, const int32_t* offsets_end,
+                                 float* dst, int n, cudaStream_t s);
 // The gate/up GEMM on E4M3 operands (A [rows_alloc, Kd] and B [G, Nb, Kd] codes, Kd % 128
 // == 0) with per-row scales a_scale [rows_alloc] and b_scale [G, Nb]; single CTAs (swapped
 // for decode-sized batches), bf16 h.

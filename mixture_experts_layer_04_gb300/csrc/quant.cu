@@ -61,7 +61,28 @@ __global__ void __launch_bounds__(kQThreads)
   }
 }
 
+// dst[r] = src[perm[r]] for the dispatched rows r < offsets_end[0], 0 for the rest: the
+// token-row scales in the permuted row order.
+__global__ void __launch_bounds__(kQThreads)
+    gather_scales_kernel(const float* __restrict__ src, const int32_t* __restrict__ perm,
+                         const int32_t* __restrict__ offsets_end, float* __restrict__ dst,
+                         int n) {
+  grid_dep_wait();
+  grid_dep_trigger();
+  const int m = *offsets_end;
+  for (int r = blockIdx.x * kQThreads + threadIdx.x; r < n; r += gridDim.x * kQThreads)
+    dst[r] = r < m ? __ldg(src + __ldg(perm + r)) : 0.f;
+}
+
 }  // namespace
+
+cudaError_t launch_gather_scales(const float* src, const int32_t* perm, const int32_t* offsets_end,
+                                 float* dst, int n, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  const int want = (n + kQThreads - 1) / kQThreads;
+  return launch_pdl(gather_scales_kernel, dim3(want < 1024 ? want : 1024), dim3(kQThreads), 0, s,
+                    src, perm, offsets_end, dst, n);
+}
 
 cudaError_t launch_quantize_fp8(const void* in, long long rows, int cols, uint8_t* codes,
                                 float* scales, cudaStream_t s) {

@@ -69,7 +69,7 @@ def ws_size(c):
 @pytest.mark.parametrize("bad", [
     dict(K=0), dict(K=9), dict(E=2000, K=2), dict(K=17, E=32), dict(H=100), dict(I=96),
     dict(I_shared=32), dict(T=-1), dict(gate_threshold=1.0), dict(gate_threshold=-0.1),
-    dict(dtype=7), dict(flags=4), dict(flags=0x80000000),
+    dict(dtype=7), dict(flags=8), dict(flags=0x80000000),
 ])
 def test_invalid_configs_are_rejected(lib, bad):
     st, _ = ws_size(cfg(**bad))

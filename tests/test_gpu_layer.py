@@ -263,6 +263,68 @@ def test_layer_with_capacity_routing(moe, shape):
     assert torch.equal(run.y, run.y32.to(shape.torch_dtype))
 
 
+@pytest.mark.parametrize("shape", [
+    synth.MoEShape("fp8_prefill", T=300, H=256, E=8, K=2, I=128, seed=31),
+    synth.MoEShape("fp8_shared", T=129, H=384, E=16, K=8, I=256, I_shared=128, bias="normal",
+                   seed=32),
+    synth.MoEShape("fp8_decode", T=8, H=512, E=32, K=4, I=128, bias="zipf", seed=33),
+], ids=lambda s: s.name)
+def test_layer_fp8_equals_oracle(moe, shape):
+    """moe_layer_forward_fp8: E4M3 experts (weights per output channel, x and h per row)
+    against the oracle's FP8 expert chain.  The oracle routes from the layer's own fp32
+    logits; h is the oracle's (fp64, rounded once to bf16), so a rare one-ulp difference of
+    h can move one E4M3 code: the output is compared within the layer tolerance."""
+    T, H_, E, K, I = shape.T, shape.H, shape.E, shape.K, shape.I
+    inp = synth.make_inputs(shape, device="cuda")
+    cfg = moe.MoEConfig.make(T, H_, E, K, I, shape.I_shared, shape.theta, moe.BF16, moe.FLAG_FP8)
+    ws = torch.empty(moe.workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    wgq = torch.empty(E, 2 * I, H_, dtype=torch.uint8, device="cuda")
+    wgs = torch.empty(E, 2 * I, dtype=torch.float32, device="cuda")
+    moe.quantize_fp8(inp["w_gate_up"].reshape(E * 2 * I, H_), wgq, wgs)
+    wdq = torch.empty(E, H_, I, dtype=torch.uint8, device="cuda")
+    wds = torch.empty(E, H_, dtype=torch.float32, device="cuda")
+    moe.quantize_fp8(inp["w_down"].reshape(E * H_, I), wdq, wds)
+    y = torch.empty(T, H_, dtype=torch.bfloat16, device="cuda")
+    y32 = torch.empty(T, H_, dtype=torch.float32, device="cuda")
+    moe.layer_forward_fp8(cfg, inp["x"], inp["w_router"], inp["router_bias"], wgq, wgs, wdq, wds,
+                          inp.get("w_shared_gate_up"), inp.get("w_shared_down"), y, y32, ws)
+    torch.cuda.synchronize()
+    moe.sync_check()
+    run = H.LayerRun(moe, shape, inp)  # only for its workspace views
+    run.cfg, run.ws = cfg, ws
+    r = run.routing()
+    x64 = H.f64(inp["x"])
+    L_ref = oracle.router_logits(x64, H.f64(inp["w_router"]), _bias_np(inp))
+    assert np.abs(r["logits"] - L_ref).max() <= 1e-4 * max(1, np.abs(L_ref).max())
+    ids_ref, w_ref = oracle.route(r["logits"].astype(np.float32), K, shape.theta)
+    np.testing.assert_array_equal(r["ids"], ids_ref)
+    counts_ref, offsets_ref, perm_ref, inv_ref = oracle.permute(ids_ref, E)
+    np.testing.assert_array_equal(r["offsets"], offsets_ref)
+    xc, xs = oracle.quantize_rows_fp8(inp["x"].float().cpu().numpy())
+    wgc, wgsr = oracle.quantize_rows_fp8(inp["w_gate_up"].reshape(E * 2 * I, H_).float().cpu().numpy())
+    wdc, wdsr = oracle.quantize_rows_fp8(inp["w_down"].reshape(E * H_, I).float().cpu().numpy())
+    wgc, wgsr = wgc.reshape(E, 2 * I, H_), wgsr.reshape(E, 2 * I)
+    wdc, wdsr = wdc.reshape(E, H_, I), wdsr.reshape(E, H_)
+    M = int(offsets_ref[-1])
+    o_ref = np.zeros((M, H_))
+    for e in range(E):
+        r0, r1 = int(offsets_ref[e]), int(offsets_ref[e + 1])
+        if r1 == r0:
+            continue
+        rows = perm_ref[r0:r1]
+        h = oracle.expert_gate_up_fp8(xc[rows], xs[rows], wgc[e], wgsr[e])
+        h = torch.from_numpy(h).to(torch.bfloat16).float().numpy()  # rounded once to bf16
+        hc, hsc = oracle.quantize_rows_fp8(h)
+        o_ref[r0:r1] = oracle.expert_down_fp8(hc, hsc, wdc[e], wdsr[e])
+    shared_ref = None
+    if shape.I_shared:
+        shared_ref = oracle.swiglu_ffn(x64, H.f64(inp["w_shared_gate_up"]),
+                                       H.f64(inp["w_shared_down"]))
+    y_ref = oracle.combine(o_ref, inv_ref, w_ref, shared_ref)
+    H.assert_close_y(y32.double().cpu().numpy(), y_ref, **_tol(shape))
+    assert torch.equal(y, y32.to(torch.bfloat16))
+
+
 @pytest.mark.parametrize("case", ["T0", "T1", "K_eq_E", "one_expert", "empty_experts"])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_edge_cases(moe, case, dtype):
