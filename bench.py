@@ -358,6 +358,18 @@ def run_ours(args, rank, world, local):
         fp8 = timed(lambda: moe.expert_gate_up_fp8(cfg, xq, xs, offsets, wq, wsc, h, ws,
                                                   stream=stream), max(args.steps, 5))
         stages["gate_up_fp8"] = fp8
+        if H_ % 128 == 0 and shape.I % 128 == 0:
+            # the whole layer with FP8 experts (moe_layer_forward_fp8), gather combine
+            cfg8 = moe.MoEConfig.make(T, H_, E, K, shape.I, shape.I_shared, shape.theta, dt,
+                                      moe.FLAG_FP8 | (moe.FLAG_CAPACITY if args.capacity else 0))
+            ws8 = torch.empty(moe.workspace_size(cfg8), dtype=torch.uint8, device=dev)
+            wdq = torch.empty(E, H_, shape.I, dtype=torch.uint8, device=dev)
+            wds = torch.empty(E, H_, dtype=torch.float32, device=dev)
+            moe.quantize_fp8(inp["w_down"].reshape(E * H_, shape.I), wdq, wds, stream=stream)
+            stages["layer_fp8"] = timed(lambda: moe.layer_forward_fp8(
+                cfg8, inp["x"], inp["w_router"], inp["router_bias"], wq, wsc, wdq, wds,
+                inp.get("w_shared_gate_up"), inp.get("w_shared_down"), y, None, ws8,
+                stream=stream), nst)
     stages["down"] = timed(lambda: moe.expert_down(cfg, h, offsets, inp["w_down"], out_perm, ws,
                                                    stream=stream), nst)
     shared_out = None
