@@ -232,24 +232,28 @@ constexpr int kPairMinRowsPerGroup = 768;
 constexpr int kPairMinRowsSwiGLU = 384;
 constexpr int kPairWideDim = 4096;
 
+// CTA pairs (256-row tiles, 2/3 of the shared-memory traffic per MMA) pay for the padding
+// of each group's last tile when groups are large (>= 768 rows on average), or half that
+// size with a long reduction or a wide output to amortise it; otherwise single CTAs with
+// 128-row tiles (measured on GB300 with the workloads' groups).  The gate/up GEMM (bf16
+// output, a light epilogue) gains from pairs from 384 rows per group; a short-reduction down
+// projection with its fp32 output does not (Qwen3-shaped layer on GB300: gate/up on pairs
+// 0.650 -> 0.637 ms per layer, down on pairs +70 us).
+bool use_pairs(const GroupedGemm& g) {
+  const long long rows_per_group = g.rows_alloc / (g.G > 0 ? g.G : 1);
+  const bool big = rows_per_group >= kPairMinRowsPerGroup ||
+                   (rows_per_group >= kPairMinRowsPerGroup / 3 &&
+                    (g.Kd >= kPairWideDim || g.N_out >= kPairWideDim)) ||
+                   (g.mode == kSwiGLU && rows_per_group >= kPairMinRowsSwiGLU);
+  return g.swap_tokens == 0 && big && g.gather_rows == nullptr;
+}
+
 moe_status_t launch_gemm(const moe_config_t* c, const DeviceInfo* d, const GroupedGemm& g0,
                          cudaStream_t s) {
   if (c->dtype == MOE_BF16) {
     GroupedGemm g = g0;
     g.swap_tokens = c->T <= kSwapMaxTokens ? c->T : 0;
-    // CTA pairs (256-row tiles, 2/3 of the shared-memory traffic per MMA) pay for the
-    // padding of each group's last tile when groups are large (>= 768 rows on average),
-    // or half that size with a long reduction or a wide output to amortise it; otherwise
-    // single CTAs with 128-row tiles (measured on GB300 with the workloads' groups)
-    const long long rows_per_group = g.rows_alloc / (g.G > 0 ? g.G : 1);
-    // The gate/up GEMM (bf16 output, a light epilogue) gains from pairs from 384 rows per
-    // group; a short-reduction down projection with its fp32 output does not (Qwen3-shaped
-    // layer on GB300: gate/up on pairs 0.650 -> 0.637 ms per layer, down on pairs +70 us).
-    const bool big = rows_per_group >= kPairMinRowsPerGroup ||
-                     (rows_per_group >= kPairMinRowsPerGroup / 3 &&
-                      (g.Kd >= kPairWideDim || g.N_out >= kPairWideDim)) ||
-                     (g.mode == kSwiGLU && rows_per_group >= kPairMinRowsSwiGLU);
-    g.pair = (g.swap_tokens == 0 && big && g.gather_rows == nullptr) ? 1 : 0;
+    g.pair = use_pairs(g) ? 1 : 0;
     return cuda_status(launch_grouped_gemm_tc(g, d->err, d->num_sms, s));
   }
   return cuda_status(launch_grouped_gemm_simt(g0, s));
@@ -554,6 +558,7 @@ moe_status_t moe_expert_gate_up_fp8(const moe_config_t* cfg, const uint8_t* x_co
   g.C = h;
   g.offsets = offsets;
   g.swap_tokens = cfg->T <= kSwapMaxTokens ? cfg->T : 0;
+  g.pair = use_pairs(g) ? 1 : 0;
   return cuda_status(launch_gate_up_fp8(g, x_scales, w_scales, d->err, d->num_sms,
                                         static_cast<cudaStream_t>(stream)));
 }
@@ -586,6 +591,7 @@ moe_status_t moe_expert_down_fp8(const moe_config_t* cfg, const uint8_t* h_codes
   g.C = out_perm;
   g.offsets = offsets;
   g.swap_tokens = cfg->T <= kSwapMaxTokens ? cfg->T : 0;
+  g.pair = use_pairs(g) ? 1 : 0;
   return cuda_status(launch_down_fp8(g, h_scales, w_scales, d->err, d->num_sms,
                                      static_cast<cudaStream_t>(stream)));
 }
@@ -719,6 +725,7 @@ moe_status_t moe_layer_forward_fp8(const moe_config_t* cfg, const void* x, const
   g.C = h;
   g.offsets = offsets;
   g.swap_tokens = T <= kSwapMaxTokens ? T : 0;
+  g.pair = use_pairs(g) ? 1 : 0;
   MOE_CUDA(launch_gate_up_fp8(g, xs_perm, w_gate_up_scales, d->err, d->num_sms, s));
   MOE_CUDA(launch_quantize_fp8(h, static_cast<long long>(T) * K, I, h_codes, h_scales, s));
   GroupedGemm gd{};
@@ -734,6 +741,7 @@ moe_status_t moe_layer_forward_fp8(const moe_config_t* cfg, const void* x, const
   gd.C = out_perm;
   gd.offsets = offsets;
   gd.swap_tokens = g.swap_tokens;
+  gd.pair = use_pairs(gd) ? 1 : 0;
   MOE_CUDA(launch_down_fp8(gd, h_scales, w_down_scales, d->err, d->num_sms, s));
   // 4. shared expert (bf16), 5. combine
   float* shared_out = nullptr;

@@ -862,8 +862,16 @@ __device__ __forceinline__ int pair_tail_n(int row0, int row_end) {
 template <int MODE>
 __device__ __forceinline__ void epilogue_pair_tail(const TcParams& p, uint32_t t_row, uint8_t* stg,
                                                    int quad, int lane, int rank, int tn, int row0,
-                                                   int row_end, int n0) {
+                                                   int row_end, int n0, int group) {
   const int L = quad * 32 + lane;
+  // FP8 operands: scale v[j] (token row0 + c + j) by this lane's weight row and that token
+  auto scale = [&](float (&v)[32], int c, int wrow, bool live) {
+    if (p.a_scale == nullptr) return;
+    const float sw = live ? __ldg(p.b_scale + static_cast<size_t>(group) * p.b_rows + wrow) : 0.f;
+    const float sx = row0 + c + lane < row_end ? __ldg(p.a_scale + row0 + c + lane) : 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] *= sw * __shfl_sync(0xffffffffu, sx, j);
+  };
   if constexpr (MODE == kSwiGLU) {
     float* xchg = reinterpret_cast<float*>(stg);  // [64][32], rotated by row
     __nv_bfloat16* C = static_cast<__nv_bfloat16*>(p.C);
@@ -874,12 +882,14 @@ __device__ __forceinline__ void epilogue_pair_tail(const TcParams& p, uint32_t t
       if (quad >= 2) {
         const int r = L - 64;
         tmem_ld_cols<32>(t_row + c, v);
+        scale(v, c, p.up_offset + col, col < p.N_out);
 #pragma unroll
         for (int j = 0; j < 32; ++j) xchg[r * 32 + ((j + r) & 31)] = v[j];
       }
       epi_bar();
       if (quad < 2) {
         tmem_ld_cols<32>(t_row + c, v);
+        scale(v, c, col, col < p.N_out);
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const int tok = row0 + c + j;
@@ -899,6 +909,7 @@ __device__ __forceinline__ void epilogue_pair_tail(const TcParams& p, uint32_t t
     for (int c = 0; c < tn; c += 32) {
       float v[32];
       tmem_ld_cols<32>(t_row + c, v);
+      scale(v, c, col, col < p.N_out);
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const int tok = row0 + c + j;
@@ -931,11 +942,12 @@ struct TcPairCfg {
   static_assert(kSmem <= 232448, "shared memory per CTA");
 };
 
-template <int MODE>
+template <int MODE, bool F8 = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_pair_gemm_kernel(const __grid_constant__ TcParams p) {
   using Cfg = TcPairCfg<MODE>;
   constexpr int S = Cfg::kStages;
+  constexpr int kKStep = F8 ? 128 : BK;  // elements per 128-byte k-step
   constexpr int BN = Cfg::kBN;
   constexpr int kTileRows = 256;  // token rows per pair tile
   extern __shared__ uint8_t smem_raw[];
@@ -1046,20 +1058,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (rank == 0)
               mbar_arrive_expect_tx(full_bar(stage), 2u * (Cfg::kABytes + tn * 64));
             if constexpr (MODE == kSwiGLU)  // gate rows w0.. then the matching up rows
-              tma_load_4d_pair(a_dst, &p.tmWgtS, fb_leader, kb * BK,
+              tma_load_4d_pair(a_dst, &p.tmWgtS, fb_leader, kb * kKStep,
                                n0 + static_cast<int>(rank) * 64, 0, g);
             else
-              tma_load_3d_pair(a_dst, &p.tmWgt, fb_leader, kb * BK, b_row, g);
+              tma_load_3d_pair(a_dst, &p.tmWgt, fb_leader, kb * kKStep, b_row, g);
             // this CTA's tn/2 token rows in boxes of 64, 32 and 16 rows
             int rr = 0;
             for (; rr + 64 <= tn / 2; rr += 64)
-              tma_load_2d_pair(b_dst + 128u * rr, &p.tmActS64, fb_leader, kb * BK, t_row + rr);
+              tma_load_2d_pair(b_dst + 128u * rr, &p.tmActS64, fb_leader, kb * kKStep, t_row + rr);
             if (rr + 32 <= tn / 2) {
-              tma_load_2d_pair(b_dst + 128u * rr, &p.tmActS32, fb_leader, kb * BK, t_row + rr);
+              tma_load_2d_pair(b_dst + 128u * rr, &p.tmActS32, fb_leader, kb * kKStep, t_row + rr);
               rr += 32;
             }
             if (rr < tn / 2)
-              tma_load_2d_pair(b_dst + 128u * rr, &p.tmActS16, fb_leader, kb * BK, t_row + rr);
+              tma_load_2d_pair(b_dst + 128u * rr, &p.tmActS16, fb_leader, kb * kKStep, t_row + rr);
             ++issued;
             if (++stage == S) {
               stage = 0;
@@ -1068,8 +1080,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             continue;
           }
           if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * Cfg::kStageBytes);
-          tma_load_2d_pair(a_dst, &p.tmAct, fb_leader, kb * BK, a_row);
-          tma_load_3d_pair(b_dst, &p.tmWgt, fb_leader, kb * BK, b_row, g);
+          tma_load_2d_pair(a_dst, &p.tmAct, fb_leader, kb * kKStep, a_row);
+          tma_load_3d_pair(b_dst, &p.tmWgt, fb_leader, kb * kKStep, b_row, g);
           ++issued;
           if (++stage == S) {
             stage = 0;
@@ -1096,7 +1108,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA ----
     if (rank == 0 && elect_one_sync()) {
-      constexpr uint32_t idesc = idesc_bf16_f32(256, BN);
+      constexpr uint32_t idesc = F8 ? idesc_e4m3_f32(256, BN) : idesc_bf16_f32(256, BN);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
@@ -1107,7 +1119,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int g, row0, row_end, n_tile;
         decode_tile(p, s_off, s_mt, num_mt, kTileRows, idx, g, row0, row_end, n_tile);
         const int tn = pair_tail_n(row0, row_end);
-        const uint32_t idesc_t = tn > 0 ? idesc_bf16_f32(256, tn) : idesc;
+        const uint32_t idesc_t =
+            tn > 0 ? (F8 ? idesc_e4m3_f32(256, tn) : idesc_bf16_f32(256, tn)) : idesc;
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.err)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -1121,8 +1134,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t b_base = smem_u32(sB + stage * Cfg::kBBytes);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
-            tc_mma_bf16_pair(d_tmem, smem_desc_sw128(a_base + kk * 32),
-                             smem_desc_sw128(b_base + kk * 32), idesc_t, (kb | kk) != 0 ? 1u : 0u);
+            if constexpr (F8)
+              tc_mma_e4m3_pair(d_tmem, smem_desc_sw128(a_base + kk * 32),
+                               smem_desc_sw128(b_base + kk * 32), idesc_t, (kb | kk) != 0 ? 1u : 0u);
+            else
+              tc_mma_bf16_pair(d_tmem, smem_desc_sw128(a_base + kk * 32),
+                               smem_desc_sw128(b_base + kk * 32), idesc_t, (kb | kk) != 0 ? 1u : 0u);
           tc_commit_pair(empty_bar(stage), 0x3);
           if (++stage == S) {
             stage = 0;
@@ -1158,10 +1175,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int tn = pair_tail_n(row0, row_end);
       if (tn > 0) {
         epilogue_pair_tail<MODE>(p, t_row, sStg, quad, lane, static_cast<int>(rank), tn, row0,
-                                 row_end, n_tile * Cfg::kColsOut);
+                                 row_end, n_tile * Cfg::kColsOut, g);
       } else {
         const int tile_row0 = row0 + static_cast<int>(rank) * 128 + quad * 32;
-        epilogue_rows<BN, MODE>(p, t_row, stg, lane, tile_row0, row_end, n_tile * Cfg::kColsOut);
+        epilogue_rows<BN, MODE>(p, t_row, stg, lane, tile_row0, row_end, n_tile * Cfg::kColsOut,
+                                g);
       }
       tc_fence_before();
       __syncwarp();
@@ -1247,14 +1265,15 @@ bool make_map_3d_u8(CUtensorMap* m, const void* base, uint64_t G, uint64_t rows,
 // 4D bf16 map of [G][2][half][cols] (two stacked blocks of `half` rows per group), box =
 // 1 x 2 x 64 rows x 64 columns: rows r..r+63 of both blocks in one load.
 bool make_map_4d_halves(CUtensorMap* m, const void* base, uint64_t G, uint64_t half,
-                        uint64_t cols) {
+                        uint64_t cols, bool u8 = false) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
+  const uint64_t eb = u8 ? 1 : 2;  // bytes per element; the box is 128 bytes wide either way
   cuuint64_t dims[4] = {cols, half, 2, G};
-  cuuint64_t strides[3] = {cols * 2, half * cols * 2, 2 * half * cols * 2};
-  cuuint32_t box[4] = {static_cast<cuuint32_t>(BK), 64, 2, 1};
+  cuuint64_t strides[3] = {cols * eb, half * cols * eb, 2 * half * cols * eb};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / eb), 64, 2, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+  return fn(m, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -1321,10 +1340,11 @@ cudaError_t launch_one(const GroupedGemm& g, unsigned* err, int num_sms, cudaStr
 }
 
 
-template <int MODE>
-cudaError_t launch_pair(const GroupedGemm& g, unsigned* err, int num_sms, cudaStream_t s) {
+template <int MODE, bool F8 = false>
+cudaError_t launch_pair(const GroupedGemm& g, unsigned* err, int num_sms, cudaStream_t s,
+                        const float* a_scale = nullptr, const float* b_scale = nullptr) {
   using Cfg = TcPairCfg<MODE>;
-  auto kernel = tc_pair_gemm_kernel<MODE>;
+  auto kernel = tc_pair_gemm_kernel<MODE, F8>;
   static int attr_set_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1336,26 +1356,28 @@ cudaError_t launch_pair(const GroupedGemm& g, unsigned* err, int num_sms, cudaSt
   }
   TcParams p;
   memset(&p, 0, sizeof(p));
-  if (!make_map_2d(&p.tmAct, g.A, static_cast<uint64_t>(g.rows_alloc), static_cast<uint64_t>(g.Kd),
-                   128))
+  const uint64_t rows = static_cast<uint64_t>(g.rows_alloc), kd = static_cast<uint64_t>(g.Kd);
+  auto act = [&](CUtensorMap* m, uint32_t box) {
+    return F8 ? make_map_2d_u8(m, g.A, rows, kd, box) : make_map_2d(m, g.A, rows, kd, box);
+  };
+  if (!act(&p.tmAct, 128) ||
+      !(F8 ? make_map_3d_u8(&p.tmWgt, g.B, static_cast<uint64_t>(g.G),
+                            static_cast<uint64_t>(g.Nb), kd, 128)
+           : make_map_3d(&p.tmWgt, g.B, static_cast<uint64_t>(g.G), static_cast<uint64_t>(g.Nb),
+                         kd, 128)))
     return cudaErrorInvalidValue;
-  if (!make_map_3d(&p.tmWgt, g.B, static_cast<uint64_t>(g.G), static_cast<uint64_t>(g.Nb),
-                   static_cast<uint64_t>(g.Kd), 128))
-    return cudaErrorInvalidValue;
-  if (!make_map_2d(&p.tmActS16, g.A, static_cast<uint64_t>(g.rows_alloc),
-                   static_cast<uint64_t>(g.Kd), 16) ||
-      !make_map_2d(&p.tmActS32, g.A, static_cast<uint64_t>(g.rows_alloc),
-                   static_cast<uint64_t>(g.Kd), 32) ||
-      !make_map_2d(&p.tmActS64, g.A, static_cast<uint64_t>(g.rows_alloc),
-                   static_cast<uint64_t>(g.Kd), 64))
+  if (!act(&p.tmActS16, 16) || !act(&p.tmActS32, 32) || !act(&p.tmActS64, 64))
     return cudaErrorInvalidValue;
   if (MODE == kSwiGLU) {
     // [G][2][I][Kd]: the gate block then the up block of each expert
     if (g.up_offset * 2 != g.Nb || g.up_offset % 64 != 0 ||
         !make_map_4d_halves(&p.tmWgtS, g.B, static_cast<uint64_t>(g.G),
-                            static_cast<uint64_t>(g.up_offset), static_cast<uint64_t>(g.Kd)))
+                            static_cast<uint64_t>(g.up_offset), kd, F8))
       return cudaErrorInvalidValue;
   }
+  p.a_scale = a_scale;
+  p.b_scale = b_scale;
+  p.b_rows = g.Nb;
   p.C = g.C;
   p.col_bias = g.col_bias;
   p.offsets = g.offsets;
@@ -1364,7 +1386,7 @@ cudaError_t launch_pair(const GroupedGemm& g, unsigned* err, int num_sms, cudaSt
   p.num_groups = g.G;
   p.err = err;
   p.rows_alloc = g.rows_alloc;
-  p.num_kb = g.Kd / BK;
+  p.num_kb = F8 ? g.Kd / 128 : g.Kd / BK;  // 128-byte k-steps either way
   p.N_out = g.N_out;
   p.n_tiles = (g.N_out + Cfg::kColsOut - 1) / Cfg::kColsOut;
   p.up_offset = g.up_offset;
@@ -1395,6 +1417,8 @@ cudaError_t launch_gate_up_fp8(const GroupedGemm& g, const float* a_scale, const
   if (g.mode != kSwiGLU || g.G > kMaxGroups || g.Kd % 128 != 0 || a_scale == nullptr ||
       b_scale == nullptr || g.gather_rows != nullptr)
     return cudaErrorInvalidValue;
+  if (g.pair && g.swap_tokens == 0)
+    return launch_pair<kSwiGLU, true>(g, err, num_sms, s, a_scale, b_scale);
   if (g.swap_tokens > 0) {
     const int bt = tc_swap_tokens(g.swap_tokens);
     if (bt == 16) return launch_one<16, kSwiGLU, true, false, true>(g, err, num_sms, s, a_scale, b_scale);
@@ -1409,6 +1433,10 @@ cudaError_t launch_down_fp8(const GroupedGemm& g, const float* a_scale, const fl
   if ((g.mode != kPlain && g.mode != kScatter) || g.G > kMaxGroups || g.Kd % 128 != 0 ||
       a_scale == nullptr || b_scale == nullptr || g.gather_rows != nullptr)
     return cudaErrorInvalidValue;
+  if (g.pair && g.swap_tokens == 0) {
+    if (g.mode == kScatter) return launch_pair<kScatter, true>(g, err, num_sms, s, a_scale, b_scale);
+    if (g.N_out > 128) return launch_pair<kPlain, true>(g, err, num_sms, s, a_scale, b_scale);
+  }
   if (g.swap_tokens > 0) {
     const int bt = tc_swap_tokens(g.swap_tokens);
     if (g.mode == kScatter) {

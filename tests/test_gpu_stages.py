@@ -470,6 +470,62 @@ def test_down_fp8_equals_oracle(moe, T, H_, E, K, I, skew):
                      what="down_fp8")
 
 
+@pytest.mark.parametrize("H_,I", [(256, 128), (512, 256)])
+def test_pair_tiles_fp8(moe, H_, I):
+    """The FP8 gate/up and down projection on CTA pairs (groups of >= 384 / 768 rows on
+    average), with every kind of last tile (PAIR_GROUPS), against the oracle."""
+    sizes = np.array(PAIR_GROUPS)
+    E, K = len(sizes), 2
+    M = int(sizes.sum())
+    T = (M + 255) // K
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    shape = synth.MoEShape("pair8", T=T, H=H_, E=E, K=K, I=I, seed=14)
+    inp = synth.make_inputs(shape, device="cuda")
+    gen = torch.Generator().manual_seed(15)
+    x_perm = torch.zeros((T * K, H_), dtype=torch.bfloat16, device="cuda")
+    x_perm[:M] = torch.randn(M, H_, generator=gen).to(torch.bfloat16).cuda()
+    c = _cfg(moe, T, H_, E, K, I=I, dtype="bf16")
+    off = torch.from_numpy(offsets).cuda()
+    ws = torch.empty(moe.workspace_size(c), dtype=torch.uint8, device="cuda")
+    xq = torch.empty(T * K, H_, dtype=torch.uint8, device="cuda")
+    xs = torch.empty(T * K, dtype=torch.float32, device="cuda")
+    moe.quantize_fp8(x_perm, xq, xs)
+    xq[M:] = 0x7f  # NaN codes after the groups: a leak into a stored row would show
+    wgq = torch.empty(E, 2 * I, H_, dtype=torch.uint8, device="cuda")
+    wgs = torch.empty(E, 2 * I, dtype=torch.float32, device="cuda")
+    moe.quantize_fp8(inp["w_gate_up"].reshape(E * 2 * I, H_), wgq, wgs)
+    h = torch.full((T * K, I), -5.0, dtype=torch.bfloat16, device="cuda")
+    moe.expert_gate_up_fp8(c, xq, xs, off, wgq, wgs, h, ws)
+    hq = torch.empty(T * K, I, dtype=torch.uint8, device="cuda")
+    hs = torch.empty(T * K, dtype=torch.float32, device="cuda")
+    moe.quantize_fp8(h, hq, hs)
+    hq[M:] = 0x7f
+    wdq = torch.empty(E, H_, I, dtype=torch.uint8, device="cuda")
+    wds = torch.empty(E, H_, dtype=torch.float32, device="cuda")
+    moe.quantize_fp8(inp["w_down"].reshape(E * H_, I), wdq, wds)
+    out = torch.full((T * K, H_), -5.0, dtype=torch.float32, device="cuda")
+    moe.expert_down_fp8(c, hq, hs, off, wdq, wds, out, ws)
+    torch.cuda.synchronize()
+    moe.sync_check()
+    assert (h[M:] == -5.0).all() and (out[M:] == -5.0).all()
+    xc, xsc = oracle.quantize_rows_fp8(x_perm[:M].float().cpu().numpy())
+    wgc, wgsr = oracle.quantize_rows_fp8(inp["w_gate_up"].reshape(E * 2 * I, H_).float().cpu().numpy())
+    wdc, wdsr = oracle.quantize_rows_fp8(inp["w_down"].reshape(E * H_, I).float().cpu().numpy())
+    wgc, wgsr = wgc.reshape(E, 2 * I, H_), wgsr.reshape(E, 2 * I)
+    wdc, wdsr = wdc.reshape(E, H_, I), wdsr.reshape(E, H_)
+    h_gpu = H.f64(h[:M])
+    hc, hsc = oracle.quantize_rows_fp8(h[:M].float().cpu().numpy())  # the GPU's h, as the GPU
+    o_gpu = out[:M].double().cpu().numpy()
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 == r0:
+            continue
+        h_ref = oracle.expert_gate_up_fp8(xc[r0:r1], xsc[r0:r1], wgc[e], wgsr[e])
+        assert (np.abs(h_gpu[r0:r1] - h_ref) <= 2.0 ** -8 * np.abs(h_ref) + 1e-4).all()
+        o_ref = oracle.expert_down_fp8(hc[r0:r1], hsc[r0:r1], wdc[e], wdsr[e])
+        H.assert_close_y(o_gpu[r0:r1], o_ref, max_abs=1e-4, rel_l2=1e-5, what="down_fp8")
+
+
 @pytest.mark.parametrize("T,H_,E,K,I,dtype,skew", [c for c in FFN_CASES if c[5] == "bf16"])
 def test_gate_up_row_gather_equals_permuted_copy(moe, T, H_, E, K, I, dtype, skew):
     """The gate/up GEMM that gathers its rows from x by perm computes, row for row, the
