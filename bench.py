@@ -366,10 +366,19 @@ def run_ours(args, rank, world, local):
             wdq = torch.empty(E, H_, shape.I, dtype=torch.uint8, device=dev)
             wds = torch.empty(E, H_, dtype=torch.float32, device=dev)
             moe.quantize_fp8(inp["w_down"].reshape(E * H_, shape.I), wdq, wds, stream=stream)
-            stages["layer_fp8"] = timed(lambda: moe.layer_forward_fp8(
-                cfg8, inp["x"], inp["w_router"], inp["router_bias"], wq, wsc, wdq, wds,
-                inp.get("w_shared_gate_up"), inp.get("w_shared_down"), y, None, ws8,
-                stream=stream), nst)
+            def fp8_layer(st=stream):
+                moe.layer_forward_fp8(cfg8, inp["x"], inp["w_router"], inp["router_bias"], wq,
+                                      wsc, wdq, wds, inp.get("w_shared_gate_up"),
+                                      inp.get("w_shared_down"), y, None, ws8, stream=st)
+            fp8_step = fp8_layer
+            if T <= 128:  # like the bf16 layer: decode-sized layers replay a CUDA graph
+                fp8_layer()
+                torch.cuda.synchronize(dev)
+                graph8 = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph8):
+                    fp8_layer(torch.cuda.current_stream(dev))
+                fp8_step = graph8.replay
+            stages["layer_fp8"] = timed(fp8_step, nst)
     stages["down"] = timed(lambda: moe.expert_down(cfg, h, offsets, inp["w_down"], out_perm, ws,
                                                    stream=stream), nst)
     shared_out = None
