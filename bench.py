@@ -359,9 +359,12 @@ def run_ours(args, rank, world, local):
                                                   stream=stream), max(args.steps, 5))
         stages["gate_up_fp8"] = fp8
         if H_ % 128 == 0 and shape.I % 128 == 0:
-            # the whole layer with FP8 experts (moe_layer_forward_fp8), gather combine
+            # the whole layer with FP8 experts (moe_layer_forward_fp8): the fused combine as
+            # above for prefill; decode-sized layers gather (its fp32 sum would cost a zeroing
+            # and a rounding launch)
             cfg8 = moe.MoEConfig.make(T, H_, E, K, shape.I, shape.I_shared, shape.theta, dt,
-                                      moe.FLAG_FP8 | (moe.FLAG_CAPACITY if args.capacity else 0))
+                                      moe.FLAG_FP8 | (moe.FLAG_CAPACITY if args.capacity else 0) |
+                                      (moe.FLAG_FUSED_COMBINE if fused and T > 128 else 0))
             ws8 = torch.empty(moe.workspace_size(cfg8), dtype=torch.uint8, device=dev)
             wdq = torch.empty(E, H_, shape.I, dtype=torch.uint8, device=dev)
             wds = torch.empty(E, H_, dtype=torch.float32, device=dev)

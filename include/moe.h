@@ -220,8 +220,9 @@ moe_status_t moe_expert_gate_up_gather(const moe_config_t* cfg, const void* x,
  *   w_gate_up_codes [E,2I,H] uint8 and w_gate_up_scales [E,2I] float, w_down_codes [E,H,I]
  *   uint8 and w_down_scales [E,H] float, from moe_quantize_fp8 of the bf16 weights (rows =
  *   output channels); the other arguments as moe_layer_forward.
- * cfg->flags must include MOE_FLAG_FP8 (the workspace size depends on it) and must not
- * include MOE_FLAG_FUSED_COMBINE; bf16 layers with H % 128 == 0 and I % 128 == 0 (else
+ * cfg->flags must include MOE_FLAG_FP8 (the workspace size depends on it); with
+ * MOE_FLAG_FUSED_COMBINE the combine is done in the FP8 down projection as in
+ * moe_layer_forward.  bf16 layers with H % 128 == 0 and I % 128 == 0 (else
  * MOE_ERR_UNSUPPORTED). */
 moe_status_t moe_layer_forward_fp8(const moe_config_t* cfg, const void* x, const void* w_router,
                                    const float* router_bias, const uint8_t* w_gate_up_codes,

@@ -661,8 +661,7 @@ moe_status_t moe_layer_forward_fp8(const moe_config_t* cfg, const void* x, const
                                    const void* w_shared_down, void* y, float* y_f32, void* ws,
                                    size_t ws_bytes, moe_stream_t stream) {
   MOE_TRY(check_config(cfg));
-  if ((cfg->flags & MOE_FLAG_FP8) == 0u || (cfg->flags & MOE_FLAG_FUSED_COMBINE) != 0u)
-    return MOE_ERR_INVALID_ARG;
+  if ((cfg->flags & MOE_FLAG_FP8) == 0u) return MOE_ERR_INVALID_ARG;
   if (cfg->T == 0) return MOE_OK;
   if (cfg->dtype != MOE_BF16 || cfg->H % 128 != 0 || cfg->I % 128 != 0) return MOE_ERR_UNSUPPORTED;
   if (x == nullptr || w_router == nullptr || w_gate_up_codes == nullptr ||
@@ -706,9 +705,11 @@ moe_status_t moe_layer_forward_fp8(const moe_config_t* cfg, const void* x, const
   // 2. x's rows to E4M3 codes, then the dispatch moves the one-byte rows (as rows of H/2
   //    bf16 units) and the scales follow the permutation
   MOE_CUDA(launch_quantize_fp8(x, T, H, x_codes, x_scales, s));
+  const bool fused = (cfg->flags & MOE_FLAG_FUSED_COMBINE) != 0u;
+  float* row_w = fused ? at<float>(ws, p.row_w) : nullptr;
   MOE_CUDA(launch_permute(MOE_BF16, x_codes, ids, T, H / 2, E, K, counts, offsets, perm, inv,
                           xq_perm, at<int32_t>(ws, p.perm_ws), nullptr, nullptr, kSimtBM, w,
-                          nullptr, s));
+                          row_w, s));
   MOE_CUDA(launch_gather_scales(x_scales, perm, offsets + E, xs_perm, T * K, s));
   // 3. FP8 gate/up -> bf16 h -> E4M3 h -> FP8 down
   GroupedGemm g{};
@@ -741,6 +742,28 @@ moe_status_t moe_layer_forward_fp8(const moe_config_t* cfg, const void* x, const
   gd.C = out_perm;
   gd.offsets = offsets;
   gd.swap_tokens = g.swap_tokens;
+  if (fused) {
+    // the combine in the down projection: the shared expert writes the fp32 sum (or it is
+    // zeroed), every routed row adds its gated output into its token's row, then one
+    // rounding pass
+    float* y32 = y_f32 != nullptr ? y_f32 : at<float>(ws, p.y32);
+    if (shared) {
+      Groups one{};
+      one.G = 1;
+      void* hs = at<void>(ws, p.shared_h);
+      MOE_TRY(run_gate_up(cfg, d, x, T, w_shared_gate_up, cfg->I_shared, hs, one, s));
+      MOE_TRY(run_down(cfg, d, hs, T, w_shared_down, cfg->I_shared, y32, one, s));
+    } else {
+      MOE_CUDA(cudaMemsetAsync(y32, 0, static_cast<size_t>(T) * H * sizeof(float), s));
+    }
+    gd.mode = kScatter;
+    gd.C = y32;
+    gd.row_token = perm;
+    gd.row_w = row_w;
+    gd.pair = use_pairs(gd) ? 1 : 0;
+    MOE_CUDA(launch_down_fp8(gd, h_scales, w_down_scales, d->err, d->num_sms, s));
+    return cuda_status(launch_finalize(cfg->dtype, y32, y, static_cast<long long>(T) * H, s));
+  }
   gd.pair = use_pairs(gd) ? 1 : 0;
   MOE_CUDA(launch_down_fp8(gd, h_scales, w_down_scales, d->err, d->num_sms, s));
   // 4. shared expert (bf16), 5. combine

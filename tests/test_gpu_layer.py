@@ -269,14 +269,16 @@ def test_layer_with_capacity_routing(moe, shape):
                    seed=32),
     synth.MoEShape("fp8_decode", T=8, H=512, E=32, K=4, I=128, bias="zipf", seed=33),
 ], ids=lambda s: s.name)
-def test_layer_fp8_equals_oracle(moe, shape):
+@pytest.mark.parametrize("fused", [False, True], ids=["gather_combine", "fused_combine"])
+def test_layer_fp8_equals_oracle(moe, shape, fused):
     """moe_layer_forward_fp8: E4M3 experts (weights per output channel, x and h per row)
     against the oracle's FP8 expert chain.  The oracle routes from the layer's own fp32
     logits; h is the oracle's (fp64, rounded once to bf16), so a rare one-ulp difference of
     h can move one E4M3 code: the output is compared within the layer tolerance."""
     T, H_, E, K, I = shape.T, shape.H, shape.E, shape.K, shape.I
     inp = synth.make_inputs(shape, device="cuda")
-    cfg = moe.MoEConfig.make(T, H_, E, K, I, shape.I_shared, shape.theta, moe.BF16, moe.FLAG_FP8)
+    cfg = moe.MoEConfig.make(T, H_, E, K, I, shape.I_shared, shape.theta, moe.BF16,
+                             moe.FLAG_FP8 | (moe.FLAG_FUSED_COMBINE if fused else 0))
     ws = torch.empty(moe.workspace_size(cfg), dtype=torch.uint8, device="cuda")
     wgq = torch.empty(E, 2 * I, H_, dtype=torch.uint8, device="cuda")
     wgs = torch.empty(E, 2 * I, dtype=torch.float32, device="cuda")
