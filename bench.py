@@ -81,6 +81,20 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value, world, dev):
+    """The largest of every rank's value (the slowest replica sets the job's time)."""
+    if world <= 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_seed(shape, rank):
+    """Each replica draws its own token batch (and weights) from seed + rank."""
+    return shape.seed + rank
+
+
 def load_peaks():
     if os.path.exists(PEAKS_FILE):
         with open(PEAKS_FILE) as f:
@@ -241,7 +255,7 @@ def run_ours(args, rank, world, local):
     moe.load()
     shape = synth.WORKLOADS[args.config]
     T = args.tokens if args.tokens is not None else shape.T
-    inp = synth.make_inputs(shape.with_(seed=shape.seed + rank), device=dev, T=T)
+    inp = synth.make_inputs(shape.with_(seed=replica_seed(shape, rank)), device=dev, T=T)
     dt = moe.BF16 if shape.dtype == "bf16" else moe.F32
     # default: the fp32 scatter-add combine fused into the down GEMM when each token has
     # many (K >= 8) contributions to add, the deterministic gather combine otherwise
@@ -308,11 +322,7 @@ def run_ours(args, rank, world, local):
     if world > 1:
         torch.distributed.barrier()
     moe.sync_check(stream)
-    ms = statistics.mean(times)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(statistics.mean(times), world, dev)
 
     # routing statistics of this batch (counts come from the layer's own workspace)
     views = moe.workspace_views(cfg, ws)
@@ -472,11 +482,7 @@ def run_ours(args, rank, world, local):
         for _ in range(2):
             e2e_run()
     e2e_times = timed(e2e_run, args.steps)
-    e2e_ms = statistics.mean(e2e_times)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(statistics.mean(e2e_times), world, dev)
     moe.sync_check(stream)
 
     res = {
