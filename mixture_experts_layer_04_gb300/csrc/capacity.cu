@@ -8,15 +8,27 @@
 // the available experts (softmax over them, then the gate drop; missing slots -1).
 //
 // The rule is sequential in t, but each token depends on earlier tokens only through, per
-// expert, the index of the token that takes its last free place.  One CTA sweeps the batch in
-// blocks of 256 tokens with the exact counts of the earlier blocks.  Inside a block it
+// expert, the index of the token that takes its last free place.  The batch is swept in blocks
+// of 256 tokens with the exact counts of the earlier blocks.  Inside a block the routing
 // iterates to a fixed point: fb[e] = the block token holding e's (cap - count[e])-th kept
 // assignment under the current choices, and every token whose availability changed chooses
 // again among the experts with count[e] < cap and fb[e] >= its index.  Token 0 of the block is
 // final after the first pass and each pass fixes at least the next token, so the fixed point
 // (the sequential routing) is reached within 257 passes; in practice in a few.  Tokens that no
-// capacity touches keep the router's choice.  No global scratch, no atomics on global memory:
-// the result is deterministic.
+// capacity touches keep the router's choice.
+//
+// One thread-block cluster runs the sweep (16 CTAs where the device allows it, else fewer).
+// CTA c owns block tokens [c * 256 / nc, (c + 1) * 256 / nc), one token per warp at nc = 16,
+// with their logit rows staged in shared memory.  Each pass, every CTA re-chooses its dirty
+// tokens and sets the bits of its tokens in its slice of the per-expert block masks (16 bits
+// per expert at nc = 16, u16 [E] contiguous), then stores the slice, in 16-byte stores, into
+// every CTA of the cluster; one cluster barrier later every CTA holds the whole block's masks
+// and derives the same fb[], the same change list and the same decision to stop.  The block
+// masks are double-buffered by pass parity, so one cluster barrier per pass suffices: a CTA
+// can only overwrite a buffer after every CTA has passed the next barrier, i.e. has finished
+// reading it.  No global scratch, no atomics on global memory: the result is deterministic.
+#include <cstring>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "topk.cuh"
@@ -24,11 +36,65 @@
 namespace moe {
 namespace {
 
-constexpr int kCapThreads = 1024;
+constexpr int kCapThreads = 512;
 constexpr int kCapWarps = kCapThreads / 32;
 constexpr int kCapBlock = 256;              // tokens per block of the sweep
 constexpr int kCapWords = kCapBlock / 32;   // token bits per expert
 constexpr int kNone = kCapBlock;            // fb value: the expert does not fill in the block
+constexpr int kCapMaxE = 1024;
+constexpr int kCapMaxK = 16;
+constexpr int kCapStageMax = 96 * 1024;     // largest logit stage kept in shared memory
+
+// Shared-memory layout of one CTA (byte offsets, 16-byte aligned); tpc = tokens per CTA.
+struct CapLayout {
+  int lg, cnt, fb, mask, own, chg, bid, bw, dirty, total;
+  int src_bytes;  // one CTA's slice of every expert's block mask: u16 [E][tpc / 16], padded
+};
+
+__host__ __device__ inline int cap_align16(int b) { return (b + 15) / 16 * 16; }
+
+__host__ __device__ inline bool cap_stages_logits(int E, int tpc) {
+  return tpc * E * 4 <= kCapStageMax;
+}
+
+__host__ __device__ inline CapLayout cap_layout(int E, int K, int tpc) {
+  CapLayout L;
+  L.src_bytes = cap_align16(E * (tpc / 16) * 2);
+  int o = 0;
+  L.lg = o;
+  o += cap_stages_logits(E, tpc) ? cap_align16(tpc * E * 4) : 0;  // float [tpc][E]
+  L.cnt = o;
+  o += cap_align16(E * 4);                                         // int [E]
+  L.fb = o;
+  o += cap_align16(E * 4);                                         // int [E]
+  L.mask = o;
+  o += 2 * (kCapBlock / tpc) * L.src_bytes;                        // [2][nc] slices
+  L.own = o;
+  o += L.src_bytes;                                                // this CTA's slice
+  L.chg = o;
+  o += cap_align16(3 * E * 4);                                     // int [E][3]
+  L.bid = o;
+  o += cap_align16(tpc * K * 4);                                   // int [tpc][K]
+  L.bw = o;
+  o += cap_align16(tpc * K * 4);                                   // float [tpc][K]
+  L.dirty = o;
+  o += cap_align16(tpc * 4);                                       // int [tpc]
+  L.total = o;
+  return L;
+}
+
+__device__ __forceinline__ uint32_t cap_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+
+// 16-byte store into the shared memory of a CTA of the cluster (a shared::cluster address).
+__device__ __forceinline__ void st_dsmem_v4(uint32_t cluster_addr, uint4 v) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
 
 // Position of the n-th (0-based) set bit of v (n < popc(v)).
 __device__ __forceinline__ int nth_set_bit(uint32_t v, int n) {
@@ -39,6 +105,18 @@ __device__ __forceinline__ int nth_set_bit(uint32_t v, int n) {
 // Inverse of float_key (the key of -0 gives +0, which the softmax cannot tell apart).
 __device__ __forceinline__ float key_float(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Word wd (block tokens [32 wd, 32 wd + 32)) of expert e's block mask, from the slices of one
+// pass: slice r holds u16 [E][upc], unit j of expert e covering block tokens
+// [16 (r upc + j), +16); upc = 1 << ulog.
+__device__ __forceinline__ uint32_t block_word(const unsigned char* mk, int src_bytes, int ulog,
+                                               int e, int wd) {
+  const int u0 = 2 * wd, u1 = u0 + 1, um = (1 << ulog) - 1;
+  const uint16_t* s0 = reinterpret_cast<const uint16_t*>(mk + (u0 >> ulog) * src_bytes);
+  const uint16_t* s1 = reinterpret_cast<const uint16_t*>(mk + (u1 >> ulog) * src_bytes);
+  return static_cast<uint32_t>(s0[(e << ulog) + (u0 & um)]) |
+         (static_cast<uint32_t>(s1[(e << ulog) + (u1 & um)]) << 16);
 }
 
 template <int NJ>  // candidates per lane: experts lane + 32 j, j < NJ (E <= 32 NJ)
@@ -116,33 +194,55 @@ __global__ void __launch_bounds__(kCapThreads, 1)
     capacity_route_kernel(const float* __restrict__ logits, int32_t* __restrict__ ids,
                           float* __restrict__ w, int T, int E, int K, float theta, int cap,
                           unsigned* err) {
-  extern __shared__ int smem_i[];
-  int* cnt = smem_i;                                        // [E] kept before the block
-  int* fb = cnt + E;                                        // [E]
-  uint32_t* mask = reinterpret_cast<uint32_t*>(fb + E);     // [E][kCapWords]
-  int32_t* bid = reinterpret_cast<int32_t*>(mask + E * kCapWords);  // [kCapBlock * K]
-  float* bw = reinterpret_cast<float*>(bid + kCapBlock * K);        // [kCapBlock * K]
-  int* chg = reinterpret_cast<int*>(bw + kCapBlock * K);           // [3 * E]: e, old, new fb
+  extern __shared__ __align__(16) unsigned char smem_c[];
   __shared__ int s_nchg;
-  __shared__ int s_dirty[kCapBlock];
+  const int c = static_cast<int>(cluster_ctarank());
+  const int nc = static_cast<int>(cap_nctarank());
+  const int tpc = kCapBlock / nc;  // block tokens owned by this CTA (a multiple of 16)
+  const int upc = tpc / 16;        // 16-token units of this CTA per expert
+  const int ulog = 31 - __clz(upc);
+  const bool stage = cap_stages_logits(E, tpc);
+  const CapLayout lay = cap_layout(E, K, tpc);
+  float* lg = reinterpret_cast<float*>(smem_c + lay.lg);
+  int* cnt = reinterpret_cast<int*>(smem_c + lay.cnt);          // kept before the block
+  int* fb = reinterpret_cast<int*>(smem_c + lay.fb);
+  unsigned char* mask = smem_c + lay.mask;  // [2][nc] slices, written by every CTA
+  uint32_t* own = reinterpret_cast<uint32_t*>(smem_c + lay.own);  // this CTA's slice
+  const int sb = lay.src_bytes;
+  int* chg = reinterpret_cast<int*>(smem_c + lay.chg);          // e, old fb, new fb
+  int32_t* bid = reinterpret_cast<int32_t*>(smem_c + lay.bid);
+  float* bw = reinterpret_cast<float*>(smem_c + lay.bw);
+  int* s_dirty = reinterpret_cast<int*>(smem_c + lay.dirty);
+  const uint32_t mask_sa = smem_u32(mask);
 
-  grid_dep_wait();  // the router's logits and choices
-  grid_dep_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int e = tid; e < E; e += kCapThreads) cnt[e] = 0;
+  for (int i = tid; i < sb / 4; i += kCapThreads) own[i] = 0u;
+  grid_dep_wait();  // the router's logits and choices
+  grid_dep_trigger();
+  cluster_sync_all();  // every CTA of the cluster is running before the first remote store
+  int parity = 0;
   for (int t0 = 0; t0 < T; t0 += kCapBlock) {
     const int nb = min(kCapBlock, T - t0);
-    for (int i = tid; i < nb * K; i += kCapThreads) {
-      bid[i] = ids[static_cast<size_t>(t0) * K + i];
-      bw[i] = w[static_cast<size_t>(t0) * K + i];
+    const int b0 = c * tpc;                    // this CTA's first token in the block
+    const int nt = max(0, min(tpc, nb - b0));  // this CTA's tokens in the block
+    const size_t g0 = static_cast<size_t>(t0) + b0;
+    for (int i = tid; i < nt * K; i += kCapThreads) {
+      bid[i] = ids[g0 * K + i];
+      bw[i] = w[g0 * K + i];
     }
+    if (stage)
+      for (int i = tid; i < nt * E; i += kCapThreads) lg[i] = logits[g0 * E + i];
     for (int e = tid; e < E; e += kCapThreads) fb[e] = kNone;
     __syncthreads();
     for (int pass = 0;; ++pass) {
+      parity ^= 1;
+      const unsigned char* mk = mask + parity * nc * sb;
       // 1. tokens whose available set may have changed choose again.  First pass: with a
       //    gate drop the router's dropped slots hide part of its choice, so every token
       //    chooses again; without one, only tokens that chose an expert already full.
-      for (int tl = warp; tl < nb; tl += kCapWarps) {
+      //    Then every token sets its bit in the masks of the experts it holds.
+      for (int tl = warp; tl < nt; tl += kCapWarps) {
         bool dirty;
         if (pass == 0) {
           const int e = lane < K ? bid[tl * K + lane] : -1;
@@ -150,35 +250,44 @@ __global__ void __launch_bounds__(kCapThreads, 1)
         } else {
           dirty = s_dirty[tl] != 0;
         }
-        if (dirty)
-          masked_topk(logits + static_cast<size_t>(t0 + tl) * E, E, K, theta, tl, cnt, fb, cap,
-                      bid + tl * K, bw + tl * K);
+        const float* Lt = stage ? lg + static_cast<size_t>(tl) * E : logits + (g0 + tl) * E;
+        if (dirty) masked_topk(Lt, E, K, theta, b0 + tl, cnt, fb, cap, bid + tl * K, bw + tl * K);
+        __syncwarp();
+        const int e = lane < K ? bid[tl * K + lane] : -1;
+        if (e >= 0) {
+          const int u = e * upc + (tl >> 4);  // 16-bit unit of the slice
+          atomicOr(&own[u >> 1], 1u << (16 * (u & 1) + (tl & 15)));
+        }
       }
-      __syncthreads();  // every warp has read the dirty flags and written its tokens' choices
-      for (int i = tid; i < E * kCapWords; i += kCapThreads) mask[i] = 0u;
       if (tid == 0) s_nchg = 0;
       __syncthreads();
-      // 2. which block tokens hold each expert
-      for (int i = tid; i < nb * K; i += kCapThreads) {
-        const int e = bid[i];
-        const int tl = i / K;
-        if (e >= 0) atomicOr(&mask[e * kCapWords + (tl >> 5)], 1u << (tl & 31));
+      // 2. this CTA's slice of every expert's block mask goes to every CTA of the cluster, in
+      //    16-byte stores
+      {
+        const int chunks = sb / 16;
+        const uint32_t dst = mask_sa + static_cast<uint32_t>((parity * nc + c) * sb);
+        for (int i = tid; i < nc * chunks; i += kCapThreads) {
+          const int r = i / chunks, ch = i - r * chunks;
+          const uint4 v = reinterpret_cast<const uint4*>(own)[ch];
+          st_dsmem_v4(mapa_shared(dst + 16u * ch, static_cast<uint32_t>(r)), v);
+        }
       }
-      __syncthreads();
-      // 3. fb[e]: the block token that takes e's last free place, if any
+      cluster_sync_all();  // every CTA's slices are in place (and all reads of `own` done)
+      for (int i = tid; i < sb / 4; i += kCapThreads) own[i] = 0u;
+      // 3. fb[e]: the block token that takes e's last free place, if any (the same in every CTA)
       for (int e = tid; e < E; e += kCapThreads) {
         const int need = cap - cnt[e];
         int f = kNone;
         if (need > 0) {
           int run = 0;
           for (int wd = 0; wd < kCapWords; ++wd) {
-            const uint32_t m = mask[e * kCapWords + wd];
-            const int c = __popc(m);
-            if (run + c >= need) {
+            const uint32_t m = block_word(mk, sb, ulog, e, wd);
+            const int pc = __popc(m);
+            if (run + pc >= need) {
               f = wd * 32 + nth_set_bit(m, need - run - 1);
               break;
             }
-            run += c;
+            run += pc;
           }
         }
         if (f != fb[e]) {
@@ -192,13 +301,14 @@ __global__ void __launch_bounds__(kCapThreads, 1)
       __syncthreads();
       const int nchg = s_nchg;
       if (nchg == 0) break;
-      // 4. which tokens must choose again: e's last free place moved from a to b.  Earlier
-      //    (b < a): tokens in (b, a] lose e, which matters to those holding it.  Later
-      //    (b > a): tokens in (a, b] gain e, which matters if its logit ties or beats the
-      //    token's weakest choice or the token has an empty slot (a dropped slot hides a
+      // 4. which of this CTA's tokens must choose again: e's last free place moved from a to
+      //    b.  Earlier (b < a): tokens in (b, a] lose e, which matters to those holding it.
+      //    Later (b > a): tokens in (a, b] gain e, which matters if its logit ties or beats
+      //    the token's weakest choice or the token has an empty slot (a dropped slot hides a
       //    choice, so it counts as empty).
-      for (int tl = tid; tl < nb; tl += kCapThreads) {
-        const float* Lt = logits + static_cast<size_t>(t0 + tl) * E;
+      for (int tl = tid; tl < nt; tl += kCapThreads) {
+        const float* Lt = stage ? lg + static_cast<size_t>(tl) * E : logits + (g0 + tl) * E;
+        const int tb = b0 + tl;
         float weakest = 0.f;
         bool has_empty = false;
         for (int k = 0; k < K; ++k) {
@@ -214,10 +324,10 @@ __global__ void __launch_bounds__(kCapThreads, 1)
         for (int j = 0; j < nchg && !d; ++j) {
           const int e = chg[3 * j], a = chg[3 * j + 1], b = chg[3 * j + 2];
           if (b < a) {
-            if (tl > b && tl <= a) {
+            if (tb > b && tb <= a) {
               for (int k = 0; k < K; ++k) d |= bid[tl * K + k] == e;
             }
-          } else if (tl > a && tl <= b) {
+          } else if (tb > a && tb <= b) {
             d = has_empty || Lt[e] >= weakest;
           }
         }
@@ -225,19 +335,20 @@ __global__ void __launch_bounds__(kCapThreads, 1)
       }
       __syncthreads();
       if (pass > nb + 1) {  // cannot happen: each pass fixes at least one more token
-        if (tid == 0) report_error(err, MOE_DEVERR_BOUNDS);
+        if (tid == 0 && c == 0) report_error(err, MOE_DEVERR_BOUNDS);
         break;
       }
     }
-    // 4. commit the block: its kept assignments count against the capacity
+    // 5. commit the block: its kept assignments count against the capacity
+    const unsigned char* mk = mask + parity * nc * sb;
     for (int e = tid; e < E; e += kCapThreads) {
-      int c = 0;
-      for (int wd = 0; wd < kCapWords; ++wd) c += __popc(mask[e * kCapWords + wd]);
-      cnt[e] += c;
+      int n = 0;
+      for (int wd = 0; wd < kCapWords; ++wd) n += __popc(block_word(mk, sb, ulog, e, wd));
+      cnt[e] += n;
     }
-    for (int i = tid; i < nb * K; i += kCapThreads) {
-      ids[static_cast<size_t>(t0) * K + i] = bid[i];
-      w[static_cast<size_t>(t0) * K + i] = bw[i];
+    for (int i = tid; i < nt * K; i += kCapThreads) {
+      ids[g0 * K + i] = bid[i];
+      w[g0 * K + i] = bw[i];
     }
     __syncthreads();
   }
@@ -253,21 +364,67 @@ int capacity_limit(int T, int K, int E) {
 cudaError_t launch_capacity_route(const float* logits, int32_t* ids, float* w, int T, int E, int K,
                                   float theta, int cap, unsigned* err, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  if (E < 1 || E > 1024 || K < 1 || K > 16) return cudaErrorInvalidValue;
-  const size_t smem = static_cast<size_t>(E) * (2 * 4 + kCapWords * 4 + 3 * 4) +
-                      static_cast<size_t>(kCapBlock) * K * 8;
+  if (E < 1 || E > kCapMaxE || K < 1 || K > kCapMaxK) return cudaErrorInvalidValue;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  static int attr_dev = -1;
-  if (attr_dev != dev) {
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  // the largest cluster (16, 8, 4, 2 or 1 CTAs) that the device can hold at the largest
+  // layout (E = 1024, K = 16), found once per device
+  static int cap_nc[64] = {0};
+  if (cap_nc[dev] == 0) {
+    int smem_max = 0;
+    for (int nc = 1; nc <= 16; nc *= 2) {
+      const int b = cap_layout(kCapMaxE, kCapMaxK, kCapBlock / nc).total;
+      smem_max = b > smem_max ? b : smem_max;
+    }
     e = cudaFuncSetAttribute(capacity_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kCapBlock * 16 * 8 + 1024 * (8 + kCapWords * 4 + 12)));
+                             smem_max);
     if (e != cudaSuccess) return e;
-    attr_dev = dev;
+    e = cudaFuncSetAttribute(capacity_route_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                             1);
+    if (e != cudaSuccess) return e;
+    int found = 1;
+    for (int nc : {16, 8, 4, 2}) {
+      cudaLaunchConfig_t lc;
+      std::memset(&lc, 0, sizeof(lc));
+      lc.gridDim = dim3(nc);
+      lc.blockDim = dim3(kCapThreads);
+      lc.dynamicSmemBytes = static_cast<size_t>(cap_layout(kCapMaxE, kCapMaxK, kCapBlock / nc).total);
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = nc;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      lc.attrs = at;
+      lc.numAttrs = 1;
+      int nclusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&nclusters, capacity_route_kernel, &lc) == cudaSuccess &&
+          nclusters >= 1) {
+        found = nc;
+        break;
+      }
+      cudaGetLastError();  // clear a refused query before trying the smaller cluster
+    }
+    cap_nc[dev] = found;
   }
-  return launch_pdl(capacity_route_kernel, dim3(1), dim3(kCapThreads), smem, s, logits, ids, w, T,
-                    E, K, theta, cap, err);
+  const int nc = cap_nc[dev];
+  cudaLaunchConfig_t lc;
+  std::memset(&lc, 0, sizeof(lc));
+  lc.gridDim = dim3(nc);
+  lc.blockDim = dim3(kCapThreads);
+  lc.dynamicSmemBytes = static_cast<size_t>(cap_layout(E, K, kCapBlock / nc).total);
+  lc.stream = s;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = nc;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = at;
+  lc.numAttrs = 2;
+  return cudaLaunchKernelEx(&lc, capacity_route_kernel, logits, ids, w, T, E, K, theta, cap, err);
 }
 
 }  // namespace moe

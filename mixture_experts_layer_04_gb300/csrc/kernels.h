@@ -64,7 +64,8 @@ cudaError_t launch_route_cluster(const void* x, const void* w_router, const floa
                                  cudaStream_t s);
 // Capacity-limited routing (capacity.cu): ceil(1.2 T K / E) kept assignments per expert, and
 // the in-place rewrite of the router's choices ids/w [T,K] (from logits [T,E]) into the
-// token-by-token capacity routing.  E <= 1024, K <= 16; one CTA.
+// token-by-token capacity routing.  E <= 1024, K <= 16; one thread-block cluster (16 CTAs
+// where the device holds it).
 int capacity_limit(int T, int K, int E);
 cudaError_t launch_capacity_route(const float* logits, int32_t* ids, float* w, int T, int E, int K,
                                   float theta, int cap, unsigned* err, cudaStream_t s);
