@@ -315,7 +315,7 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
 
 /* Intermediates of the last moe_layer_forward that used `ws` (views into ws; valid
  * until ws is reused).  Any output pointer may be NULL.  Useful to check every stage.
- * x_perm is not written by decode-sized bf16 layers (T <= 64, E <= 256, K <= 16), whose
+ * x_perm is not written by decode-sized bf16 layers (T <= 16, E <= 256, K <= 16), whose
  * gate/up GEMM gathers token rows from x through perm instead; out_perm is not written
  * with MOE_FLAG_FUSED_COMBINE. */
 moe_status_t moe_workspace_views(const moe_config_t* cfg, void* ws, float** logits,
