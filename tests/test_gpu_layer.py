@@ -133,6 +133,10 @@ def _sample_tokens(r, T, n, seed=0):
 FULL = [
     ("mixtral", None, 48), ("qwen_prefill", None, 48), ("qwen_decode", 1, 1),
     ("qwen_decode", 8, 8), ("qwen_decode", 32, 32), ("qwen_decode", 64, 64), ("deepseek", None, 24),
+    # decode-sized batches of the other two layer shapes: one-cluster routing and swapped
+    # GEMMs with H = 4096 and I = 14336 (Mixtral), and with H = 7168, 256 experts, the
+    # gate drop and the shared expert (DeepSeek)
+    ("mixtral", 4, 4), ("deepseek", 8, 8),
 ]
 
 
