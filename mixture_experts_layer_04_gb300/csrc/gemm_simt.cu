@@ -2,9 +2,9 @@
 //
 // The float32 layer keeps every operand in float32 (the tensor cores would round the
 // inputs to tf32), so its expert FFN runs as a classic shared-memory tiled SIMT GEMM:
-// 64x64 output tiles, k-steps of 16, 4x4 outputs per thread.  It walks the same ragged
-// m-tile table as the tensor-core engine (one tile never mixes two experts' rows) and
-// supports the same two epilogues: plain fp32 store (+ optional column bias) and the
+// 64x64 output tiles, k-steps of 16 double-buffered in shared memory, 4x4 outputs per
+// thread.  It walks the same ragged m-tile table as the tensor-core engine (one tile
+// never mixes two experts' rows) and supports the same two epilogues: plain fp32 store (+ optional column bias) and the
 // SwiGLU pair silu(gate) * up, whose gate and up columns come from the two halves of
 // the expert's stacked [W_g; W_u] weight.
 #include "common.cuh"
@@ -24,9 +24,11 @@ __global__ void __launch_bounds__(kThreads)
                              float* __restrict__ C, const float* __restrict__ col_bias,
                              const int4* __restrict__ table, const int32_t* __restrict__ num_mt,
                              int rows_alloc, int Kd, int Nb, int N_out, int up_offset) {
-  __shared__ float As[kBK][kBM + 4];
-  __shared__ float Bg[kBK][kBN + 4];
-  __shared__ float Bu[kSwi ? kBK : 1][kSwi ? kBN + 4 : 1];
+  // two shared-memory buffers: the global loads of k-step s+1 are in flight (in
+  // registers) while k-step s is computed from the other buffer
+  __shared__ float As[2][kBK][kBM + 4];
+  __shared__ float Bg[2][kBK][kBN + 4];
+  __shared__ float Bu[2][kSwi ? kBK : 1][kSwi ? kBN + 4 : 1];
 
   grid_dep_wait();
   grid_dep_trigger();
@@ -54,44 +56,49 @@ __global__ void __launch_bounds__(kThreads)
 
   const int lr = tid / 4;        // 0..63: row of the tile this thread loads
   const int lk = (tid % 4) * 4;  // 0,4,8,12: k offset inside the 16-wide step
+  const bool a_ok = row0 + lr < row_end, b_ok = n0 + lr < N_out;
+  const float* a_src = A + static_cast<size_t>(a_ok ? row0 + lr : 0) * Kd + lk;
+  const float* g_src = Bgrp + static_cast<size_t>(b_ok ? n0 + lr : 0) * Kd + lk;
+  const float* u_src = Bgrp + static_cast<size_t>(b_ok ? up_offset + n0 + lr : 0) * Kd + lk;
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 va, vg, vu = zero;
+  auto load = [&](int k0) {
+    va = a_ok ? *reinterpret_cast<const float4*>(a_src + k0) : zero;
+    vg = b_ok ? *reinterpret_cast<const float4*>(g_src + k0) : zero;
+    if constexpr (kSwi) vu = b_ok ? *reinterpret_cast<const float4*>(u_src + k0) : zero;
+  };
+  auto stash = [&](int buf) {
+    As[buf][lk + 0][lr] = va.x;
+    As[buf][lk + 1][lr] = va.y;
+    As[buf][lk + 2][lr] = va.z;
+    As[buf][lk + 3][lr] = va.w;
+    Bg[buf][lk + 0][lr] = vg.x;
+    Bg[buf][lk + 1][lr] = vg.y;
+    Bg[buf][lk + 2][lr] = vg.z;
+    Bg[buf][lk + 3][lr] = vg.w;
+    if constexpr (kSwi) {
+      Bu[buf][lk + 0][lr] = vu.x;
+      Bu[buf][lk + 1][lr] = vu.y;
+      Bu[buf][lk + 2][lr] = vu.z;
+      Bu[buf][lk + 3][lr] = vu.w;
+    }
+  };
+  load(0);
+  stash(0);
+  __syncthreads();
+  int buf = 0;
   for (int k0 = 0; k0 < Kd; k0 += kBK) {
-    {
-      const int r = row0 + lr;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (r < row_end) v = *reinterpret_cast<const float4*>(A + static_cast<size_t>(r) * Kd + k0 + lk);
-      As[lk + 0][lr] = v.x;
-      As[lk + 1][lr] = v.y;
-      As[lk + 2][lr] = v.z;
-      As[lk + 3][lr] = v.w;
-    }
-    {
-      const int n = n0 + lr;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (n < N_out) v = *reinterpret_cast<const float4*>(Bgrp + static_cast<size_t>(n) * Kd + k0 + lk);
-      Bg[lk + 0][lr] = v.x;
-      Bg[lk + 1][lr] = v.y;
-      Bg[lk + 2][lr] = v.z;
-      Bg[lk + 3][lr] = v.w;
-      if constexpr (kSwi) {
-        float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (n < N_out)
-          u = *reinterpret_cast<const float4*>(Bgrp + static_cast<size_t>(up_offset + n) * Kd + k0 + lk);
-        Bu[lk + 0][lr] = u.x;
-        Bu[lk + 1][lr] = u.y;
-        Bu[lk + 2][lr] = u.z;
-        Bu[lk + 3][lr] = u.w;
-      }
-    }
-    __syncthreads();
+    const bool more = k0 + kBK < Kd;
+    if (more) load(k0 + kBK);
 #pragma unroll
     for (int kk = 0; kk < kBK; ++kk) {
       float a[4], bg[4], bu[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+      for (int i = 0; i < 4; ++i) a[i] = As[buf][kk][ty * 4 + i];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        bg[j] = Bg[kk][tx * 4 + j];
-        if constexpr (kSwi) bu[j] = Bu[kk][tx * 4 + j];
+        bg[j] = Bg[buf][kk][tx * 4 + j];
+        if constexpr (kSwi) bu[j] = Bu[buf][kk][tx * 4 + j];
       }
 #pragma unroll
       for (int i = 0; i < 4; ++i)
@@ -101,7 +108,10 @@ __global__ void __launch_bounds__(kThreads)
           if constexpr (kSwi) accu[i][j] = fmaf(a[i], bu[j], accu[i][j]);
         }
     }
+    // the other buffer was last read before the previous barrier, so it can be refilled
+    if (more) stash(buf ^ 1);
     __syncthreads();
+    buf ^= 1;
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
