@@ -165,7 +165,7 @@ def gate_up_kernel(shape, T):
     threshold), else single CTAs with 128-row tiles; decode-sized batches (T <= 128) put
     the weights on the MMA's 128-row side."""
     if shape.dtype != "bf16":
-        return "grouped_gemm_simt_kernel<SwiGLU> (moe_expert_gate_up)"
+        return "tf32x3_gemm_kernel<SwiGLU> (moe_expert_gate_up)"
     if T <= 128:
         bt = 16 if T <= 16 else 32 if T <= 32 else 64
         return f"tc_grouped_gemm_kernel<{bt},SwiGLU,swap> (moe_expert_gate_up)"

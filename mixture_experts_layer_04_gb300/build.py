@@ -23,8 +23,9 @@ BUILD = os.path.join(PKG, "_build")
 LIB_NAME = "libmoe_gb300.so"
 LIB_PATH = os.path.join(BUILD, LIB_NAME)
 
-SOURCES = ["api.cu", "route.cu", "permute.cu", "combine.cu", "gemm_simt.cu", "gemm_tc.cu",
-           "permute_noalloc.cu", "route_cluster.cu", "capacity.cu", "quant.cu"]
+SOURCES = ["api.cu", "route.cu", "permute.cu", "combine.cu", "gemm_tc.cu",
+           "permute_noalloc.cu", "route_cluster.cu", "capacity.cu", "quant.cu",
+           "gemm_tf32.cu"]
 GENCODE = "-gencode=arch=compute_103a,code=sm_103a"
 NVCC_FLAGS = [
     GENCODE, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",

@@ -83,7 +83,7 @@ inline size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 Plan make_plan(const moe_config_t* c) {
   const size_t T = c->T, H = c->H, E = c->E, K = c->K, I = c->I, Is = c->I_shared;
   const size_t ab = act_bytes(c->dtype);
-  const int bm = c->dtype == MOE_BF16 ? kTcBM : kSimtBM;
+  const int bm = c->dtype == MOE_BF16 ? kTcBM : kF32TileRows;
   Plan p;
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -212,7 +212,7 @@ moe_status_t run_route(const moe_config_t* c, const DeviceInfo* d, const void* x
 }
 
 // Grouped-GEMM launch descriptions of the two expert GEMMs.  Groups come from `offsets`
-// (tensor-core engine) or from the m-tile table (SIMT engine); with neither, A is one
+// (bf16 engine) or from the m-tile table (float32 engine); with neither, A is one
 // dense group of rows_alloc rows (the shared expert).
 struct Groups {
   const int32_t* offsets;
@@ -256,7 +256,7 @@ moe_status_t launch_gemm(const moe_config_t* c, const DeviceInfo* d, const Group
     g.pair = use_pairs(g) ? 1 : 0;
     return cuda_status(launch_grouped_gemm_tc(g, d->err, d->num_sms, s));
   }
-  return cuda_status(launch_grouped_gemm_simt(g0, s));
+  return cuda_status(launch_grouped_gemm_tf32(g0, d->err, s));
 }
 
 // h = silu(A W_g^T) * (A W_u^T) per group.  With `gather_rows`, row r of the groups is
@@ -343,9 +343,9 @@ moe_status_t routed_groups(const moe_config_t* c, const int32_t* offsets, void* 
   } else {
     gr.table = at<int4>(ws, p.table);
     gr.num_mt = at<int32_t>(ws, p.num_mt);
-    gr.max_mt = max_mtiles(c->T, c->K, c->E, kSimtBM);
+    gr.max_mt = max_mtiles(c->T, c->K, c->E, kF32TileRows);
     if (!table_ready)
-      MOE_CUDA(launch_build_mtile_table(offsets, c->E, kSimtBM, const_cast<int4*>(gr.table),
+      MOE_CUDA(launch_build_mtile_table(offsets, c->E, kF32TileRows, const_cast<int4*>(gr.table),
                                         const_cast<int32_t*>(gr.num_mt), s));
   }
   *out = gr;
@@ -708,7 +708,7 @@ moe_status_t moe_layer_forward_fp8(const moe_config_t* cfg, const void* x, const
   const bool fused = (cfg->flags & MOE_FLAG_FUSED_COMBINE) != 0u;
   float* row_w = fused ? at<float>(ws, p.row_w) : nullptr;
   MOE_CUDA(launch_permute(MOE_BF16, x_codes, ids, T, H / 2, E, K, counts, offsets, perm, inv,
-                          xq_perm, at<int32_t>(ws, p.perm_ws), nullptr, nullptr, kSimtBM, w,
+                          xq_perm, at<int32_t>(ws, p.perm_ws), nullptr, nullptr, kF32TileRows, w,
                           row_w, s));
   MOE_CUDA(launch_gather_scales(x_scales, perm, offsets + E, xs_perm, T * K, s));
   // 3. FP8 gate/up -> bf16 h -> E4M3 h -> FP8 down
@@ -815,15 +815,15 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
   int32_t* num_mt = at<int32_t>(ws, p.num_mt);
   void* x_perm = at<void>(ws, p.x_perm);
   float* out_perm = at<float>(ws, p.out_perm);
-  const bool simt = cfg->dtype == MOE_F32;
+  const bool f32 = cfg->dtype == MOE_F32;
   // the fused combine needs the tensor-core engine; float32 layers keep the gather combine
-  const bool fused = (cfg->flags & MOE_FLAG_FUSED_COMBINE) != 0u && !simt;
+  const bool fused = (cfg->flags & MOE_FLAG_FUSED_COMBINE) != 0u && !f32;
   // Larger batches: the gate/up GEMM reads the permuted copy x_perm.  Its row-gather
   // variant (TMA tile::gather4, four 128-byte rows per request) measured about 3x slower
   // than the copy plus whole-tile TMA loads when every group has hundreds of rows.
 
   // 1. router scores, top-k, gate drop
-  // 2. dispatch: stable permutation, inverse map, row gather (+ the SIMT m-tile table);
+  // 2. dispatch: stable permutation, inverse map, row gather (+ the float32 m-tile table);
   //    decode-sized bf16 batches do both in one cluster launch, other small batches run
   //    the top-k inside the permutation's launch
   float* row_w = fused ? at<float>(ws, p.row_w) : nullptr;
@@ -852,12 +852,12 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
       MOE_CUDA(launch_topk_permute_small(partial, deferred, router_bias, logits, ids, w,
                                          cfg->gate_threshold, cfg->dtype, x, cfg->T, cfg->H,
                                          cfg->E, cfg->K, counts, offsets, perm, inv, x_perm,
-                                         simt ? table : nullptr, simt ? num_mt : nullptr, kSimtBM,
+                                         f32 ? table : nullptr, f32 ? num_mt : nullptr, kF32TileRows,
                                          row_w, s));
     } else {
       MOE_CUDA(launch_permute(cfg->dtype, x, ids, cfg->T, cfg->H, cfg->E, cfg->K, counts,
                               offsets, perm, inv, x_perm, at<int32_t>(ws, p.perm_ws),
-                              simt ? table : nullptr, simt ? num_mt : nullptr, kSimtBM, w, row_w,
+                              f32 ? table : nullptr, f32 ? num_mt : nullptr, kF32TileRows, w, row_w,
                               s));
     }
   }

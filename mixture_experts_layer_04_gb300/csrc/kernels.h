@@ -35,9 +35,10 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&lc, kernel, std::forward<Args>(args)...);
 }
 
-// Rows per m-tile of the tensor-core grouped GEMM and of the SIMT grouped GEMM.
+// Rows per m-tile of the bf16 grouped GEMM and of the float32 grouped GEMM (whose groups
+// come from an m-tile table of 64-row tiles).
 constexpr int kTcBM = 128;
-constexpr int kSimtBM = 64;
+constexpr int kF32TileRows = 64;
 
 // ------------------------------------------------------------------ routing ----
 // Router logits on the CUDA cores (see route.cu for when each is used).
@@ -122,7 +123,7 @@ cudaError_t launch_combine(int dtype, const float* out_perm, const int32_t* inv,
                            cudaStream_t s);
 
 // --------------------------------------------------------- grouped GEMMs ----
-// Grouped NT GEMM description shared by the SIMT (float) and the tcgen05 (bf16)
+// Grouped NT GEMM description shared by the float32 (tf32 split) and the bf16 / FP8
 // engines: for every m-tile (group g, rows row0..row_end-1 of A):
 //   C[row, n] = sum_k A[row, k] * B[g, n, k]                      (mode kPlain)
 //   C[row, n] = silu(sum_k A B[g, n, k]) * (sum_k A B[g, up + n, k])  (mode kSwiGLU)
@@ -149,7 +150,7 @@ struct GroupedGemm {
   // Groups: device row offsets [G+1] of the groups in A (tensor-core engine), or
   // null for a single group 0 covering rows 0..rows_alloc-1.
   const int32_t* offsets;
-  // SIMT engine: a device m-tile table {group, row0, row_end, 0} with a device count,
+  // float32 engine: a device m-tile table {group, row0, row_end, 0} with a device count,
   // or null for a single group.
   const int4* mtile_table;
   const int32_t* num_mtiles;
@@ -174,7 +175,9 @@ struct GroupedGemm {
 };
 
 
-cudaError_t launch_grouped_gemm_simt(const GroupedGemm& g, cudaStream_t s);
+// float32 layers on the tensor cores (gemm_tf32.cu): three kind::tf32 MMAs per k-step on
+// operands split into a tf32 part and a remainder; groups from the m-tile table (64 rows).
+cudaError_t launch_grouped_gemm_tf32(const GroupedGemm& g, unsigned* err, cudaStream_t s);
 // FP8 (E4M3) per-row quantisation of a bf16 [rows, cols] matrix (quant.cu); cols % 8 == 0.
 cudaError_t launch_quantize_fp8(const void* in, long long rows, int cols, uint8_t* codes,
                                 float* scales, cudaStream_t s);
