@@ -256,7 +256,7 @@ moe_status_t launch_gemm(const moe_config_t* c, const DeviceInfo* d, const Group
     g.pair = use_pairs(g) ? 1 : 0;
     return cuda_status(launch_grouped_gemm_tc(g, d->err, d->num_sms, s));
   }
-  return cuda_status(launch_grouped_gemm_tf32(g0, d->err, s));
+  return cuda_status(launch_grouped_gemm_tf32(g0, d->err, d->num_sms, s));
 }
 
 // h = silu(A W_g^T) * (A W_u^T) per group.  With `gather_rows`, row r of the groups is

@@ -13,7 +13,8 @@
 // and the 64 matching up rows), 64 token rows of one group (an entry of the m-tile table)
 // as N.  TMEM lane = weight row (output feature), column = token row.  Per CTA one tile:
 //   warp 0    TMA producer: weights [G, Nb, Kd] and token rows [rows, Kd] in 128-byte
-//             k-steps (32 floats) with the 128-byte swizzle, S stages ahead;
+//             k-steps (32 floats) with the 128-byte swizzle, 4 stages ahead (2, with two
+//             CTAs per SM, when the grid has more tiles than the GPU has SMs);
 //   warps 2-5 split every landed stage into hi (in place) and lo (a second buffer), then
 //             run the epilogue;
 //   warp 1    allocates TMEM and issues the MMAs; tcgen05.commit frees each stage.
@@ -35,16 +36,22 @@ constexpr int kTfThreads = 192;
 constexpr int kTfRowsW = 128;   // weight rows per tile (MMA M)
 constexpr int kTfRowsT = kF32TileRows;  // token rows per tile (MMA N), one m-tile table entry
 constexpr int kTfKStep = 32;    // floats per 128-byte k-step
-constexpr int kTfStages = 4;
 constexpr int kWBytes = kTfRowsW * 128;  // 16 KB
 constexpr int kTBytes = kTfRowsT * 128;  // 8 KB
 constexpr int kHiBytes = kWBytes + kTBytes;
 constexpr int kStageBytes = 2 * kHiBytes;  // hi (weights, tokens) then lo (same layout)
 constexpr int kXchgStride = kTfRowsT + 1;  // floats per exchange row (bank spread)
-constexpr int kXchgBytes = 64 * kXchgStride * 4;
-constexpr int kTfSmem = 1024 + kTfStages * kStageBytes + kXchgBytes + 256;
+constexpr int kXchgBytes = 64 * kXchgStride * 4;  // reuses stage 0 once the MMAs are done
+// Stages: 4 with one CTA per SM, or 2 with two CTAs per SM when the grid has more tiles
+// than the GPU has SMs (the same bytes in flight per SM, and one wave instead of two).
+template <int S>
+constexpr int tf_smem() {
+  return 1024 + S * kStageBytes + 256;
+}
+static_assert(kXchgBytes <= kStageBytes, "exchange buffer inside stage 0");
 static_assert(kTfRowsT == 64, "MMA N = 64 token rows");
-static_assert(kTfSmem <= 232448, "shared memory per CTA");
+static_assert(tf_smem<4>() <= 232448, "shared memory per CTA");
+static_assert(2 * (tf_smem<2>() + 1024) <= 233472, "two CTAs per SM");
 
 struct TfParams {
   CUtensorMap tmW;  // [G, Nb, Kd] fp32, box 32 x (64 or 128) x 1
@@ -107,13 +114,15 @@ __device__ __forceinline__ float4 split_hi(float4& v) {
   return hi;
 }
 
-template <int MODE>
-__global__ void __launch_bounds__(kTfThreads, 1) tf32x3_gemm_kernel(const __grid_constant__ TfParams p) {
+template <int MODE, int kTfStages>
+__global__ void __launch_bounds__(kTfThreads, kTfStages == 2 ? 2 : 1)
+    tf32x3_gemm_kernel(const __grid_constant__ TfParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  float* xchg = reinterpret_cast<float*>(smem + kTfStages * kStageBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kTfStages * kStageBytes + kXchgBytes);
+  // SwiGLU epilogue exchange: stage 0's buffer, free once the last MMA has completed
+  float* xchg = reinterpret_cast<float*>(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kTfStages * kStageBytes);
   // bars: full[S], split[S], empty[S], tfull, mma_done; then the TMEM slot and abort flag
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kTfStages + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -371,15 +380,15 @@ bool make_map_f32(CUtensorMap* m, const void* base, int rank, const uint64_t* di
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE>
-cudaError_t launch_tf32(const GroupedGemm& g, unsigned* err, cudaStream_t s) {
+template <int MODE, int S>
+cudaError_t launch_tf32(const GroupedGemm& g, unsigned* err, dim3 grid, cudaStream_t s) {
   static int attr_set_dev = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  auto kernel = tf32x3_gemm_kernel<MODE>;
+  auto kernel = tf32x3_gemm_kernel<MODE, S>;
   if (attr_set_dev != dev) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTfSmem);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tf_smem<S>());
     if (e != cudaSuccess) return e;
     attr_set_dev = dev;
   }
@@ -400,19 +409,27 @@ cudaError_t launch_tf32(const GroupedGemm& g, unsigned* err, cudaStream_t s) {
   p.num_kb = g.Kd / kTfKStep;
   p.N_out = g.N_out;
   p.up_offset = g.up_offset;
+  return launch_pdl(kernel, grid, dim3(kTfThreads), tf_smem<S>(), s, p);
+}
+
+template <int MODE>
+cudaError_t launch_tf32_mode(const GroupedGemm& g, unsigned* err, int num_sms, cudaStream_t s) {
   constexpr int kColsOut = MODE == kSwiGLU ? kTfRowsW / 2 : kTfRowsW;
   const int mt = g.mtile_table != nullptr ? g.max_mtiles : (g.rows_alloc + kTfRowsT - 1) / kTfRowsT;
   if (mt == 0) return cudaSuccess;
-  dim3 grid((g.N_out + kColsOut - 1) / kColsOut, mt);
-  return launch_pdl(kernel, grid, dim3(kTfThreads), kTfSmem, s, p);
+  const dim3 grid((g.N_out + kColsOut - 1) / kColsOut, mt);
+  if (static_cast<long long>(grid.x) * grid.y > num_sms)
+    return launch_tf32<MODE, 2>(g, err, grid, s);
+  return launch_tf32<MODE, 4>(g, err, grid, s);
 }
 
 }  // namespace
 
-cudaError_t launch_grouped_gemm_tf32(const GroupedGemm& g, unsigned* err, cudaStream_t s) {
+cudaError_t launch_grouped_gemm_tf32(const GroupedGemm& g, unsigned* err, int num_sms,
+                                     cudaStream_t s) {
   if (g.dtype != kF32 || g.Kd % kTfKStep != 0 || g.rows_alloc == 0) return cudaErrorInvalidValue;
-  if (g.mode == kSwiGLU) return launch_tf32<kSwiGLU>(g, err, s);
-  if (g.mode == kPlain) return launch_tf32<kPlain>(g, err, s);
+  if (g.mode == kSwiGLU) return launch_tf32_mode<kSwiGLU>(g, err, num_sms, s);
+  if (g.mode == kPlain) return launch_tf32_mode<kPlain>(g, err, num_sms, s);
   return cudaErrorInvalidValue;
 }
 

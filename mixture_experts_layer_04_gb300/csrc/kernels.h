@@ -177,7 +177,8 @@ struct GroupedGemm {
 
 // float32 layers on the tensor cores (gemm_tf32.cu): three kind::tf32 MMAs per k-step on
 // operands split into a tf32 part and a remainder; groups from the m-tile table (64 rows).
-cudaError_t launch_grouped_gemm_tf32(const GroupedGemm& g, unsigned* err, cudaStream_t s);
+cudaError_t launch_grouped_gemm_tf32(const GroupedGemm& g, unsigned* err, int num_sms,
+                                     cudaStream_t s);
 // FP8 (E4M3) per-row quantisation of a bf16 [rows, cols] matrix (quant.cu); cols % 8 == 0.
 cudaError_t launch_quantize_fp8(const void* in, long long rows, int cols, uint8_t* codes,
                                 float* scales, cudaStream_t s);
