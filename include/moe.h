@@ -173,7 +173,9 @@ moe_status_t moe_permute_noalloc(const moe_config_t* cfg, const void* x, const i
  * activation and output projection) and "MoE大模型的智能调度…" §2.2 expert layer (every
  * expert is a two-layer FFN of the same shape with its own weights).  Activation:
  * SwiGLU, out = (silu(x W_g^T) * (x W_u^T)) W_d^T; the intermediate h is rounded to
- * `act` between the two GEMMs; accumulation is fp32.
+ * `act` between the two GEMMs; accumulation is fp32.  Float32 layers multiply on the
+ * tensor cores with each operand split into a tf32 part and its remainder (three tf32
+ * products per step), which keeps the accuracy of a float32 dot product.
  *   x_perm    [T*K,H] act in; rows offsets[e]..offsets[e+1]-1 belong to expert e.
  *   offsets   [E+1] int32 in (device).
  *   w_gate_up [E,2I,H] act: rows 0..I-1 of expert e = W_g, rows I..2I-1 = W_u.
