@@ -11,6 +11,7 @@ import pytest
 import oracle
 import oracle.moe_oracle as om
 from tests import test_oracle_bruteforce as bf
+from tests import test_oracle_fp8 as fp8_pins
 from tests import test_oracle_pins as pins
 
 
@@ -142,3 +143,55 @@ def test_planted_mistake_is_caught(monkeypatch, golden_dir, name, bad):
     _patch(monkeypatch, name, bad)
     with pytest.raises(AssertionError):
         _all_pins(golden_dir)
+
+
+# FP8 experts (P1 §4.1, 8-bit expert weights): plausible slips in applying the per-row and
+# per-channel scales.  The unit-scale pins cannot see them; the hand-worked cases with
+# distinct power-of-two scales and the dequantised-operand comparison must.
+
+def _gate_up_fp8_divides_scales(x_codes, x_scale, w_codes, w_scale):
+    acc = np.asarray(x_codes, np.float64) @ np.asarray(w_codes, np.float64).T
+    acc = acc / np.asarray(x_scale, np.float64)[:, None] / np.asarray(w_scale, np.float64)[None, :]
+    I = acc.shape[1] // 2
+    return om.silu(acc[:, :I]) * acc[:, I:]
+
+
+def _gate_up_fp8_gate_scales_on_up(x_codes, x_scale, w_codes, w_scale):
+    ws = np.asarray(w_scale, np.float64)
+    I = ws.shape[0] // 2
+    ws = np.concatenate([ws[:I], ws[:I]])
+    acc = (np.asarray(x_codes, np.float64) @ np.asarray(w_codes, np.float64).T) * \
+        np.asarray(x_scale, np.float64)[:, None] * ws[None, :]
+    return om.silu(acc[:, :I]) * acc[:, I:]
+
+
+def _down_fp8_divides_scales(h_codes, h_scale, w_codes, w_scale):
+    acc = np.asarray(h_codes, np.float64) @ np.asarray(w_codes, np.float64).T
+    return acc / np.asarray(h_scale, np.float64)[:, None] / np.asarray(w_scale, np.float64)[None, :]
+
+
+def _down_fp8_row_scale_per_channel(h_codes, h_scale, w_codes, w_scale):
+    acc = np.asarray(h_codes, np.float64) @ np.asarray(w_codes, np.float64).T
+    hs = np.resize(np.asarray(h_scale, np.float64), acc.shape[1])
+    return acc * hs[None, :] * np.asarray(w_scale, np.float64)[None, :]
+
+
+def _fp8_pins():
+    fp8_pins.test_fp8_gate_up_reduces_to_plain_on_exact_operands()
+    fp8_pins.test_fp8_down_reduces_to_plain_on_exact_operands()
+    fp8_pins.test_fp8_gate_up_hand_worked()
+    fp8_pins.test_fp8_down_hand_worked()
+    fp8_pins.test_fp8_products_equal_plain_products_of_dequantised_operands()
+
+
+@pytest.mark.parametrize("name,bad", [
+    ("expert_gate_up_fp8", _gate_up_fp8_divides_scales),
+    ("expert_gate_up_fp8", _gate_up_fp8_gate_scales_on_up),
+    ("expert_down_fp8", _down_fp8_divides_scales),
+    ("expert_down_fp8", _down_fp8_row_scale_per_channel),
+])
+def test_planted_fp8_scale_mistake_is_caught(monkeypatch, name, bad):
+    _fp8_pins()                      # the real oracle passes every FP8 pin
+    monkeypatch.setattr(om, name, bad)
+    with pytest.raises(AssertionError):
+        _fp8_pins()
