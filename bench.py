@@ -11,11 +11,19 @@ step's data is evicted and no dirty lines are left behind); W untimed warm-up st
 N > 1 (torchrun) every rank runs an independent replica on its own GPU (the layer has
 no exchange step on one GPU): weak scaling, value = all tokens / slowest rank's time.
 
+The default workload is the largest one, the DeepSeek-shaped layer (T=16384, H=7168,
+256 routed experts top-8 with the 0.05 gate drop, one shared expert).  The same line
+carries the decode half of the metric: the Qwen3-shaped layer at T = 1, 8, 32 and 64
+tokens, each replayed from a CUDA graph ("decode_sweep"; --no-decode-sweep skips it).
+
 Extra keys: "roofline" for the dominant kernel (the grouped gate/up GEMM, timed alone
-through moe_expert_gate_up), "cpu_baseline" (the CPU oracle on a bounded token sample),
-"e2e" (the same metric with host buffers: H2D of x and D2H of y inside the timed
-region), "stages_us" (route / permute / gate_up / down / shared / combine, timed one by
-one), "clocks" (nvidia-smi samples taken during the timed region).
+through moe_expert_gate_up, against the measured peaks), "layer_roofline" (the whole layer
+against the measured and the nominal GB300 peaks, 2.25 PFLOP/s dense bf16 and 8 TB/s),
+"cpu_baseline" (the CPU oracle on a bounded token sample), "e2e" (the same metric with
+host buffers: H2D of x and D2H of y inside the timed region), "stages_us" (route /
+permute / gate_up / down / shared / combine, timed one by one), "gpu_launches" (the
+library's own launch counter over the timed region), "clocks" (nvidia-smi samples taken
+during the timed region).
 """
 
 from __future__ import annotations
@@ -45,6 +53,10 @@ KERNEL_SOURCES = [os.path.join(ROOT, "mixture_experts_layer_04_gb300", "csrc", f
                   for f in ("gemm_tc.cu", "common.cuh")]
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# nominal GB300 peaks, the ones the layer's targets are stated against
+NOMINAL_TFLOPS = 2250.0
+NOMINAL_GBS = 8000.0
+DECODE_SWEEP = (1, 8, 32, 64)
 
 
 def parse():
@@ -53,7 +65,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="mixtral", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--config", default="deepseek", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--tokens", type=int, default=None, help="token count (decode sweeps)")
     ap.add_argument("--cpu-sample", type=int, default=None, help="tokens in the CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -71,6 +83,8 @@ def parse():
                     help="capacity-limited routing (MOE_FLAG_CAPACITY: ceil(1.2 T K / E) per expert)")
     ap.add_argument("--time-row-gather", action="store_true",
                     help="also time the row-gather gate/up variant as a stage")
+    ap.add_argument("--no-decode-sweep", action="store_true",
+                    help="skip the Qwen3-shaped decode sweep (T = 1, 8, 32, 64)")
     return ap.parse_args()
 
 
@@ -197,42 +211,6 @@ def recorded_traffic(workload, kernel):
     return None
 
 
-def kernel_launches_per_step(shape, T, capacity=False):
-    """Kernels this library launches for one moe_layer_forward (the count is exact: it
-    mirrors the launch sequence of the C ABI for this config)."""
-    if T == 0:
-        return 0
-    n = 0
-    b = 2 if shape.dtype == "bf16" else 4
-    E, H, K = shape.E, shape.H, shape.K
-    tc_router = shape.dtype == "bf16" and T >= 256 and E >= 32 and E % 16 == 0
-    wsmem_router = E <= 16 and E * H * b <= 96 * 1024 and T >= 64
-    fused_small = T <= 64 and (E * 8 * 4 + (2 * E + 1) * 4 + T * K * 12 + T * E * 4) <= 200 * 1024
-    cluster = shape.dtype == "bf16" and T <= 64 and E <= 256 and K <= 16 and not capacity
-    if capacity:
-        fused_small = False           # the top-k is not deferred into the permutation
-    if cluster:
-        n += 2                            # routing + permutation in one cluster launch; gate/up
-        n += 1                            # down
-        if shape.I_shared:
-            n += 2
-        return n + 1                      # combine
-    if tc_router:
-        n += 1 if E <= 256 else 2         # router GEMM (top-k in its epilogue up to 256 experts)
-    elif wsmem_router:
-        n += 1                            # router with the top-k fused
-    else:
-        n += 1 if fused_small else 2      # partial logits (+ top-k unless fused below)
-    if capacity:
-        n += 1                            # the capacity sweep over the router's choices
-    n += 1 if T <= 256 else 3             # one-launch permutation, or rank + scan + scatter
-    n += 2                                # grouped gate/up, grouped down
-    if shape.I_shared:
-        n += 2
-    n += 1                                # combine
-    return n
-
-
 def algorithmic(shape, T, counts):
     """FLOPs and bytes the layer must do (not the dense work it avoids)."""
     M = int(counts.sum())
@@ -303,10 +281,12 @@ def run_ours(args, rank, world, local):
     layer_step = step
     if use_graph:
         graph = torch.cuda.CUDAGraph()
+        c0 = moe.kernel_launch_count()
         with torch.cuda.graph(graph):
             moe.layer_forward(cfg, inp["x"], inp["w_router"], inp["router_bias"], inp["w_gate_up"],
                               inp["w_down"], inp.get("w_shared_gate_up"), inp.get("w_shared_down"),
                               y, None, ws, stream=torch.cuda.current_stream(dev))
+        graph_launches = moe.kernel_launch_count() - c0
         layer_step = graph.replay
         for _ in range(3):
             flush_l2()
@@ -317,9 +297,15 @@ def run_ours(args, rank, world, local):
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
+        n0 = moe.kernel_launch_count()
         t_wall0 = time.perf_counter()
         times = timed(layer_step, args.steps)
         t_wall = time.perf_counter() - t_wall0
+        # the library's own launch counter (timed() makes one untimed call before the K
+        # timed ones); a graph replays the launches counted at its capture
+        per_step = ((moe.kernel_launch_count() - n0) / (args.steps + 1) if not use_graph
+                    else graph_launches)
+        launches = per_step * args.steps
     if world > 1:
         torch.distributed.barrier()
     moe.sync_check(stream)
@@ -449,9 +435,13 @@ def run_ours(args, rank, world, local):
         fp8_roof["us"] = round(f8_s * 1e6, 2)
         fp8_roof["kernel"] = "tc_grouped_gemm_kernel<...,SwiGLU,F8> (moe_expert_gate_up_fp8)"
 
-    # whole-layer roofline: the slower of FLOPs at the bf16 peak and bytes at HBM speed
+    # whole-layer roofline: the slower of FLOPs at the bf16 peak and bytes at HBM speed,
+    # against the measured peaks and against the nominal GB300 peaks
     t_roof = max(alg["flops"] / (peaks["bf16_tflops"] * 1e12), alg["bytes"] / (peaks["hbm_gbs"] * 1e9))
     layer_frac = t_roof / (ms / 1e3)
+    t_nom = max(alg["flops"] / (NOMINAL_TFLOPS * 1e12), alg["bytes"] / (NOMINAL_GBS * 1e9))
+    layer_bound = "tensor" if alg["flops"] / NOMINAL_TFLOPS / 1e12 >= alg["bytes"] / NOMINAL_GBS / 1e9 \
+        else "hbm"
 
     # end to end through the public API with host buffers (x in, y out, pinned)
     x_host = inp["x"].cpu().pin_memory()
@@ -512,19 +502,95 @@ def run_ours(args, rank, world, local):
                    "group_rows_max": int(counts.max()), "empty_experts": int((counts == 0).sum())},
         "roofline": roof,
         **({"fp8_gate_up": fp8_roof} if fp8_roof is not None else {}),
-        "layer_roofline": {"t_roofline_us": round(t_roof * 1e6, 2), "frac": round(layer_frac, 4),
-                           "flops": alg["flops"], "bytes": alg["bytes"], "peaks": peak_kind},
+        "layer_roofline": {"bound": layer_bound,
+                           "t_roofline_us": round(t_roof * 1e6, 2), "frac": round(layer_frac, 4),
+                           "peaks": peak_kind,
+                           "t_roofline_nominal_us": round(t_nom * 1e6, 2),
+                           "frac_nominal": round(t_nom / (ms / 1e3), 4),
+                           "nominal_peaks": {"tflops_bf16": NOMINAL_TFLOPS, "hbm_gbs": NOMINAL_GBS},
+                           "target_frac_nominal": 0.6 if layer_bound == "tensor" else 0.7,
+                           "flops": alg["flops"], "bytes": alg["bytes"]},
         "stages_us": stages_us,
         "e2e": {"value": round(T * world / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                 "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
                 "d2h_bytes_per_step": y_host.numel() * y_host.element_size(),
                 "cuda_graph": bool(use_graph)},
-        "gpu_launches": kernel_launches_per_step(shape, T, args.capacity) * args.steps,
+        "gpu_launches": int(launches),
+        "gpu_launches_source": "moe_kernel_launch_count() over the timed steps (graph: launches "
+                               "captured x replays)",
         "clocks": clk.summary(),
         "wall_s_timed_region": round(t_wall, 3),
     }
+    if not args.no_decode_sweep and args.config != "qwen_decode" and args.tokens is None:
+        res["decode_sweep"] = decode_sweep(args, moe, dev, stream, timed, peaks)
     return res, shape, T, inp
+
+
+def decode_sweep(args, moe, dev, stream, timed, peaks):
+    """The decode half of the metric: the Qwen3-shaped layer (H=2048, E=128, top-8, I=768,
+    per-expert logit bias) at T = 1, 8, 32 and 64 tokens, each replayed from a CUDA graph
+    with L2 flushed between replays.  Per T: us per layer, the layer against its HBM
+    roofline (measured copy bandwidth and nominal 8 TB/s), and the gate/up GEMM alone
+    (its algorithmic bytes / its time, against the measured copy bandwidth)."""
+    shape = synth.WORKLOADS["qwen_decode"]
+    out = {}
+    for T in DECODE_SWEEP:
+        inp = synth.make_inputs(shape, device=dev, T=T)
+        fused = shape.K >= 8
+        cfg = moe.MoEConfig.make(T, shape.H, shape.E, shape.K, shape.I, shape.I_shared,
+                                 shape.theta, moe.BF16, moe.FLAG_FUSED_COMBINE if fused else 0)
+        ws = torch.empty(moe.workspace_size(cfg), dtype=torch.uint8, device=dev)
+        y = torch.empty(T, shape.H, dtype=shape.torch_dtype, device=dev)
+
+        def layer(st):
+            moe.layer_forward(cfg, inp["x"], inp["w_router"], inp["router_bias"],
+                              inp["w_gate_up"], inp["w_down"], None, None, y, None, ws, stream=st)
+
+        for _ in range(3):
+            layer(stream)
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        c0 = moe.kernel_launch_count()
+        with torch.cuda.graph(graph):
+            layer(torch.cuda.current_stream(dev))
+        n_launch = moe.kernel_launch_count() - c0
+        for _ in range(3):
+            graph.replay()
+        t_layer = statistics.mean(timed(graph.replay, max(args.steps, 10))) / 1e3
+        moe.sync_check(stream)
+        # routing and dispatch of this batch, then the gate/up GEMM alone
+        E, K, H_, I = shape.E, shape.K, shape.H, shape.I
+        logits = torch.empty(T, E, dtype=torch.float32, device=dev)
+        ids = torch.empty(T, K, dtype=torch.int32, device=dev)
+        w = torch.empty(T, K, dtype=torch.float32, device=dev)
+        counts = torch.empty(E, dtype=torch.int32, device=dev)
+        offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        perm = torch.empty(T * K, dtype=torch.int32, device=dev)
+        inv = torch.empty(T * K, dtype=torch.int32, device=dev)
+        x_perm = torch.empty(T * K, H_, dtype=shape.torch_dtype, device=dev)
+        h = torch.empty(T * K, I, dtype=shape.torch_dtype, device=dev)
+        moe.route(cfg, inp["x"], inp["w_router"], inp["router_bias"], logits, ids, w, stream=stream)
+        moe.permute(cfg, inp["x"], ids, counts, offsets, perm, inv, x_perm, ws, stream=stream)
+        t_gu = statistics.mean(timed(lambda: moe.expert_gate_up(
+            cfg, x_perm, offsets, inp["w_gate_up"], h, ws, stream=stream), max(args.steps, 10))) / 1e3
+        moe.sync_check(stream)
+        alg = algorithmic(shape, T, counts.cpu().numpy())
+        gu_gbs = alg["gate_up_bytes"] / t_gu / 1e9
+        out[f"T{T}"] = {
+            "us_per_layer": round(t_layer * 1e6, 2),
+            "layer_bytes": alg["bytes"], "experts_touched": alg["touched"],
+            "layer_gbs": round(alg["bytes"] / t_layer / 1e9, 1),
+            "layer_frac_measured_hbm": round(alg["bytes"] / t_layer / 1e9 / peaks["hbm_gbs"], 4),
+            "layer_frac_nominal_hbm": round(alg["bytes"] / t_layer / 1e9 / NOMINAL_GBS, 4),
+            "gate_up_us": round(t_gu * 1e6, 2), "gate_up_gbs": round(gu_gbs, 1),
+            "gate_up_frac_measured_hbm": round(gu_gbs / peaks["hbm_gbs"], 4),
+            "launches_per_layer": int(n_launch),
+        }
+        del graph
+    return {"workload": "qwen_decode (H=2048, E=128, K=8, I=768, N(0,1) expert bias)",
+            "timing": "CUDA-graph replay, L2 flushed between replays", "target_frac_nominal_hbm": 0.7,
+            **out}
 
 
 def oracle_sample(shape, T, inp, n_tokens, seed=0):

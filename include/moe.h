@@ -338,6 +338,13 @@ moe_status_t moe_sync_check(moe_stream_t stream);
  * exits normally, so the CUDA context stays usable.  `done` is an int in device memory. */
 moe_status_t moe_debug_wait_timeout(unsigned limit_us, int* done, moe_stream_t stream);
 
+/* Number of kernels this library has launched in this process, on every device: each
+ * launch the CUDA runtime accepted counts once.  A launch issued while a stream is being
+ * captured into a CUDA graph counts once, at capture; replays of the graph are not
+ * counted.  Memset and copy operations are not kernels of this library and do not count.
+ * No counterpart on the pages: a diagnostic for callers that check which work ran. */
+unsigned long long moe_kernel_launch_count(void);
+
 /* Static, human-readable name of a status code. */
 const char* moe_status_string(moe_status_t status);
 

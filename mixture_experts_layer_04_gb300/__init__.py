@@ -88,6 +88,7 @@ _SIGS = {
     "moe_debug_wait_timeout": [ctypes.c_uint, _P, _P],
     "moe_status_string": [ctypes.c_int],
     "moe_version": [],
+    "moe_kernel_launch_count": [],
 }
 
 
@@ -104,7 +105,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     for name, args in _SIGS.items():
         fn = getattr(lib, name)
         fn.argtypes = args
-        fn.restype = ctypes.c_char_p if name in ("moe_status_string", "moe_version") else ctypes.c_int
+        fn.restype = (ctypes.c_char_p if name in ("moe_status_string", "moe_version") else
+                      ctypes.c_ulonglong if name == "moe_kernel_launch_count" else ctypes.c_int)
     _LIB = lib
     return lib
 
@@ -137,6 +139,11 @@ def status_string(status: int) -> str:
 
 def version() -> str:
     return load().moe_version().decode()
+
+
+def kernel_launch_count() -> int:
+    """Kernels the library has launched in this process (moe_kernel_launch_count)."""
+    return int(load().moe_kernel_launch_count())
 
 
 def workspace_size(cfg: MoEConfig) -> int:

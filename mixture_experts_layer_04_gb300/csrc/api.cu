@@ -380,6 +380,14 @@ __global__ void wait_timeout_probe_kernel(unsigned* err, unsigned long long limi
 }
 
 }  // namespace
+
+std::atomic<unsigned long long> g_kernel_launches{0};
+
+moe_status_t check_current_device() {
+  const DeviceInfo* d = nullptr;
+  return check_device(&d);
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -912,7 +920,11 @@ moe_status_t moe_debug_wait_timeout(unsigned limit_us, int* done, moe_stream_t s
   MOE_TRY(check_device(&d));
   wait_timeout_probe_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(
       d->err, static_cast<unsigned long long>(limit_us) * 1000ull, done);
-  return cuda_status(cudaGetLastError());
+  return cuda_status(count_launch(cudaGetLastError()));
+}
+
+unsigned long long moe_kernel_launch_count(void) {
+  return moe::g_kernel_launches.load(std::memory_order_relaxed);
 }
 
 moe_status_t moe_sync_check(moe_stream_t stream) {

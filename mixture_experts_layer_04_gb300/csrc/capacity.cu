@@ -424,7 +424,7 @@ cudaError_t launch_capacity_route(const float* logits, int32_t* ids, float* w, i
   at[1].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = at;
   lc.numAttrs = 2;
-  return cudaLaunchKernelEx(&lc, capacity_route_kernel, logits, ids, w, T, E, K, theta, cap, err);
+  return count_launch(cudaLaunchKernelEx(&lc, capacity_route_kernel, logits, ids, w, T, E, K, theta, cap, err));
 }
 
 }  // namespace moe

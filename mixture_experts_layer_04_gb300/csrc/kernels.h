@@ -6,6 +6,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/moe.h"
+
+#include <atomic>
 #include <cstring>
 #include <utility>
 
@@ -14,6 +17,15 @@ namespace moe {
 enum DType : int { kF32 = 0, kBF16 = 1 };
 
 inline size_t act_bytes(int dtype) { return dtype == kBF16 ? 2 : 4; }
+
+// Kernels this library has launched in this process (launches the runtime accepted, on
+// every device; a launch into a stream being captured counts once, at capture).
+extern std::atomic<unsigned long long> g_kernel_launches;
+
+inline cudaError_t count_launch(cudaError_t e) {
+  if (e == cudaSuccess) g_kernel_launches.fetch_add(1, std::memory_order_relaxed);
+  return e;
+}
 
 // Launch with programmatic stream serialization: the kernel may be scheduled while the
 // previous kernel on the stream is still running; every kernel of this library calls
@@ -32,7 +44,7 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, kernel, std::forward<Args>(args)...);
+  return count_launch(cudaLaunchKernelEx(&lc, kernel, std::forward<Args>(args)...));
 }
 
 // Rows per m-tile of the bf16 grouped GEMM and of the float32 grouped GEMM (whose groups
@@ -85,6 +97,11 @@ cudaError_t launch_topk(const float* partial, int S, const float* bias, float* l
 // ---------------------------------------------------------------- dispatch ----
 // Workspace (int32 words) the permutation needs for T tokens, E experts.
 size_t permute_ws_words(int T, int E);
+
+// MOE_OK when the current device is an sm_103 GPU this library runs on (the same check
+// every entry point makes), MOE_ERR_UNSUPPORTED when it is not, MOE_ERR_CUDA when the
+// device cannot be queried.
+moe_status_t check_current_device();
 // Maximum number of m-tiles of `bm` rows over all groups of T*K rows and E experts.
 inline int max_mtiles(int T, int K, int E, int bm) {
   return static_cast<int>((static_cast<long long>(T) * K + bm - 1) / bm) + E;

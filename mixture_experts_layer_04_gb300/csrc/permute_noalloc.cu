@@ -28,37 +28,26 @@ static __device__ __align__(256) int32_t g_permute_scratch[MOE_PERMUTE_NOALLOC_M
 
 constexpr int kMaxDevices = 64;
 
-struct NoAllocDevice {
-  bool ready = false;
-  bool supported = false;
-  int32_t* scratch = nullptr;  // device address of g_permute_scratch on this device
-};
-
-NoAllocDevice g_noalloc_dev[kMaxDevices];
+int32_t* g_noalloc_scratch[kMaxDevices];  // device address of g_permute_scratch, per device
 std::mutex g_noalloc_mu;
 
 // One-time set-up per device, done by the first call on that device with the device
 // current: the symbol above is a host-side stand-in, so its device address has to be
-// looked up with cudaGetSymbolAddress before a kernel may be given it.
+// looked up with cudaGetSymbolAddress before a kernel may be given it.  Which devices are
+// supported is decided by the library's common device check.
 moe_status_t noalloc_setup(int32_t** scratch) {
+  const moe_status_t sd = check_current_device();
+  if (sd != MOE_OK) return sd;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  NoAllocDevice& d = g_noalloc_dev[dev];
-  if (!d.ready) {
-    int major = 0, minor = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    d.supported = (major == 10 && minor == 3);
+  if (g_noalloc_scratch[dev] == nullptr) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || p == nullptr)
       return MOE_ERR_CUDA;
-    d.scratch = static_cast<int32_t*>(p);
-    d.ready = true;
+    g_noalloc_scratch[dev] = static_cast<int32_t*>(p);
   }
-  if (!d.supported) return MOE_ERR_UNSUPPORTED;
-  *scratch = d.scratch;
+  *scratch = g_noalloc_scratch[dev];
   return MOE_OK;
 }
 

@@ -513,7 +513,7 @@ cudaError_t launch_route_cluster(const void* x, const void* w_router, const floa
   at[1].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = at;
   lc.numAttrs = 2;
-  return cudaLaunchKernelEx(&lc, route_dispatch_cluster_kernel, p);
+  return count_launch(cudaLaunchKernelEx(&lc, route_dispatch_cluster_kernel, p));
 }
 
 }  // namespace moe

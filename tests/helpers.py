@@ -100,6 +100,29 @@ def assert_close_y(got, want, max_abs=Y_MAX_ABS, rel_l2=Y_REL_L2, what="y"):
     return err, rel
 
 
+def bf16_half_ulp(v):
+    """Half the spacing of bfloat16 numbers at |v| (8 significant bits): the most a correct
+    round-to-nearest store can move a value."""
+    a = np.maximum(np.abs(np.asarray(v, dtype=np.float64)), 2.0 ** -126)
+    return np.exp2(np.floor(np.log2(a)) - 8)
+
+
+def assert_close_y_rounded(got_bf16, want, max_abs=Y_MAX_ABS, rel_l2=Y_REL_L2, what="y (bf16)"):
+    """The rounded bf16 output against the float64 oracle: every element within max_abs plus
+    half a bf16 ulp of the oracle's value (the store's own rounding, which exceeds max_abs
+    where |y| >= 8), and relative L2 within rel_l2."""
+    got = np.asarray(got_bf16, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    assert got.shape == want.shape
+    if got.size == 0:
+        return
+    excess = np.abs(got - want) - (max_abs + bf16_half_ulp(want))
+    nrm = float(np.linalg.norm(want))
+    rel = float(np.linalg.norm(got - want) / nrm) if nrm > 0 else 0.0
+    assert excess.max() <= 0 and rel <= rel_l2, \
+        f"{what}: worst excess over max-abs + half ulp {excess.max():.3g}, rel-L2 {rel:.3g} (<= {rel_l2})"
+
+
 class LayerRun:
     """Buffers and one moe_layer_forward call of a workload on the GPU."""
 

@@ -10,8 +10,14 @@
   takes every token, forced-empty experts).
 
 Output tolerance (bf16 layers): max-abs 2e-2 and relative L2 1e-2 on the fp32 sum
-y_f32, plus: the bf16 output equals the round-to-nearest-even of y_f32 bit for bit.
-Float32 layers: max-abs and relative L2 1e-3.
+y_f32; the bf16 output y equals the round-to-nearest-even of y_f32 bit for bit, and y
+itself is within max-abs 2e-2 plus half a bf16 ulp of the oracle (the store's rounding)
+and relative L2 1e-2.  Float32 layers: max-abs and relative L2 1e-3.
+
+At full size the sample holds, besides random tokens, the token of the last row of every
+non-empty expert's group and of the first and last rows of its last 128- and 256-row
+tiles, so every group's tail tile (single-CTA, CTA-pair and swapped tails) is compared
+element by element.
 """
 
 import numpy as np
@@ -115,10 +121,14 @@ def test_layer_small_full_oracle(moe, shape, fused):
     y32 = run.y32.double().cpu().numpy()
     H.assert_close_y(y32[ok], ref["y"][ok], **_tol(shape))
     assert torch.equal(run.y, run.y32.to(shape.torch_dtype))
+    if shape.dtype == "bf16":
+        H.assert_close_y_rounded(run.y.double().cpu().numpy()[ok], ref["y"][ok])
 
 
-def _sample_tokens(r, T, n, seed=0):
-    """n tokens: random ones plus tokens routed to the largest and smallest groups."""
+def _sample_tokens(r, T, n, seed=0, tails=False):
+    """n random tokens plus tokens routed to the largest and smallest groups; with
+    `tails`, also the tokens of every non-empty group's last row and of the first and last
+    rows of its last 128- and 256-row tiles (the single-CTA and CTA-pair tail tiles)."""
     rng = np.random.default_rng(seed)
     counts, ids = r["counts"], r["ids"]
     nz = np.nonzero(counts)[0]
@@ -127,7 +137,24 @@ def _sample_tokens(r, T, n, seed=0):
     for e in (big, small):
         hit = np.nonzero((ids == e).any(axis=1))[0]
         pick.update(hit[:2].tolist())
+    if tails:
+        pick.update(_tail_tile_tokens(r).tolist())
     return np.array(sorted(pick))
+
+
+def _tail_tile_tokens(r):
+    """Tokens of every non-empty group's last row and of the first and last rows of its
+    last 128- and 256-row tiles."""
+    counts, offsets, perm = r["counts"], r["offsets"], r["perm"]
+    rows = set()
+    for e in np.nonzero(counts)[0]:
+        c, o = int(counts[e]), int(offsets[e])
+        rows.add(o + c - 1)
+        for tile in (128, 256):
+            rows.add(o + ((c - 1) // tile) * tile)
+            if c > tile:
+                rows.add(o + ((c - 1) // tile) * tile - 1)   # last row of the last full tile
+    return np.unique(perm[np.array(sorted(rows), dtype=np.int64)])
 
 
 FULL = [
@@ -162,11 +189,16 @@ def test_layer_full_size_sampled(moe, name, T, nsample, fused):
     if not amb.any():
         _, offsets_ref, _, _ = oracle.permute(ids_ref, shape.E)
         np.testing.assert_array_equal(r["offsets"], offsets_ref)
-    toks = _sample_tokens(r, Tn, nsample)
+    toks = _sample_tokens(r, Tn, nsample, tails=True)
     toks = toks[~amb[toks]]
     assert len(toks) >= max(1, nsample // 2), "too few unambiguous sampled tokens"
-    experts_checked = len(np.unique(r["ids"][toks][r["ids"][toks] >= 0]))
-    assert experts_checked >= min(shape.E // 4, 8)
+    # every touched expert's tail tile is in the sample (ambiguous tokens aside)
+    checked = set(np.unique(r["ids"][toks][r["ids"][toks] >= 0]).tolist())
+    tail_rows = r["offsets"][1:][r["counts"] > 0] - 1
+    tail_tok = r["perm"][tail_rows]
+    missing = [e for e, t in zip(np.nonzero(r["counts"])[0], tail_tok)
+               if not amb[t] and int(e) not in checked]
+    assert not missing, f"experts whose tail row was not compared: {missing[:8]}"
     sh = {}
     if shape.I_shared:
         sh = dict(w_shared_gate_up=H.f64(inp["w_shared_gate_up"]), w_shared_down=H.f64(inp["w_shared_down"]))
@@ -176,6 +208,7 @@ def test_layer_full_size_sampled(moe, name, T, nsample, fused):
     y32 = run.y32.double().cpu().numpy()[toks]
     H.assert_close_y(y32, ref["y"], **_tol(shape))
     assert torch.equal(run.y, run.y32.to(shape.torch_dtype))
+    H.assert_close_y_rounded(run.y.double().cpu().numpy()[toks], ref["y"])
 
 
 def test_fused_combine_matches_gather_combine(moe):
@@ -382,3 +415,23 @@ def test_streams_and_sync_check(moe):
     b.run()
     torch.cuda.synchronize()
     assert torch.equal(a.y, b.y)
+
+
+def test_kernel_launch_counter(moe):
+    """moe_kernel_launch_count() grows by the same number for two identical layer calls,
+    by at least one launch per stage, and not at all for an empty batch."""
+    shape = synth.MoEShape("cnt", T=700, H=256, E=32, K=4, I=128, I_shared=64, bias="normal",
+                           seed=12)
+    inp = synth.make_inputs(shape, device="cuda")
+    run = H.LayerRun(moe, shape, inp)
+    deltas = []
+    for _ in range(2):
+        n0 = moe.kernel_launch_count()
+        run.run()
+        deltas.append(moe.kernel_launch_count() - n0)
+    moe.sync_check()
+    assert deltas[0] == deltas[1] >= 5      # route, permute, gate/up, down, combine at least
+    empty = H.LayerRun(moe, shape, {k: v[:0] if k == "x" else v for k, v in inp.items()}, T=0)
+    n0 = moe.kernel_launch_count()
+    empty.run()
+    assert moe.kernel_launch_count() == n0
