@@ -89,6 +89,9 @@ struct TcParams {
   const float* a_scale;
   const float* b_scale;
   int b_rows;
+  // grouped launches in the normal operand order: interleave the tiles of groups that
+  // have a single token tile with the tiles of the larger groups (see build_schedule)
+  int interleave;
 };
 
 template <int BN, int MODE, bool SWAP>
@@ -104,7 +107,7 @@ struct TcCfg {
   static constexpr int kStgBytes =
       SWAP ? (MODE == kSwiGLU ? 64 * BN * 4 : 0) : kEpiWarps * 32 * (MODE == kSwiGLU ? 64 : 128);
   static constexpr int kBarBytes = 256;
-  static constexpr int kSchedBytes = 2 * (kMaxGroups + 4) * 4 + 32 * 4;
+  static constexpr int kSchedBytes = 3 * (kMaxGroups + 4) * 4 + 32 * 4;
   // as many stages as shared memory holds (up to 12): the bytes a CTA keeps in flight set
   // its load rate, which is what bounds the small-tile decode kernels
   static constexpr int kStagesRaw =
@@ -116,18 +119,92 @@ struct TcCfg {
   static_assert(kSmem <= 232448, "shared memory per CTA");
 };
 
-// Tile idx -> (group g, token rows row0..row_end-1, weight tile n_tile).  s_off holds the
-// group row offsets and s_mt the exclusive prefix of token tiles per group.
-// Order: groups one after another; inside a group, chunks of up to `swz` token tiles, and
-// inside a chunk the weight tiles outer, token tiles inner.  CTAs running at the same time
-// thus share a weight tile (read once from HBM) and keep a chunk's token rows in L2 while
-// they sweep the weight tiles, and no chunk mixes two groups' weights.
+// The tile schedule of one launch, which every CTA derives from the group row offsets.
+//   s_off[0..G]   the group row offsets;
+//   s_mt[0..G]    exclusive prefix of the token tiles of the groups in the "heavy" order;
+//   s_light[j]    with interleaving, the j-th group that has exactly one token tile.
+// Groups with a single token tile (up to `tile_rows` rows) stream a whole expert's weights
+// for a few rows of MMA work: their tiles are bound by DRAM, while the tiles of large
+// groups reuse each weight tile from L2 across many token tiles and are bound by the
+// tensor cores.  In group order the two kinds come in long runs of one kind (a run of
+// small experts leaves the tensor cores idle while DRAM saturates, a large expert leaves
+// DRAM idle), so with `p.interleave` the single-tile groups are taken out of the heavy
+// order and their tiles are spread evenly through it: out of every N tiles of the launch,
+// N_light/N are single-tile-group tiles.  CTAs that run at the same time then mix both
+// kinds, and the weight streaming of the small experts overlaps the MMAs of the large.
+struct Sched {
+  int num_mt;     // token tiles in the heavy order
+  int num_light;  // groups taken out of the heavy order (interleaved)
+  int total;      // tiles of the launch: (num_mt + num_light) * n_tiles
+};
+
+__device__ __forceinline__ Sched build_schedule(const TcParams& p, int* s_off, int* s_mt,
+                                                int* s_light, int* s_scan, int tile_rows) {
+  Sched sc;
+  sc.num_light = 0;
+  if (p.offsets == nullptr) {
+    sc.num_mt = (p.rows_alloc + tile_rows - 1) / tile_rows;
+    sc.total = sc.num_mt * p.n_tiles;
+    return sc;
+  }
+  const int G = p.num_groups;
+  for (int i = threadIdx.x; i <= G; i += blockDim.x) s_off[i] = p.offsets[i];
+  __syncthreads();
+  const int per = (G + blockDim.x - 1) / blockDim.x;
+  const int beg = min(G, static_cast<int>(threadIdx.x) * per), end = min(G, beg + per);
+  auto tiles_of = [&](int q) { return (s_off[q + 1] - s_off[q] + tile_rows - 1) / tile_rows; };
+  auto light = [&](int q) { return p.interleave != 0 && tiles_of(q) == 1; };
+  int mine = 0, mine_light = 0;
+  for (int q = beg; q < end; ++q) {
+    if (light(q)) ++mine_light;
+    else mine += tiles_of(q);
+  }
+  int all = 0, all_light = 0;
+  int run = block_exclusive_scan(mine, s_scan, &all);
+  int run_light = block_exclusive_scan(mine_light, s_scan, &all_light);
+  for (int q = beg; q < end; ++q) {
+    s_mt[q] = run;
+    if (light(q)) s_light[run_light++] = q;
+    else run += tiles_of(q);
+  }
+  if (threadIdx.x == 0) s_mt[G] = all;
+  __syncthreads();
+  sc.num_mt = all;
+  sc.num_light = all_light;
+  sc.total = (all + all_light) * p.n_tiles;
+  return sc;
+}
+
+// Tile idx -> (group g, token rows row0..row_end-1, weight tile n_tile).
+// Heavy order: groups one after another; inside a group, chunks of up to `swz` token tiles,
+// and inside a chunk the weight tiles outer, token tiles inner.  CTAs running at the same
+// time thus share a weight tile (read once from HBM) and keep a chunk's token rows in L2
+// while they sweep the weight tiles, and no chunk mixes two groups' weights.  With
+// interleaved single-tile groups, tile idx is one of theirs when floor(idx * NL / N) steps
+// up at idx (NL of the N tiles are theirs, taken group by group, weight tiles inner);
+// otherwise it is heavy tile idx - floor(idx * NL / N).
 __device__ __forceinline__ void decode_tile(const TcParams& p, const int* s_off, const int* s_mt,
-                                            int num_mt, int tile_rows, int idx, int& g, int& row0,
-                                            int& row_end, int& n_tile) {
+                                            const int* s_light, const Sched& sc, int tile_rows,
+                                            int idx, int& g, int& row0, int& row_end,
+                                            int& n_tile) {
   const int nt = p.n_tiles;
   int mt;  // token tile index inside its group
   if (p.offsets != nullptr) {
+    if (sc.num_light > 0) {
+      const long long NL = static_cast<long long>(sc.num_light) * nt;
+      const long long N = sc.total;
+      const long long cl = static_cast<long long>(idx) * NL / N;
+      const long long cl1 = (static_cast<long long>(idx) + 1) * NL / N;
+      if (cl1 > cl) {
+        const int j = static_cast<int>(cl / nt);
+        n_tile = static_cast<int>(cl - static_cast<long long>(j) * nt);
+        g = s_light[j];
+        row0 = s_off[g];
+        row_end = s_off[g + 1];
+        return;
+      }
+      idx -= static_cast<int>(cl);
+    }
     const int mi = idx / nt;  // the group holding tile idx: s_mt[g] * nt <= idx
     int lo = 0, hi = p.num_groups - 1;
     while (lo < hi) {
@@ -148,7 +225,7 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, const int* s_off,
     g = 0;
     const int chunk = idx / (p.swz * nt);
     const int rem = idx - chunk * p.swz * nt;
-    const int cm = min(p.swz, num_mt - chunk * p.swz);
+    const int cm = min(p.swz, sc.num_mt - chunk * p.swz);
     n_tile = rem / cm;
     mt = chunk * p.swz + (rem - n_tile * cm);
     row0 = mt * tile_rows;
@@ -497,6 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* s_off = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(bars) + Cfg::kBarBytes);
   int* s_mt = s_off + kMaxGroups + 4;
   int* s_scan = s_mt + kMaxGroups + 4;
+  int* s_light = s_scan + 32;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t bar0 = smem_u32(bars);
@@ -535,28 +613,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   grid_dep_trigger();
 
   // Ragged schedule: every CTA derives the token tiles of every group from the offsets.
-  int num_mt;
-  if (p.offsets != nullptr) {
-    const int G = p.num_groups;
-    for (int i = threadIdx.x; i <= G; i += blockDim.x) s_off[i] = p.offsets[i];
-    __syncthreads();
-    const int per = (G + blockDim.x - 1) / blockDim.x;
-    const int beg = min(G, static_cast<int>(threadIdx.x) * per), end = min(G, beg + per);
-    int mine = 0;
-    for (int q = beg; q < end; ++q) mine += (s_off[q + 1] - s_off[q] + kTileRows - 1) / kTileRows;
-    int all = 0;
-    int run = block_exclusive_scan(mine, s_scan, &all);
-    for (int q = beg; q < end; ++q) {
-      s_mt[q] = run;
-      run += (s_off[q + 1] - s_off[q] + kTileRows - 1) / kTileRows;
-    }
-    if (threadIdx.x == 0) s_mt[G] = all;
-    __syncthreads();
-    num_mt = all;
-  } else {
-    num_mt = (p.rows_alloc + kTileRows - 1) / kTileRows;
-  }
-  const int total = num_mt * p.n_tiles;
+  const Sched sc = build_schedule(p, s_off, s_mt, s_light, s_scan, kTileRows);
+  const int total = sc.total;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer ----
@@ -575,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int idx = blockIdx.x; idx < total && ok; idx += gridDim.x) {
         int g, row0, row_end, n_tile;
-        decode_tile(p, s_off, s_mt, num_mt, kTileRows, idx, g, row0, row_end, n_tile);
+        decode_tile(p, s_off, s_mt, s_light, sc, kTileRows, idx, g, row0, row_end, n_tile);
         const int n0 = n_tile * Cfg::kColsOut;  // first weight row of the tile
         // With a row gather only the lanes whose four rows start inside the group load
         // anything: the rest of the tile's rows are never stored, so whatever an earlier
@@ -697,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int local = 0;
     for (int idx = blockIdx.x; idx < total; idx += gridDim.x, ++local) {
       int g, row0, row_end, n_tile;
-      decode_tile(p, s_off, s_mt, num_mt, kTileRows, idx, g, row0, row_end, n_tile);
+      decode_tile(p, s_off, s_mt, s_light, sc, kTileRows, idx, g, row0, row_end, n_tile);
       const int acc = local & 1;
       const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
       const bool ready = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.err);
@@ -937,7 +995,7 @@ struct TcPairCfg {
   static constexpr int kTmemCols = 512;
   static constexpr int kStgBytes = kEpiWarps * 32 * (MODE == kSwiGLU ? 64 : 128);
   static constexpr int kBarBytes = 256;
-  static constexpr int kSchedBytes = 2 * (kMaxGroups + 4) * 4 + 32 * 4;
+  static constexpr int kSchedBytes = 3 * (kMaxGroups + 4) * 4 + 32 * 4;
   static constexpr int kSmem = 1024 + kStages * kStageBytes + kStgBytes + kBarBytes + kSchedBytes;
   static_assert(kSmem <= 232448, "shared memory per CTA");
 };
@@ -963,6 +1021,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   int* s_off = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(bars) + Cfg::kBarBytes);
   int* s_mt = s_off + kMaxGroups + 4;
   int* s_scan = s_mt + kMaxGroups + 4;
+  int* s_light = s_scan + 32;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -1005,28 +1064,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   grid_dep_wait();
   grid_dep_trigger();
 
-  int num_mt;
-  if (p.offsets != nullptr) {
-    const int G = p.num_groups;
-    for (int i = threadIdx.x; i <= G; i += blockDim.x) s_off[i] = p.offsets[i];
-    __syncthreads();
-    const int per = (G + blockDim.x - 1) / blockDim.x;
-    const int beg = min(G, static_cast<int>(threadIdx.x) * per), end = min(G, beg + per);
-    int mine = 0;
-    for (int q = beg; q < end; ++q) mine += (s_off[q + 1] - s_off[q] + kTileRows - 1) / kTileRows;
-    int all = 0;
-    int run = block_exclusive_scan(mine, s_scan, &all);
-    for (int q = beg; q < end; ++q) {
-      s_mt[q] = run;
-      run += (s_off[q + 1] - s_off[q] + kTileRows - 1) / kTileRows;
-    }
-    if (threadIdx.x == 0) s_mt[G] = all;
-    __syncthreads();
-    num_mt = all;
-  } else {
-    num_mt = (p.rows_alloc + kTileRows - 1) / kTileRows;
-  }
-  const int total = num_mt * p.n_tiles;
+  const Sched sc = build_schedule(p, s_off, s_mt, s_light, s_scan, kTileRows);
+  const int total = sc.total;
   const int pair = static_cast<int>(blockIdx.x >> 1), npairs = static_cast<int>(gridDim.x >> 1);
 
   if (warp == 0) {
@@ -1038,7 +1077,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int idx = pair; idx < total && ok; idx += npairs) {
         int g, row0, row_end, n_tile;
-        decode_tile(p, s_off, s_mt, num_mt, kTileRows, idx, g, row0, row_end, n_tile);
+        decode_tile(p, s_off, s_mt, s_light, sc, kTileRows, idx, g, row0, row_end, n_tile);
         const int n0 = n_tile * Cfg::kColsOut;
         const int a_row = row0 + static_cast<int>(rank) * 128;
         const int b_row = MODE == kSwiGLU ? (rank == 0 ? n0 : p.up_offset + n0)
@@ -1117,7 +1156,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int acc = local & 1;
         const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
         int g, row0, row_end, n_tile;
-        decode_tile(p, s_off, s_mt, num_mt, kTileRows, idx, g, row0, row_end, n_tile);
+        decode_tile(p, s_off, s_mt, s_light, sc, kTileRows, idx, g, row0, row_end, n_tile);
         const int tn = pair_tail_n(row0, row_end);
         const uint32_t idesc_t =
             tn > 0 ? (F8 ? idesc_e4m3_f32(256, tn) : idesc_bf16_f32(256, tn)) : idesc;
@@ -1163,7 +1202,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int local = 0;
     for (int idx = pair; idx < total; idx += npairs, ++local) {
       int g, row0, row_end, n_tile;
-      decode_tile(p, s_off, s_mt, num_mt, kTileRows, idx, g, row0, row_end, n_tile);
+      decode_tile(p, s_off, s_mt, s_light, sc, kTileRows, idx, g, row0, row_end, n_tile);
       const int acc = local & 1;
       const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
       const bool ready = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.err);
@@ -1331,6 +1370,7 @@ cudaError_t launch_one(const GroupedGemm& g, unsigned* err, int num_sms, cudaStr
   p.n_tiles = (g.N_out + Cfg::kColsOut - 1) / Cfg::kColsOut;
   p.up_offset = g.up_offset;
   p.swz = kSwz;
+  p.interleave = (!SWAP && g.offsets != nullptr) ? 1 : 0;
   const long long rows_tiles = (g.rows_alloc + Cfg::kActRows - 1) / Cfg::kActRows;
   const long long max_mt = g.offsets != nullptr ? rows_tiles + g.G : rows_tiles;
   const long long max_tiles = max_mt * p.n_tiles;
@@ -1391,6 +1431,7 @@ cudaError_t launch_pair(const GroupedGemm& g, unsigned* err, int num_sms, cudaSt
   p.n_tiles = (g.N_out + Cfg::kColsOut - 1) / Cfg::kColsOut;
   p.up_offset = g.up_offset;
   p.swz = kSwz;
+  p.interleave = g.offsets != nullptr ? 1 : 0;
   const long long rows_tiles = (g.rows_alloc + 255) / 256;
   const long long max_mt = g.offsets != nullptr ? rows_tiles + g.G : rows_tiles;
   const long long max_tiles = max_mt * p.n_tiles;
