@@ -327,6 +327,9 @@ moe_status_t moe_workspace_views(const moe_config_t* cfg, void* ws, float** logi
 
 /* Synchronise `stream` and report (then clear) the device error word of the current
  * device: MOE_ERR_TIMEOUT if a bounded device-side wait gave up since the last check,
+ * MOE_ERR_INTERNAL if a kernel of the debug build (compiled with -DMOE_DEBUG) found an
+ * index out of range in its inputs (an expert id >= E, group offsets that decrease or
+ * exceed the rows, an inverse-map or gather row out of range) and skipped that access,
  * MOE_ERR_CUDA if the stream reports a CUDA error, MOE_OK otherwise. */
 moe_status_t moe_sync_check(moe_stream_t stream);
 
@@ -337,6 +340,25 @@ moe_status_t moe_sync_check(moe_stream_t stream);
  * device error word, which the next moe_sync_check() reports and clears.  The kernel
  * exits normally, so the CUDA context stays usable.  `done` is an int in device memory. */
 moe_status_t moe_debug_wait_timeout(unsigned limit_us, int* done, moe_stream_t stream);
+
+/* Host-side fault injection, for testing how a caller handles errors (no counterpart on
+ * the pages: section 3.2 of "MoE大模型的智能调度…" recounts production failures of the
+ * routing step, one an out-of-memory crash; this lets a caller rehearse its clean-up
+ * after a failed call without causing a real failure).
+ * Arms one fault: the n-th time (n >= 1, counted from this call) the library passes the
+ * named point, the call returns MOE_ERR_CUDA there, as a failed launch would, and the
+ * fault disarms itself.  point == NULL or n <= 0 disarms.  Returns MOE_ERR_INVALID_ARG
+ * for an unknown point.  The same fault can be armed when the library loads by setting
+ * MOE_FAULT=<point>:<n> in the environment.  Points:
+ *  - every entry point by its own name ("moe_route", "moe_layer_forward", ...,
+ *    "moe_workspace_size", "moe_sync_check"): checked first, before any argument check,
+ *    so nothing is launched and no output is written;
+ *  - the stages inside moe_layer_forward: "moe_layer_forward.route", ".permute",
+ *    ".gate_up", ".shared", ".down", ".combine": checked before that stage's launches, so
+ *    the earlier stages have been enqueued on the stream.  y is then untouched; the
+ *    workspace (and y_f32 with MOE_FLAG_FUSED_COMBINE) may hold partial results.
+ * Thread-safe; the fault is process-wide.  No GPU state is involved. */
+moe_status_t moe_debug_set_fault(const char* point, int n);
 
 /* Number of kernels this library has launched in this process, on every device: each
  * launch the CUDA runtime accepted counts once.  A launch issued while a stream is being

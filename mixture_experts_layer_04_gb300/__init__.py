@@ -59,8 +59,10 @@ class MoEConfig(ctypes.Structure):
                 f"I_shared={self.I_shared}, theta={self.gate_threshold}, dtype={self.dtype})")
 
 
-def library_path() -> str:
-    return os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libmoe_gb300.so")
+def library_path(debug: bool = False) -> str:
+    """The release library, or with ``debug`` the bounds-checking build (-DMOE_DEBUG)."""
+    return os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                        "_build_debug" if debug else "_build", "libmoe_gb300.so")
 
 
 _LIB: Optional[ctypes.CDLL] = None
@@ -89,6 +91,7 @@ _SIGS = {
     "moe_status_string": [ctypes.c_int],
     "moe_version": [],
     "moe_kernel_launch_count": [],
+    "moe_debug_set_fault": [ctypes.c_char_p, ctypes.c_int],
 }
 
 
@@ -101,14 +104,27 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     if not os.path.exists(path):
         raise RuntimeError(f"libmoe_gb300.so not built ({path}); run "
                            "`python -c 'import __graft_entry__ as g; g.build()'` first")
+    _LIB = _open(path)
+    return _LIB
+
+
+def _open(path: str) -> ctypes.CDLL:
     lib = ctypes.CDLL(path)
     for name, args in _SIGS.items():
         fn = getattr(lib, name)
         fn.argtypes = args
         fn.restype = (ctypes.c_char_p if name in ("moe_status_string", "moe_version") else
                       ctypes.c_ulonglong if name == "moe_kernel_launch_count" else ctypes.c_int)
-    _LIB = lib
     return lib
+
+
+def load_debug() -> ctypes.CDLL:
+    """A handle on the bounds-checking build (``build.build(debug=True)``), separate from
+    the release library that ``load()`` returns; raises if it is not built."""
+    path = library_path(debug=True)
+    if not os.path.exists(path):
+        raise RuntimeError(f"debug build of libmoe_gb300.so missing ({path})")
+    return _open(path)
 
 
 def _ptr(t) -> Optional[int]:
@@ -144,6 +160,13 @@ def version() -> str:
 def kernel_launch_count() -> int:
     """Kernels the library has launched in this process (moe_kernel_launch_count)."""
     return int(load().moe_kernel_launch_count())
+
+
+def debug_set_fault(point: Optional[str], n: int = 1) -> None:
+    """Arm (or with point None, disarm) the host-side fault injector: the n-th pass through
+    `point` returns MOE_ERR_CUDA (moe_debug_set_fault)."""
+    _check(load().moe_debug_set_fault(point.encode() if point else None, int(n)),
+           "moe_debug_set_fault")
 
 
 def workspace_size(cfg: MoEConfig) -> int:

@@ -1,8 +1,10 @@
 // C ABI of the MoE layer (include/moe.h): argument validation, the workspace plan and
 // the order of launches.  Every check happens on the host before the first launch; the
 // library never allocates, frees or synchronises on the compute paths.
+#include <atomic>
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <initializer_list>
 #include <mutex>
@@ -329,6 +331,7 @@ moe_status_t run_down_scatter(const moe_config_t* c, const DeviceInfo* d, const 
   g.offsets = gr.offsets;
   g.row_token = perm;
   g.row_w = row_w;
+  g.c_rows = c->T;
   return launch_gemm(c, d, g, s);
 }
 
@@ -345,7 +348,8 @@ moe_status_t routed_groups(const moe_config_t* c, const int32_t* offsets, void* 
     gr.num_mt = at<int32_t>(ws, p.num_mt);
     gr.max_mt = max_mtiles(c->T, c->K, c->E, kF32TileRows);
     if (!table_ready)
-      MOE_CUDA(launch_build_mtile_table(offsets, c->E, kF32TileRows, const_cast<int4*>(gr.table),
+      MOE_CUDA(launch_build_mtile_table(offsets, c->E, c->T * c->K, kF32TileRows,
+                                        const_cast<int4*>(gr.table),
                                         const_cast<int32_t*>(gr.num_mt), s));
   }
   *out = gr;
@@ -383,6 +387,97 @@ __global__ void wait_timeout_probe_kernel(unsigned* err, unsigned long long limi
 
 std::atomic<unsigned long long> g_kernel_launches{0};
 
+unsigned* device_error_word() {
+  const DeviceInfo* d = device_info();
+  return d != nullptr ? d->err : nullptr;
+}
+
+// ------------------------------------------------------------- fault injection ----
+// A one-shot host-side fault for testing callers' error handling: once armed (by
+// moe_debug_set_fault, or by MOE_FAULT=<point>:<n> in the environment when the library
+// loads), the n-th pass through the named point returns MOE_ERR_CUDA there, as a failed
+// launch would, and disarms.  Unarmed, a point costs one relaxed atomic load.
+namespace {
+
+const char* const kFaultPoints[] = {
+    "moe_workspace_size",      "moe_route",                 "moe_permute",
+    "moe_permute_noalloc",     "moe_grouped_ffn",           "moe_expert_gate_up",
+    "moe_expert_gate_up_gather", "moe_expert_down",         "moe_quantize_fp8",
+    "moe_expert_gate_up_fp8",  "moe_expert_down_fp8",       "moe_combine",
+    "moe_layer_forward",       "moe_layer_forward_fp8",     "moe_sync_check",
+    "moe_layer_forward.route", "moe_layer_forward.permute", "moe_layer_forward.gate_up",
+    "moe_layer_forward.shared", "moe_layer_forward.down",   "moe_layer_forward.combine"};
+
+struct Fault {
+  std::mutex mu;
+  std::atomic<bool> armed{false};
+  char point[64] = {0};
+  long long n = 0;
+  long long seen = 0;
+};
+
+Fault& fault() {
+  static Fault f;
+  return f;
+}
+
+bool known_fault_point(const char* name) {
+  for (const char* q : kFaultPoints)
+    if (std::strcmp(q, name) == 0) return true;
+  return false;
+}
+
+moe_status_t arm_fault(const char* point, long long n) {
+  Fault& f = fault();
+  std::lock_guard<std::mutex> lock(f.mu);
+  if (point == nullptr || n <= 0) {
+    f.armed.store(false);
+    f.point[0] = 0;
+    f.n = f.seen = 0;
+    return MOE_OK;
+  }
+  if (!known_fault_point(point)) return MOE_ERR_INVALID_ARG;
+  std::snprintf(f.point, sizeof(f.point), "%s", point);
+  f.n = n;
+  f.seen = 0;
+  f.armed.store(true);
+  return MOE_OK;
+}
+
+// MOE_FAULT=<point>:<n> arms the injector when the library is loaded.
+struct FaultFromEnvironment {
+  FaultFromEnvironment() {
+    const char* e = std::getenv("MOE_FAULT");
+    if (e == nullptr || *e == 0) return;
+    const char* colon = std::strrchr(e, ':');
+    char point[64] = {0};
+    char* end = nullptr;
+    const long long n = colon != nullptr ? std::strtoll(colon + 1, &end, 10) : 0;
+    const size_t len = colon != nullptr ? static_cast<size_t>(colon - e) : 0;
+    if (colon == nullptr || len == 0 || len >= sizeof(point) || end == colon + 1 || *end != 0 ||
+        n <= 0) {
+      std::fprintf(stderr, "moe_gb300: MOE_FAULT=%s ignored (expected <point>:<n>, n >= 1)\n", e);
+      return;
+    }
+    std::memcpy(point, e, len);
+    if (arm_fault(point, n) != MOE_OK)
+      std::fprintf(stderr, "moe_gb300: MOE_FAULT=%s ignored (unknown point)\n", e);
+  }
+};
+FaultFromEnvironment g_fault_from_environment;
+
+}  // namespace
+
+moe_status_t fault_point(const char* name) {
+  Fault& f = fault();
+  if (!f.armed.load(std::memory_order_relaxed)) return MOE_OK;
+  std::lock_guard<std::mutex> lock(f.mu);
+  if (!f.armed.load() || std::strcmp(f.point, name) != 0) return MOE_OK;
+  if (++f.seen < f.n) return MOE_OK;
+  f.armed.store(false);
+  return MOE_ERR_CUDA;
+}
+
 moe_status_t check_current_device() {
   const DeviceInfo* d = nullptr;
   return check_device(&d);
@@ -411,6 +506,7 @@ const char* moe_status_string(moe_status_t s) {
 const char* moe_version(void) { return "moe_gb300 0.1 sm_103a"; }
 
 moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes) {
+  MOE_TRY(fault_point("moe_workspace_size"));
   MOE_TRY(check_config(cfg));
   if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
   *bytes = make_plan(cfg).total;
@@ -440,6 +536,7 @@ moe_status_t moe_workspace_views(const moe_config_t* cfg, void* ws, float** logi
 moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* w_router,
                        const float* router_bias, float* logits, int32_t* topk_ids, float* topk_w,
                        moe_stream_t stream) {
+  MOE_TRY(fault_point("moe_route"));
   MOE_TRY(check_config(cfg));
   if (cfg->T == 0) return MOE_OK;
   if (logits == nullptr || topk_ids == nullptr || topk_w == nullptr) return MOE_ERR_INVALID_ARG;
@@ -463,6 +560,7 @@ moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* w_rou
 moe_status_t moe_permute(const moe_config_t* cfg, const void* x, const int32_t* topk_ids,
                          int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
                          void* x_perm, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(fault_point("moe_permute"));
   MOE_TRY(check_config(cfg));
   if (cfg->T == 0) return MOE_OK;
   if (x == nullptr || topk_ids == nullptr || counts == nullptr || offsets == nullptr ||
@@ -486,6 +584,7 @@ moe_status_t moe_permute(const moe_config_t* cfg, const void* x, const int32_t* 
 moe_status_t moe_grouped_ffn(const moe_config_t* cfg, const void* x_perm, const int32_t* offsets,
                              const void* w_gate_up, const void* w_down, float* out_perm, void* ws,
                              size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(fault_point("moe_grouped_ffn"));
   MOE_TRY(check_config(cfg));
   if (cfg->T == 0) return MOE_OK;
   if (x_perm == nullptr || offsets == nullptr || w_gate_up == nullptr || w_down == nullptr ||
@@ -509,6 +608,7 @@ moe_status_t moe_grouped_ffn(const moe_config_t* cfg, const void* x_perm, const 
 moe_status_t moe_expert_gate_up(const moe_config_t* cfg, const void* x_perm,
                                 const int32_t* offsets, const void* w_gate_up, void* h, void* ws,
                                 size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(fault_point("moe_expert_gate_up"));
   MOE_TRY(check_config(cfg));
   if (cfg->T == 0) return MOE_OK;
   if (x_perm == nullptr || offsets == nullptr || w_gate_up == nullptr || h == nullptr)
@@ -527,6 +627,7 @@ moe_status_t moe_expert_gate_up(const moe_config_t* cfg, const void* x_perm,
 
 moe_status_t moe_quantize_fp8(const void* in, int64_t rows, int32_t cols, uint8_t* codes,
                               float* scales, moe_stream_t stream) {
+  MOE_TRY(fault_point("moe_quantize_fp8"));
   if (rows < 0 || cols <= 0 || cols % 8 != 0) return MOE_ERR_INVALID_ARG;
   if (rows == 0) return MOE_OK;
   if (in == nullptr || codes == nullptr || scales == nullptr) return MOE_ERR_INVALID_ARG;
@@ -541,6 +642,7 @@ moe_status_t moe_expert_gate_up_fp8(const moe_config_t* cfg, const uint8_t* x_co
                                     const float* x_scales, const int32_t* offsets,
                                     const uint8_t* w_codes, const float* w_scales, void* h,
                                     void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(fault_point("moe_expert_gate_up_fp8"));
   MOE_TRY(check_config(cfg));
   if (cfg->T == 0) return MOE_OK;
   if (cfg->dtype != MOE_BF16 || cfg->H % 128 != 0) return MOE_ERR_UNSUPPORTED;
@@ -575,6 +677,7 @@ moe_status_t moe_expert_down_fp8(const moe_config_t* cfg, const uint8_t* h_codes
                                  const float* h_scales, const int32_t* offsets,
                                  const uint8_t* w_codes, const float* w_scales, float* out_perm,
                                  void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(fault_point("moe_expert_down_fp8"));
   MOE_TRY(check_config(cfg));
   if (cfg->T == 0) return MOE_OK;
   if (cfg->dtype != MOE_BF16 || cfg->I % 128 != 0) return MOE_ERR_UNSUPPORTED;
@@ -608,6 +711,7 @@ moe_status_t moe_expert_gate_up_gather(const moe_config_t* cfg, const void* x,
                                        const int32_t* perm, const int32_t* offsets,
                                        const void* w_gate_up, void* h, void* ws, size_t ws_bytes,
                                        moe_stream_t stream) {
+  MOE_TRY(fault_point("moe_expert_gate_up_gather"));
   MOE_TRY(check_config(cfg));
   if (cfg->T == 0) return MOE_OK;
   if (x == nullptr || perm == nullptr || offsets == nullptr || w_gate_up == nullptr ||
@@ -628,6 +732,7 @@ moe_status_t moe_expert_gate_up_gather(const moe_config_t* cfg, const void* x,
 moe_status_t moe_expert_down(const moe_config_t* cfg, const void* h, const int32_t* offsets,
                              const void* w_down, float* out_perm, void* ws, size_t ws_bytes,
                              moe_stream_t stream) {
+  MOE_TRY(fault_point("moe_expert_down"));
   MOE_TRY(check_config(cfg));
   if (cfg->T == 0) return MOE_OK;
   if (h == nullptr || offsets == nullptr || w_down == nullptr || out_perm == nullptr)
@@ -647,6 +752,7 @@ moe_status_t moe_expert_down(const moe_config_t* cfg, const void* h, const int32
 moe_status_t moe_combine(const moe_config_t* cfg, const float* out_perm, const int32_t* inv,
                          const float* topk_w, const float* shared_out, void* y, float* y_f32,
                          moe_stream_t stream) {
+  MOE_TRY(fault_point("moe_combine"));
   MOE_TRY(check_config(cfg));
   if (cfg->T == 0) return MOE_OK;
   if (out_perm == nullptr || inv == nullptr || topk_w == nullptr || y == nullptr)
@@ -668,6 +774,7 @@ moe_status_t moe_layer_forward_fp8(const moe_config_t* cfg, const void* x, const
                                    const float* w_down_scales, const void* w_shared_gate_up,
                                    const void* w_shared_down, void* y, float* y_f32, void* ws,
                                    size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(fault_point("moe_layer_forward_fp8"));
   MOE_TRY(check_config(cfg));
   if ((cfg->flags & MOE_FLAG_FP8) == 0u) return MOE_ERR_INVALID_ARG;
   if (cfg->T == 0) return MOE_OK;
@@ -768,6 +875,7 @@ moe_status_t moe_layer_forward_fp8(const moe_config_t* cfg, const void* x, const
     gd.C = y32;
     gd.row_token = perm;
     gd.row_w = row_w;
+    gd.c_rows = T;
     gd.pair = use_pairs(gd) ? 1 : 0;
     MOE_CUDA(launch_down_fp8(gd, h_scales, w_down_scales, d->err, d->num_sms, s));
     return cuda_status(launch_finalize(cfg->dtype, y32, y, static_cast<long long>(T) * H, s));
@@ -792,6 +900,7 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
                                const void* w_down, const void* w_shared_gate_up,
                                const void* w_shared_down, void* y, float* y_f32, void* ws,
                                size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(fault_point("moe_layer_forward"));
   MOE_TRY(check_config(cfg));
   if ((cfg->flags & MOE_FLAG_FP8) != 0u) return MOE_ERR_INVALID_ARG;  // moe_layer_forward_fp8
   if (cfg->T == 0) return MOE_OK;
@@ -844,7 +953,9 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
   const bool cluster =
       !capacity && route_cluster_ok(cfg->dtype, cfg->T, cfg->H, cfg->E, cfg->K);
   const bool gather = cluster && cfg->T <= kGatherMaxTokens;
+  MOE_TRY(fault_point("moe_layer_forward.route"));
   if (cluster) {
+    MOE_TRY(fault_point("moe_layer_forward.permute"));  // the cluster launch dispatches too
     MOE_CUDA(launch_route_cluster(x, w_router, router_bias, logits, ids, w, cfg->gate_threshold,
                                   cfg->T, cfg->H, cfg->E, cfg->K, counts, offsets, perm, inv,
                                   row_w, gather ? nullptr : x_perm, d->err, s));
@@ -856,6 +967,7 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
     if (capacity)
       MOE_CUDA(launch_capacity_route(logits, ids, w, cfg->T, cfg->E, cfg->K, cfg->gate_threshold,
                                      capacity_limit(cfg->T, cfg->K, cfg->E), d->err, s));
+    MOE_TRY(fault_point("moe_layer_forward.permute"));
     if (deferred > 0) {
       MOE_CUDA(launch_topk_permute_small(partial, deferred, router_bias, logits, ids, w,
                                          cfg->gate_threshold, cfg->dtype, x, cfg->T, cfg->H,
@@ -874,6 +986,7 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
   MOE_TRY(routed_groups(cfg, offsets, ws, p, true, s, &gr));
   void* h = at<void>(ws, p.h);
   const int rows = cfg->T * cfg->K;
+  MOE_TRY(fault_point("moe_layer_forward.gate_up"));
   if (gather)
     MOE_TRY(run_gate_up(cfg, d, x, rows, w_gate_up, cfg->I, h, gr, s, perm));
   else
@@ -883,6 +996,7 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
     //     down projection adds every routed row, scaled by its gate, into its token's row,
     //     and one pass rounds the sum to the output type
     float* y32 = y_f32 != nullptr ? y_f32 : at<float>(ws, p.y32);
+    MOE_TRY(fault_point("moe_layer_forward.shared"));
     if (shared) {
       Groups one{};
       one.G = 1;
@@ -892,14 +1006,18 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
     } else {
       MOE_CUDA(cudaMemsetAsync(y32, 0, static_cast<size_t>(cfg->T) * cfg->H * sizeof(float), s));
     }
+    MOE_TRY(fault_point("moe_layer_forward.down"));
     MOE_TRY(run_down_scatter(cfg, d, h, rows, w_down, cfg->I, y32, gr, perm,
                              at<float>(ws, p.row_w), s));
+    MOE_TRY(fault_point("moe_layer_forward.combine"));
     return cuda_status(
         launch_finalize(cfg->dtype, y32, y, static_cast<long long>(cfg->T) * cfg->H, s));
   }
+  MOE_TRY(fault_point("moe_layer_forward.down"));
   MOE_TRY(run_down(cfg, d, h, rows, w_down, cfg->I, out_perm, gr, s));
   // 5. shared expert: the same engine on all T rows of x as one group
   float* shared_out = nullptr;
+  MOE_TRY(fault_point("moe_layer_forward.shared"));
   if (shared) {
     shared_out = at<float>(ws, p.shared_out);
     Groups one{};
@@ -909,6 +1027,7 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
     MOE_TRY(run_down(cfg, d, hs, cfg->T, w_shared_down, cfg->I_shared, shared_out, one, s));
   }
   // 6. un-permute and weighted combine
+  MOE_TRY(fault_point("moe_layer_forward.combine"));
   return cuda_status(launch_combine(cfg->dtype, out_perm, inv, w, shared_out, y, y_f32, cfg->T,
                                     cfg->H, cfg->K, s));
 }
@@ -923,11 +1042,16 @@ moe_status_t moe_debug_wait_timeout(unsigned limit_us, int* done, moe_stream_t s
   return cuda_status(count_launch(cudaGetLastError()));
 }
 
+moe_status_t moe_debug_set_fault(const char* point, int n) {
+  return arm_fault(point, static_cast<long long>(n));
+}
+
 unsigned long long moe_kernel_launch_count(void) {
   return moe::g_kernel_launches.load(std::memory_order_relaxed);
 }
 
 moe_status_t moe_sync_check(moe_stream_t stream) {
+  MOE_TRY(fault_point("moe_sync_check"));
   const DeviceInfo* d = device_info();
   if (d == nullptr) return MOE_ERR_CUDA;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;

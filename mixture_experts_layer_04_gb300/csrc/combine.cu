@@ -32,14 +32,17 @@ template <typename TOut>
 __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(const float* __restrict__ out_perm, const int32_t* __restrict__ inv,
                    const float* __restrict__ w, const float* __restrict__ shared_out,
-                   TOut* __restrict__ y, float* __restrict__ y_f32, int H, int K) {
+                   TOut* __restrict__ y, float* __restrict__ y_f32, int H, int K,
+                   unsigned* __restrict__ err) {
   __shared__ int rows[kMaxK];
   __shared__ float gates[kMaxK];
   grid_dep_wait();
   grid_dep_trigger();
   const int t = blockIdx.x;
   if (threadIdx.x < K) {
-    rows[threadIdx.x] = inv[static_cast<size_t>(t) * K + threadIdx.x];
+    // the grid has one x-block per token, so the rows of out_perm number gridDim.x * K
+    const int r = inv[static_cast<size_t>(t) * K + threadIdx.x];
+    rows[threadIdx.x] = dcheck(r < static_cast<int>(gridDim.x) * K, err) ? r : -1;
     gates[threadIdx.x] = w[static_cast<size_t>(t) * K + threadIdx.x];
   }
   __syncthreads();
@@ -77,14 +80,17 @@ template <typename TOut>
 __global__ void __launch_bounds__(kCombineThreads)
     combine_split_kernel(const float* __restrict__ out_perm, const int32_t* __restrict__ inv,
                          const float* __restrict__ w, const float* __restrict__ shared_out,
-                         TOut* __restrict__ y, float* __restrict__ y_f32, int H, int K) {
+                         TOut* __restrict__ y, float* __restrict__ y_f32, int H, int K,
+                         unsigned* __restrict__ err) {
   __shared__ int rows[kMaxK];
   __shared__ float gates[kMaxK];
   grid_dep_wait();
   grid_dep_trigger();
   const int t = blockIdx.x;
   if (threadIdx.x < K) {
-    rows[threadIdx.x] = inv[static_cast<size_t>(t) * K + threadIdx.x];
+    // the grid has one x-block per token, so the rows of out_perm number gridDim.x * K
+    const int r = inv[static_cast<size_t>(t) * K + threadIdx.x];
+    rows[threadIdx.x] = dcheck(r < static_cast<int>(gridDim.x) * K, err) ? r : -1;
     gates[threadIdx.x] = w[static_cast<size_t>(t) * K + threadIdx.x];
   }
   __syncthreads();
@@ -151,15 +157,19 @@ cudaError_t launch_combine(int dtype, const float* out_perm, const int32_t* inv,
     const dim3 grid(T, (H / 4 + kCombineThreads - 1) / kCombineThreads);
     if (dtype == kBF16)
       return launch_pdl(combine_split_kernel<__nv_bfloat16>, grid, dim3(kCombineThreads), 0, s,
-                        out_perm, inv, w, shared_out, static_cast<__nv_bfloat16*>(y), y_f32, H, K);
+                        out_perm, inv, w, shared_out, static_cast<__nv_bfloat16*>(y), y_f32, H, K,
+                      device_error_word());
     return launch_pdl(combine_split_kernel<float>, grid, dim3(kCombineThreads), 0, s, out_perm,
-                      inv, w, shared_out, static_cast<float*>(y), y_f32, H, K);
+                      inv, w, shared_out, static_cast<float*>(y), y_f32, H, K,
+                      device_error_word());
   }
   if (dtype == kBF16)
     return launch_pdl(combine_kernel<__nv_bfloat16>, dim3(T), dim3(kCombineThreads), 0, s,
-                      out_perm, inv, w, shared_out, static_cast<__nv_bfloat16*>(y), y_f32, H, K);
+                      out_perm, inv, w, shared_out, static_cast<__nv_bfloat16*>(y), y_f32, H, K,
+                      device_error_word());
   return launch_pdl(combine_kernel<float>, dim3(T), dim3(kCombineThreads), 0, s, out_perm, inv, w,
-                    shared_out, static_cast<float*>(y), y_f32, H, K);
+                    shared_out, static_cast<float*>(y), y_f32, H, K,
+                      device_error_word());
 }
 
 }  // namespace moe

@@ -30,6 +30,23 @@ __device__ __forceinline__ void report_error(unsigned* err, unsigned bit) {
   if (err != nullptr) atomicOr(err, bit);
 }
 
+// Debug bounds checks.  A library built with -DMOE_DEBUG checks the indices its kernels
+// take from their inputs (expert ids, group offsets, row maps) before using them:
+// dcheck(ok, err) records MOE_DEVERR_BOUNDS in the error word when `ok` is false and
+// returns `ok`, and the caller then skips the access (no trap, the kernel carries on).
+// moe_sync_check() reports the bit as MOE_ERR_INTERNAL.  In the normal build dcheck is the
+// constant true and every check compiles away.
+__device__ __forceinline__ bool dcheck(bool ok, unsigned* err) {
+#ifdef MOE_DEBUG
+  if (!ok) report_error(err, MOE_DEVERR_BOUNDS);
+  return ok;
+#else
+  (void)ok;
+  (void)err;
+  return true;
+#endif
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

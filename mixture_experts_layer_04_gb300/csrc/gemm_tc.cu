@@ -92,6 +92,8 @@ struct TcParams {
   // grouped launches in the normal operand order: interleave the tiles of groups that
   // have a single token tile with the tiles of the larger groups (see build_schedule)
   int interleave;
+  int a_rows;  // rows of the tensor behind tmAct (the gather's source rows with a row gather)
+  int c_rows;  // kScatter: rows of C, 0 = unknown (both checked in the debug build only)
 };
 
 template <int BN, int MODE, bool SWAP>
@@ -150,6 +152,18 @@ __device__ __forceinline__ Sched build_schedule(const TcParams& p, int* s_off, i
   const int G = p.num_groups;
   for (int i = threadIdx.x; i <= G; i += blockDim.x) s_off[i] = p.offsets[i];
   __syncthreads();
+#ifdef MOE_DEBUG
+  // the offsets must be non-decreasing within [0, rows_alloc]: otherwise the launch does
+  // nothing (every CTA sees the same offsets and takes the same decision)
+  bool bad = threadIdx.x == 0 && (s_off[0] < 0 || s_off[G] > p.rows_alloc);
+  for (int q = threadIdx.x; q < G; q += blockDim.x) bad = bad || s_off[q] > s_off[q + 1];
+  if (__syncthreads_or(bad)) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) report_error(p.err, MOE_DEVERR_BOUNDS);
+    sc.num_mt = 0;
+    sc.total = 0;
+    return sc;
+  }
+#endif
   const int per = (G + blockDim.x - 1) / blockDim.x;
   const int beg = min(G, static_cast<int>(threadIdx.x) * per), end = min(G, beg + per);
   auto tiles_of = [&](int q) { return (s_off[q + 1] - s_off[q] + tile_rows - 1) / tile_rows; };
@@ -418,7 +432,8 @@ __device__ __forceinline__ void epilogue_rows(const TcParams& p, uint32_t t_row,
         if (grow < row_end && col < p.N_out) {
           if constexpr (MODE == kScatter) {
             const int tok = __ldg(p.row_token + grow);
-            red_add_v4(C + static_cast<size_t>(tok) * p.N_out + col, v);
+            if (dcheck(tok >= 0 && (p.c_rows == 0 || tok < p.c_rows), p.err))
+              red_add_v4(C + static_cast<size_t>(tok) * p.N_out + col, v);
           } else {
             *reinterpret_cast<uint4*>(C + static_cast<size_t>(grow) * p.N_out + col) = v;
           }
@@ -650,6 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 4; ++i) {
             const int r = row0 + 4 * lane + i;
             src[i] = r < row_end ? p.gather_rows[r] : pad;
+            if (!dcheck(src[i] >= 0 && src[i] < p.a_rows, p.err)) src[i] = 0;
           }
         }
         for (int kb = 0; kb < p.num_kb; ++kb) {
@@ -863,8 +879,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (row < row_end && col < p.N_out) {
                 if constexpr (MODE == kScatter) {
                   const int tok = __ldg(p.row_token + row);
-                  red_add_f32(C + static_cast<size_t>(tok) * p.N_out + col,
-                              __ldg(p.row_w + row) * v[j]);
+                  if (dcheck(tok >= 0 && (p.c_rows == 0 || tok < p.c_rows), p.err))
+                    red_add_f32(C + static_cast<size_t>(tok) * p.N_out + col,
+                                __ldg(p.row_w + row) * v[j]);
                 } else {
                   C[static_cast<size_t>(row) * p.N_out + col] = v[j] + b;
                 }
@@ -973,8 +990,10 @@ __device__ __forceinline__ void epilogue_pair_tail(const TcParams& p, uint32_t t
         const int tok = row0 + c + j;
         if (tok < row_end && col < p.N_out) {
           if constexpr (MODE == kScatter) {
-            red_add_f32(C + static_cast<size_t>(__ldg(p.row_token + tok)) * p.N_out + col,
-                        __ldg(p.row_w + tok) * v[j]);
+            const int dst = __ldg(p.row_token + tok);
+            if (dcheck(dst >= 0 && (p.c_rows == 0 || dst < p.c_rows), p.err))
+              red_add_f32(C + static_cast<size_t>(dst) * p.N_out + col,
+                          __ldg(p.row_w + tok) * v[j]);
           } else {
             C[static_cast<size_t>(tok) * p.N_out + col] = v[j] + b;
           }
@@ -1371,6 +1390,8 @@ cudaError_t launch_one(const GroupedGemm& g, unsigned* err, int num_sms, cudaStr
   p.up_offset = g.up_offset;
   p.swz = kSwz;
   p.interleave = (!SWAP && g.offsets != nullptr) ? 1 : 0;
+  p.a_rows = GATHER ? g.src_rows : g.rows_alloc;
+  p.c_rows = g.c_rows;
   const long long rows_tiles = (g.rows_alloc + Cfg::kActRows - 1) / Cfg::kActRows;
   const long long max_mt = g.offsets != nullptr ? rows_tiles + g.G : rows_tiles;
   const long long max_tiles = max_mt * p.n_tiles;
@@ -1432,6 +1453,8 @@ cudaError_t launch_pair(const GroupedGemm& g, unsigned* err, int num_sms, cudaSt
   p.up_offset = g.up_offset;
   p.swz = kSwz;
   p.interleave = g.offsets != nullptr ? 1 : 0;
+  p.a_rows = g.rows_alloc;
+  p.c_rows = g.c_rows;
   const long long rows_tiles = (g.rows_alloc + 255) / 256;
   const long long max_mt = g.offsets != nullptr ? rows_tiles + g.G : rows_tiles;
   const long long max_tiles = max_mt * p.n_tiles;

@@ -98,6 +98,15 @@ cudaError_t launch_topk(const float* partial, int S, const float* bias, float* l
 // Workspace (int32 words) the permutation needs for T tokens, E experts.
 size_t permute_ws_words(int T, int E);
 
+// Device address of the current device's error word (MOE_DEVERR_* bits, reported by
+// moe_sync_check), or null when the device cannot be set up.  Launchers pass it to kernels
+// that check indices in the debug build.
+unsigned* device_error_word();
+
+// Host-side fault injection (moe_debug_set_fault, MOE_FAULT): MOE_ERR_CUDA when the armed
+// fault is due at the named point, else MOE_OK.
+moe_status_t fault_point(const char* name);
+
 // MOE_OK when the current device is an sm_103 GPU this library runs on (the same check
 // every entry point makes), MOE_ERR_UNSUPPORTED when it is not, MOE_ERR_CUDA when the
 // device cannot be queried.
@@ -129,8 +138,9 @@ cudaError_t launch_topk_permute_small(const float* partial, int S, const float* 
                                       int32_t* num_mtiles, int bm, float* row_w, cudaStream_t s);
 
 // The m-tile table of a grouped GEMM from offsets alone.
-cudaError_t launch_build_mtile_table(const int32_t* offsets, int E, int bm, int4* table,
-                                     int32_t* num_mtiles, cudaStream_t s);
+// `rows`: rows of the grouped matrix (offsets[E] must not exceed it).
+cudaError_t launch_build_mtile_table(const int32_t* offsets, int E, int rows, int bm,
+                                     int4* table, int32_t* num_mtiles, cudaStream_t s);
 
 // ----------------------------------------------------------------- combine ----
 // y = act(y_f32) elementwise (the last step of the fused combine).
@@ -178,6 +188,7 @@ struct GroupedGemm {
   int swap_tokens;
   const int32_t* row_token;  // kScatter only
   const float* row_w;        // kScatter only
+  int c_rows;                // kScatter: rows of C (checked in the debug build; 0 = unknown)
   // Tensor-core engine, normal order only: run on CTA pairs (cta_group::2, 256-row tiles)
   int pair;
   // Tensor-core engine, single CTAs: row r of the (grouped) A is row gather_rows[r] of the

@@ -29,7 +29,8 @@ constexpr int kScanThreads = 1024;
 
 __global__ void __launch_bounds__(kRankTokens)
     permute_rank_kernel(const int32_t* __restrict__ ids, int T, int E, int K,
-                        int32_t* __restrict__ rank_out, int32_t* __restrict__ block_counts) {
+                        int32_t* __restrict__ rank_out, int32_t* __restrict__ block_counts,
+                        unsigned* __restrict__ err) {
   extern __shared__ uint32_t masks[];  // [8][E]
   grid_dep_wait();
   grid_dep_trigger();
@@ -40,7 +41,7 @@ __global__ void __launch_bounds__(kRankTokens)
   if (t < T) {
     for (int k = 0; k < K; ++k) {
       const int e = ids[static_cast<size_t>(t) * K + k];
-      if (e >= 0) atomicOr(&masks[warp * E + e], 1u << lane);
+      if (e >= 0 && dcheck(e < E, err)) atomicOr(&masks[warp * E + e], 1u << lane);
     }
   }
   __syncthreads();
@@ -49,7 +50,7 @@ __global__ void __launch_bounds__(kRankTokens)
     for (int k = 0; k < K; ++k) {
       const int e = ids[static_cast<size_t>(t) * K + k];
       int r = -1;
-      if (e >= 0) {
+      if (e >= 0 && dcheck(e < E, nullptr)) {
         r = __popc(masks[warp * E + e] & lower);
         for (int w = 0; w < warp; ++w) r += __popc(masks[w * E + e]);
       }
@@ -121,14 +122,29 @@ __global__ void __launch_bounds__(kScanThreads)
 }
 
 __global__ void __launch_bounds__(kScanThreads)
-    mtile_table_kernel(const int32_t* __restrict__ offsets, int E, int4* __restrict__ table,
-                       int32_t* __restrict__ num_mtiles, int bm) {
+    mtile_table_kernel(const int32_t* __restrict__ offsets, int E, int rows,
+                       int4* __restrict__ table, int32_t* __restrict__ num_mtiles, int bm,
+                       unsigned* __restrict__ err) {
   __shared__ int scratch[32];
   grid_dep_wait();
   grid_dep_trigger();
   const int e = threadIdx.x;
   const int base = e < E ? offsets[e] : 0;
   const int count = e < E ? offsets[e + 1] - base : 0;
+#ifdef MOE_DEBUG
+  // offsets must be non-decreasing within [0, rows]: otherwise no tile is emitted
+  const bool bad = e < E && (base < 0 || count < 0 || base + count > rows);
+  if (__syncthreads_or(bad)) {
+    if (e == 0) {
+      report_error(err, MOE_DEVERR_BOUNDS);
+      *num_mtiles = 0;
+    }
+    return;
+  }
+#else
+  (void)rows;
+  (void)err;
+#endif
   const int nt = (count + bm - 1) / bm;
   int all = 0;
   const int first = block_exclusive_scan(nt, scratch, &all);
@@ -152,7 +168,7 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
   int row = -1;
   if (lane < K) {
     const int e = ids[static_cast<size_t>(t) * K + lane];
-    if (e >= 0) {
+    if (e >= 0 && dcheck(e < E, nullptr)) {  // an id out of range was reported by the rank pass
       const int b = t / kRankTokens;
       row = block_base[static_cast<size_t>(b) * E + e] + inv[static_cast<size_t>(t) * K + lane];
       inv[static_cast<size_t>(t) * K + lane] = row;
@@ -212,7 +228,8 @@ __global__ void __launch_bounds__(kSmallThreads)
                          int32_t* __restrict__ inv, const uint4* __restrict__ x,
                          uint4* __restrict__ x_perm, int4* __restrict__ mtile_table,
                          int32_t* __restrict__ num_mtiles, int bm,
-                         const float* __restrict__ gate_w, float* __restrict__ row_w) {
+                         const float* __restrict__ gate_w, float* __restrict__ row_w,
+                         unsigned* __restrict__ err) {
   extern __shared__ uint32_t smem_u[];
   uint32_t* masks = smem_u;                                        // [E][8]
   int* cnt = reinterpret_cast<int*>(masks + E * kSmallMaskWords);  // [E]
@@ -263,7 +280,7 @@ __global__ void __launch_bounds__(kSmallThreads)
   __syncthreads();
   for (int a = tid; a < TK; a += blockDim.x) {
     const int e = ids[a];
-    if (e >= 0) {
+    if (e >= 0 && dcheck(e < E, blockIdx.x == 0 ? err : nullptr)) {
       const int t = a / K;
       atomicOr(&masks[e * kSmallMaskWords + (t >> 5)], 1u << (t & 31));
     }
@@ -285,7 +302,7 @@ __global__ void __launch_bounds__(kSmallThreads)
   for (int a = tid; a < TK; a += blockDim.x) {
     const int e = ids[a];
     int row = -1;
-    if (e >= 0) {
+    if (e >= 0 && dcheck(e < E, nullptr)) {
       const int t = a / K;
       const uint32_t* m = masks + e * kSmallMaskWords;
       int r = __popc(m[t >> 5] & ((1u << (t & 31)) - 1u));
@@ -377,7 +394,7 @@ cudaError_t launch_small_t(int dtype, const void* x, const int32_t* ids, const S
   return launch_pdl(permute_small_kernel<kRoute>, dim3(blocks), dim3(kSmallThreads), smem, s, ids,
                     r, T, E, K, row_units, counts, offsets, perm, inv,
                     static_cast<const uint4*>(x), static_cast<uint4*>(x_perm), mtile_table,
-                    num_mtiles, bm, gate_w, row_w);
+                    num_mtiles, bm, gate_w, row_w, device_error_word());
 }
 
 cudaError_t launch_small(int dtype, const void* x, const int32_t* ids, const SmallRoute* rt,
@@ -425,7 +442,8 @@ cudaError_t launch_permute(int dtype, const void* x, const int32_t* ids, int T, 
   const int nb = (T + kRankTokens - 1) / kRankTokens;
   if (nb > 0) {
     cudaError_t err = launch_pdl(permute_rank_kernel, dim3(nb), dim3(kRankTokens),
-                                 8 * E * sizeof(uint32_t), s, ids, T, E, K, inv, ws_words);
+                                 8 * E * sizeof(uint32_t), s, ids, T, E, K, inv, ws_words,
+                                 device_error_word());
     if (err != cudaSuccess) return err;
   }
   cudaError_t err = launch_pdl(permute_scan_kernel, dim3(1), dim3(kScanThreads), 0, s, ws_words,
@@ -438,10 +456,10 @@ cudaError_t launch_permute(int dtype, const void* x, const int32_t* ids, int T, 
                     static_cast<uint4*>(x_perm), gate_w, row_w);
 }
 
-cudaError_t launch_build_mtile_table(const int32_t* offsets, int E, int bm, int4* table,
-                                     int32_t* num_mtiles, cudaStream_t s) {
-  return launch_pdl(mtile_table_kernel, dim3(1), dim3(kScanThreads), 0, s, offsets, E, table,
-                    num_mtiles, bm);
+cudaError_t launch_build_mtile_table(const int32_t* offsets, int E, int rows, int bm,
+                                     int4* table, int32_t* num_mtiles, cudaStream_t s) {
+  return launch_pdl(mtile_table_kernel, dim3(1), dim3(kScanThreads), 0, s, offsets, E, rows,
+                    table, num_mtiles, bm, device_error_word());
 }
 
 }  // namespace moe

@@ -61,6 +61,8 @@ extern "C" moe_status_t moe_permute_noalloc(const moe_config_t* cfg, const void*
                                             int32_t* offsets, int32_t* perm, int32_t* inv,
                                             void* x_perm, moe_stream_t stream) {
   using namespace moe;
+  const moe_status_t sf = fault_point("moe_permute_noalloc");
+  if (sf != MOE_OK) return sf;
   size_t ignored = 0;
   const moe_status_t st = moe_workspace_size(cfg, &ignored);  // validates cfg on the host
   if (st != MOE_OK) return st;
