@@ -83,7 +83,7 @@ def build(force: bool = False, verbose: bool = False, debug: bool = False) -> st
     newest = max(os.path.getmtime(o) for o in objs)
     if force or not os.path.exists(lib_path) or os.path.getmtime(lib_path) < newest:
         tmp = lib_path + ".tmp"
-        cmd = [nvcc(), GENCODE, "-shared", "-o", tmp, *objs, "-cudart", "static"]
+        cmd = [nvcc(), GENCODE, "-shared", "-o", tmp, *objs, "-cudart", "static", "-ldl"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

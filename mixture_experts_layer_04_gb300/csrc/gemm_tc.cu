@@ -92,6 +92,8 @@ struct TcParams {
   // grouped launches in the normal operand order: interleave the tiles of groups that
   // have a single token tile with the tiles of the larger groups (see build_schedule)
   int interleave;
+  float* zero_ptr;  // cleared by the epilogue warps before the first tile (n floats), or null
+  long long zero_n;
   int a_rows;  // rows of the tensor behind tmAct (the gather's source rows with a row gather)
   int c_rows;  // kScatter: rows of C, 0 = unknown (both checked in the debug build only)
 };
@@ -245,6 +247,20 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, const int* s_off,
     row0 = mt * tile_rows;
     row_end = p.rows_alloc;
   }
+}
+
+// This CTA's share of the array to clear (see TcParams::zero_ptr), by the `nthreads`
+// epilogue threads before they wait for the first accumulator; the writes need no ordering
+// with the rest of this launch, only with later launches.
+__device__ __forceinline__ void clear_share(const TcParams& p, int part, int parts, int t,
+                                            int nthreads) {
+  if (p.zero_ptr == nullptr) return;
+  const long long n4 = p.zero_n / 4;
+  const long long per = (n4 + parts - 1) / parts;
+  const long long beg = per * part;
+  const long long end = beg + per < n4 ? beg + per : n4;
+  float4* q = reinterpret_cast<float4*>(p.zero_ptr);
+  for (long long i = beg + t; i < end; i += nthreads) q[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // Swizzled offset of 16-byte unit u of row r in a per-warp staging buffer.
@@ -768,6 +784,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue ----
     const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
+    clear_share(p, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x),
+                static_cast<int>(threadIdx.x) - 64, 32 * kEpiWarps);
     int local = 0;
     for (int idx = blockIdx.x; idx < total; idx += gridDim.x, ++local) {
       int g, row0, row_end, n_tile;
@@ -1216,6 +1234,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue ----
     const int quad = warp & 3;
+    clear_share(p, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x),
+                static_cast<int>(threadIdx.x) - 64, 32 * kEpiWarps);
     const uint32_t stg =
         smem_u32(sStg) + static_cast<uint32_t>((warp - 2) * 32 * (MODE == kSwiGLU ? 64 : 128));
     int local = 0;
@@ -1392,6 +1412,8 @@ cudaError_t launch_one(const GroupedGemm& g, unsigned* err, int num_sms, cudaStr
   p.interleave = (!SWAP && g.offsets != nullptr) ? 1 : 0;
   p.a_rows = GATHER ? g.src_rows : g.rows_alloc;
   p.c_rows = g.c_rows;
+  p.zero_ptr = g.zero_ptr;
+  p.zero_n = g.zero_n;
   const long long rows_tiles = (g.rows_alloc + Cfg::kActRows - 1) / Cfg::kActRows;
   const long long max_mt = g.offsets != nullptr ? rows_tiles + g.G : rows_tiles;
   const long long max_tiles = max_mt * p.n_tiles;
@@ -1455,6 +1477,8 @@ cudaError_t launch_pair(const GroupedGemm& g, unsigned* err, int num_sms, cudaSt
   p.interleave = g.offsets != nullptr ? 1 : 0;
   p.a_rows = g.rows_alloc;
   p.c_rows = g.c_rows;
+  p.zero_ptr = g.zero_ptr;
+  p.zero_n = g.zero_n;
   const long long rows_tiles = (g.rows_alloc + 255) / 256;
   const long long max_mt = g.offsets != nullptr ? rows_tiles + g.G : rows_tiles;
   const long long max_tiles = max_mt * p.n_tiles;

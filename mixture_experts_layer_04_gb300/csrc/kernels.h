@@ -189,6 +189,12 @@ struct GroupedGemm {
   const int32_t* row_token;  // kScatter only
   const float* row_w;        // kScatter only
   int c_rows;                // kScatter: rows of C (checked in the debug build; 0 = unknown)
+  // Tensor-core engine: a float array that the launch clears (n floats, n % 4 == 0,
+  // 16-byte aligned) before the scatter-add of a later launch, or null.  The fused
+  // combine's fp32 sum is cleared this way by the gate/up GEMM that precedes its down
+  // projection, so no separate memset sits between the two launches.
+  float* zero_ptr;
+  long long zero_n;
   // Tensor-core engine, normal order only: run on CTA pairs (cta_group::2, 256-row tiles)
   int pair;
   // Tensor-core engine, single CTAs: row r of the (grouped) A is row gather_rows[r] of the
