@@ -28,6 +28,12 @@ struct DeviceInfo {
   bool supported = false;
   int num_sms = 0;
   unsigned* err = nullptr;
+  // Prefill layers with a shared expert run it on a second stream, concurrently with the
+  // dispatch permutation (see side_stream()); created on first use, kept until exit.
+  bool side_tried = false;
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  std::mutex side_mu;  // one layer at a time enqueues work on the side stream
 };
 
 DeviceInfo g_dev[kMaxDevices];
@@ -51,6 +57,31 @@ const DeviceInfo* device_info() {
     d.ready = true;
   }
   return &d;
+}
+
+// The device's side stream (lowest priority, not synchronising with the legacy stream)
+// and its fork/join events, created by the first call that asks for them, or null if they
+// cannot be created.  Not called while `s` is being captured into a graph.
+DeviceInfo* side_stream(const DeviceInfo* dc) {
+  DeviceInfo* d = const_cast<DeviceInfo*>(dc);
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  if (!d->side_tried) {
+    d->side_tried = true;
+    int lo = 0, hi = 0;
+    cudaStream_t st = nullptr;
+    cudaEvent_t f = nullptr, j = nullptr;
+    if (cudaDeviceGetStreamPriorityRange(&lo, &hi) == cudaSuccess &&
+        cudaStreamCreateWithPriority(&st, cudaStreamNonBlocking, lo) == cudaSuccess &&
+        cudaEventCreateWithFlags(&f, cudaEventDisableTiming) == cudaSuccess &&
+        cudaEventCreateWithFlags(&j, cudaEventDisableTiming) == cudaSuccess) {
+      d->side = st;
+      d->fork = f;
+      d->join = j;
+    } else {
+      cudaGetLastError();  // leave no sticky error behind; the layer then runs in order
+    }
+  }
+  return d->side != nullptr ? d : nullptr;
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -233,6 +264,8 @@ constexpr int kSwapMaxTokens = 128;
 // the gate/up GEMM instead of copying them.
 constexpr int kGatherMaxTokens = 16;
 constexpr int kPairMinRowsPerGroup = 768;
+// batches from this many tokens run the shared expert on the side stream
+constexpr int kSharedSideMinTokens = 1024;
 constexpr int kPairMinRowsSwiGLU = 384;
 constexpr int kPairWideDim = 4096;
 
@@ -976,6 +1009,37 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
   const bool cluster =
       !capacity && route_cluster_ok(cfg->dtype, cfg->T, cfg->H, cfg->E, cfg->K);
   const bool gather = cluster && cfg->T <= kGatherMaxTokens;
+  // Prefill batches with a shared expert run it on the device's side stream, concurrently
+  // with the dispatch permutation and the routed gate/up GEMM: it needs only x, and it is
+  // tensor-bound while the permutation is memory-bound.  The routed down projection (or
+  // the combine) waits for it.  Not while the caller's stream is being captured.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  const bool conc_wanted = shared && !f32 && cfg->T >= kSharedSideMinTokens &&
+                           cudaStreamIsCapturing(s, &cap) == cudaSuccess &&
+                           cap == cudaStreamCaptureStatusNone;
+  DeviceInfo* side = conc_wanted ? side_stream(d) : nullptr;
+  std::unique_lock<std::mutex> side_lock;
+  if (side != nullptr) side_lock = std::unique_lock<std::mutex>(side->side_mu);
+  // once the shared expert is on the side stream, every return makes `s` wait for it
+  struct JoinOnExit {
+    DeviceInfo* side = nullptr;
+    cudaStream_t s = nullptr;
+    bool armed = false;
+    ~JoinOnExit() {
+      if (armed) cudaStreamWaitEvent(s, side->join, 0);
+    }
+  } join_guard;
+  void* hs = at<void>(ws, p.shared_h);
+  float* y32 = fused ? (y_f32 != nullptr ? y_f32 : at<float>(ws, p.y32)) : nullptr;
+  float* shared_out = nullptr;
+  if (shared && !fused) shared_out = at<float>(ws, p.shared_out);
+  auto run_shared = [&](cudaStream_t st) -> moe_status_t {
+    Groups one{};
+    one.G = 1;
+    MOE_TRY(run_gate_up(cfg, d, x, cfg->T, w_shared_gate_up, cfg->I_shared, hs, one, st));
+    return run_down(cfg, d, hs, cfg->T, w_shared_down, cfg->I_shared, fused ? y32 : shared_out,
+                    one, st);
+  };
   StageRanges nv;
   nv.next("moe_layer_forward.route");
   MOE_TRY(fault_point("moe_layer_forward.route"));
@@ -993,6 +1057,19 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
     if (capacity)
       MOE_CUDA(launch_capacity_route(logits, ids, w, cfg->T, cfg->E, cfg->K, cfg->gate_threshold,
                                      capacity_limit(cfg->T, cfg->K, cfg->E), d->err, s));
+    if (side != nullptr) {
+      nv.next("moe_layer_forward.shared");
+      MOE_TRY(fault_point("moe_layer_forward.shared"));
+      MOE_CUDA(cudaEventRecord(side->fork, s));
+      MOE_CUDA(cudaStreamWaitEvent(side->side, side->fork, 0));
+      const moe_status_t st_shared = run_shared(side->side);
+      const cudaError_t e_join = cudaEventRecord(side->join, side->side);
+      join_guard.side = side;
+      join_guard.s = s;
+      join_guard.armed = e_join == cudaSuccess;
+      MOE_TRY(st_shared);
+      MOE_CUDA(e_join);
+    }
     nv.next("moe_layer_forward.permute");
     MOE_TRY(fault_point("moe_layer_forward.permute"));
     if (deferred > 0) {
@@ -1017,7 +1094,6 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
   // else the routed gate/up GEMM clears it (a memset node between the two expert GEMMs
   // would keep the down projection from launching early), except for 17..128 tokens,
   // where a memset measured about 1% faster
-  float* y32 = fused ? (y_f32 != nullptr ? y_f32 : at<float>(ws, p.y32)) : nullptr;
   const bool memset_sum = fused && !shared && cfg->T > 16 && cfg->T <= 128;
   float* clear = fused && !shared && !memset_sum ? y32 : nullptr;
   const long long clear_n = static_cast<long long>(cfg->T) * cfg->H;
@@ -1032,19 +1108,21 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
     // 5'. shared expert written straight into the fp32 sum (cleared above otherwise), then
     //     the down projection adds every routed row, scaled by its gate, into its token's
     //     row, and one pass rounds the sum to the output type
-    nv.next("moe_layer_forward.shared");
-    MOE_TRY(fault_point("moe_layer_forward.shared"));
-    if (shared) {
-      Groups one{};
-      one.G = 1;
-      void* hs = at<void>(ws, p.shared_h);
-      MOE_TRY(run_gate_up(cfg, d, x, cfg->T, w_shared_gate_up, cfg->I_shared, hs, one, s));
-      MOE_TRY(run_down(cfg, d, hs, cfg->T, w_shared_down, cfg->I_shared, y32, one, s));
+    if (side == nullptr) {
+      nv.next("moe_layer_forward.shared");
+      MOE_TRY(fault_point("moe_layer_forward.shared"));
+    }
+    if (shared && side == nullptr) {
+      MOE_TRY(run_shared(s));
     } else if (memset_sum) {
       MOE_CUDA(cudaMemsetAsync(y32, 0, static_cast<size_t>(cfg->T) * cfg->H * sizeof(float), s));
     }
     nv.next("moe_layer_forward.down");
     MOE_TRY(fault_point("moe_layer_forward.down"));
+    if (side != nullptr) {  // the shared expert has written the fp32 sum
+      join_guard.armed = false;
+      MOE_CUDA(cudaStreamWaitEvent(s, side->join, 0));
+    }
     MOE_TRY(run_down_scatter(cfg, d, h, rows, w_down, cfg->I, y32, gr, perm,
                              at<float>(ws, p.row_w), s));
     nv.next("moe_layer_forward.combine");
@@ -1055,21 +1133,20 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
   nv.next("moe_layer_forward.down");
   MOE_TRY(fault_point("moe_layer_forward.down"));
   MOE_TRY(run_down(cfg, d, h, rows, w_down, cfg->I, out_perm, gr, s));
-  // 5. shared expert: the same engine on all T rows of x as one group
-  float* shared_out = nullptr;
-  nv.next("moe_layer_forward.shared");
-  MOE_TRY(fault_point("moe_layer_forward.shared"));
-  if (shared) {
-    shared_out = at<float>(ws, p.shared_out);
-    Groups one{};
-    one.G = 1;
-    void* hs = at<void>(ws, p.shared_h);
-    MOE_TRY(run_gate_up(cfg, d, x, cfg->T, w_shared_gate_up, cfg->I_shared, hs, one, s));
-    MOE_TRY(run_down(cfg, d, hs, cfg->T, w_shared_down, cfg->I_shared, shared_out, one, s));
+  // 5. shared expert: the same engine on all T rows of x as one group (already enqueued on
+  //    the side stream for prefill batches)
+  if (side == nullptr) {
+    nv.next("moe_layer_forward.shared");
+    MOE_TRY(fault_point("moe_layer_forward.shared"));
+    if (shared) MOE_TRY(run_shared(s));
   }
   // 6. un-permute and weighted combine
   nv.next("moe_layer_forward.combine");
   MOE_TRY(fault_point("moe_layer_forward.combine"));
+  if (side != nullptr) {  // the shared expert's output is complete
+    join_guard.armed = false;
+    MOE_CUDA(cudaStreamWaitEvent(s, side->join, 0));
+  }
   return cuda_status(launch_combine(cfg->dtype, out_perm, inv, w, shared_out, y, y_f32, cfg->T,
                                     cfg->H, cfg->K, s));
 }

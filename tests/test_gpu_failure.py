@@ -72,8 +72,9 @@ def test_debug_wait_rejects_bad_arguments(moe):
                                    "moe_layer_forward.gate_up", "moe_layer_forward.shared",
                                    "moe_layer_forward.down", "moe_layer_forward.combine"])
 @pytest.mark.parametrize("fused", [False, True], ids=["gather_combine", "fused_combine"])
-def test_injected_fault_leaves_output_untouched(moe, point, fused):
-    shape = synth.MoEShape("fault", T=700, H=256, E=32, K=4, I=128, I_shared=64, theta=0.05,
+@pytest.mark.parametrize("T", [700, 1100])   # from 1024 tokens the shared expert runs on a side stream
+def test_injected_fault_leaves_output_untouched(moe, point, fused, T):
+    shape = synth.MoEShape("fault", T=T, H=256, E=32, K=4, I=128, I_shared=64, theta=0.05,
                            bias="zipf", seed=13)
     inp = synth.make_inputs(shape, device="cuda")
     flags = moe.FLAG_FUSED_COMBINE if fused else 0

@@ -435,3 +435,38 @@ def test_kernel_launch_counter(moe):
     n0 = moe.kernel_launch_count()
     empty.run()
     assert moe.kernel_launch_count() == n0
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["gather_combine", "fused_combine"])
+def test_shared_expert_on_side_stream_matches_in_order_layer(moe, fused):
+    """From 1024 tokens the shared expert runs on the library's side stream, concurrently
+    with the permutation; under graph capture the layer runs in stream order instead.  Both
+    must give the same output (bitwise with the deterministic gather combine)."""
+    shape = synth.MoEShape("side", T=2048, H=512, E=64, K=8, I=256, I_shared=256, theta=0.05,
+                           bias="zipf", seed=15)
+    inp = synth.make_inputs(shape, device="cuda")
+    flags = moe.FLAG_FUSED_COMBINE if fused else 0
+    eager = H.LayerRun(moe, shape, inp, flags=flags)
+    eager.run()
+    moe.sync_check()
+    cap = H.LayerRun(moe, shape, inp, flags=flags)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cap.run(stream=torch.cuda.current_stream())
+    g.replay()
+    torch.cuda.synchronize()
+    moe.sync_check()
+    if fused:   # additions in no fixed order
+        torch.testing.assert_close(eager.y32, cap.y32, rtol=1e-5, atol=1e-5)
+    else:
+        assert torch.equal(eager.y, cap.y) and torch.equal(eager.y32, cap.y32)
+    # and against the oracle on a sample of tokens
+    r = eager.routing()
+    toks = np.arange(0, shape.T, 97)
+    sh = dict(w_shared_gate_up=H.f64(inp["w_shared_gate_up"]), w_shared_down=H.f64(inp["w_shared_down"]))
+    ref = oracle.moe_layer_tokens(H.f64(inp["x"])[toks], H.f64(inp["w_router"]),
+                                  H.ExpertSlices(inp["w_gate_up"]), H.ExpertSlices(inp["w_down"]),
+                                  shape.K, shape.theta, _bias_np(inp), **sh)
+    L32 = r["logits"][toks]
+    amb = H.ambiguous_tokens(L32, shape.K, shape.theta, ref["w"])
+    H.assert_close_y(eager.y32.double().cpu().numpy()[toks][~amb], ref["y"][~amb])
