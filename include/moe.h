@@ -308,7 +308,12 @@ moe_status_t moe_combine(const moe_config_t* cfg, const float* out_perm, const i
  *   w_shared_gate_up [2*I_shared,H] act and w_shared_down [H,I_shared] act, both NULL
  *   when I_shared == 0;
  *   y [T,H] act out; y_f32 [T,H] float out or NULL;
- *   ws workspace of at least moe_workspace_size() bytes. */
+ *   ws workspace of at least moe_workspace_size() bytes.
+ * Batches of 1024 tokens or more with a shared expert run it on a stream the library owns
+ * (one per device, created by the first such call), concurrently with the dispatch and the
+ * routed gate/up GEMM; `stream` waits for it before the routed down projection, so work
+ * the caller enqueues on `stream` afterwards sees the whole layer, as with one stream.
+ * While `stream` is being captured into a CUDA graph the layer runs in stream order. */
 moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const void* w_router,
                                const float* router_bias, const void* w_gate_up,
                                const void* w_down, const void* w_shared_gate_up,
