@@ -350,9 +350,19 @@ __device__ __forceinline__ void epilogue_rows(const TcParams& p, uint32_t t_row,
     // FP8 operands: this thread's token-row scale, and the group's weight-row scales
     float sa = 1.f;
     const float* sb = nullptr;
+    // the weight-row scales of every chunk, loaded at once (one coalesced load per chunk,
+    // broadcast by shuffles below) so their latency is paid once, not once per chunk
+    constexpr int kChunks = BN / 64;
+    float sgv[kChunks], suv[kChunks];
     if (p.a_scale != nullptr) {
       sa = tile_row0 + lane < row_end ? __ldg(p.a_scale + tile_row0 + lane) : 0.f;
       sb = p.b_scale + static_cast<size_t>(group) * p.b_rows;
+#pragma unroll
+      for (int k = 0; k < kChunks; ++k) {
+        const int cl = col0 + 32 * k + lane;
+        sgv[k] = cl < p.N_out ? __ldg(sb + cl) : 0.f;
+        suv[k] = cl < p.N_out ? __ldg(sb + p.up_offset + cl) : 0.f;
+      }
     }
 #pragma unroll 1
     for (int c = 0; c < BN / 2; c += 32) {
@@ -361,9 +371,13 @@ __device__ __forceinline__ void epilogue_rows(const TcParams& p, uint32_t t_row,
       tmem_ld_32x32b_x32(t_row + BN / 2 + c, ur);
       tmem_ld_wait();
       if (sb != nullptr) {
-        const int cl = col0 + c + lane;  // one coalesced load per chunk, then broadcast
-        const float sg = cl < p.N_out ? __ldg(sb + cl) : 0.f;
-        const float su = cl < p.N_out ? __ldg(sb + p.up_offset + cl) : 0.f;
+        float sg = 0.f, su = 0.f;
+#pragma unroll
+        for (int k = 0; k < kChunks; ++k)
+          if (32 * k == c) {
+            sg = sgv[k];
+            su = suv[k];
+          }
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           gr[j] = __float_as_uint(__uint_as_float(gr[j]) * (sa * __shfl_sync(0xffffffffu, sg, j)));
@@ -403,11 +417,19 @@ __device__ __forceinline__ void epilogue_rows(const TcParams& p, uint32_t t_row,
       const int grow = tile_row0 + lane;
       rw = grow < row_end ? __ldg(p.row_w + grow) : 0.f;
     }
-    // FP8 operands: this thread's row scale and the group's output-channel scales
+    // FP8 operands: this thread's row scale and the group's output-channel scales, the
+    // latter for every chunk at once
     const float* sb = nullptr;
+    constexpr int kChunks = BN / 32;
+    float scv[kChunks];
     if (p.a_scale != nullptr) {
       rw *= tile_row0 + lane < row_end ? __ldg(p.a_scale + tile_row0 + lane) : 0.f;
       sb = p.b_scale + static_cast<size_t>(group) * p.b_rows;
+#pragma unroll
+      for (int k = 0; k < kChunks; ++k) {
+        const int cl = col0 + 32 * k + lane;
+        scv[k] = cl < p.N_out ? __ldg(sb + cl) : 0.f;
+      }
     }
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
@@ -415,8 +437,10 @@ __device__ __forceinline__ void epilogue_rows(const TcParams& p, uint32_t t_row,
       tmem_ld_32x32b_x32(t_row + c, r);
       tmem_ld_wait();
       if (sb != nullptr) {
-        const int cl = col0 + c + lane;
-        const float sc = cl < p.N_out ? __ldg(sb + cl) : 0.f;
+        float sc = 0.f;
+#pragma unroll
+        for (int k = 0; k < kChunks; ++k)
+          if (32 * k == c) sc = scv[k];
         const float rs = MODE == kScatter ? 1.f : rw;  // kScatter applies rw below
 #pragma unroll
         for (int j = 0; j < 32; ++j)
