@@ -844,6 +844,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           epilogue_rows<BN, MODE>(p, t_row, stg, lane, tile_row0, row_end, col0, g);
       } else {
         // swapped: lane = weight row of the tile, column j = token row0 + j
+        // FP8 operands: the token-row scales of every chunk, loaded before the chunk loops
+        // (lane l of chunk k holds token row0 + k kNC + l's scale)
+        constexpr int kSwChunks = BN / kNC;
+        float sxv[kSwChunks];
+        if (p.a_scale != nullptr) {
+#pragma unroll
+          for (int k = 0; k < kSwChunks; ++k) {
+            const int r = row0 + k * kNC + lane;
+            sxv[k] = r < row_end ? __ldg(p.a_scale + r) : 0.f;
+          }
+        }
+        auto chunk_sx = [&](int c) {
+          float sx = 0.f;
+#pragma unroll
+          for (int k = 0; k < kSwChunks; ++k)
+            if (k * kNC == c) sx = sxv[k];
+          return sx;
+        };
         if constexpr (MODE == kSwiGLU) {
           // lanes 0-63: gate rows (quads 0, 1); lanes 64-127: up rows (quads 2, 3).
           // xchg[r][j] holds up row r for token j, rotated by r to spread the banks.
@@ -864,7 +882,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               float v[32];
               tmem_ld_cols<kNC>(t_row + c, v);
               if (p.a_scale != nullptr) {
-                const float sx = row0 + c + lane < row_end ? __ldg(p.a_scale + row0 + c + lane) : 0.f;
+                const float sx = chunk_sx(c);
 #pragma unroll
                 for (int j = 0; j < kNC; ++j) v[j] *= sw * __shfl_sync(0xffffffffu, sx, j);
               }
@@ -882,7 +900,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               float v[32];
               tmem_ld_cols<kNC>(t_row + c, v);
               if (p.a_scale != nullptr) {
-                const float sx = row0 + c + lane < row_end ? __ldg(p.a_scale + row0 + c + lane) : 0.f;
+                const float sx = chunk_sx(c);
 #pragma unroll
                 for (int j = 0; j < kNC; ++j) v[j] *= sw * __shfl_sync(0xffffffffu, sx, j);
               }
@@ -911,7 +929,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float v[32];
             tmem_ld_cols<kNC>(t_row + c, v);
             if (p.a_scale != nullptr) {
-              const float sx = row0 + c + lane < row_end ? __ldg(p.a_scale + row0 + c + lane) : 0.f;
+              const float sx = chunk_sx(c);
 #pragma unroll
               for (int j = 0; j < kNC; ++j) v[j] *= sw * __shfl_sync(0xffffffffu, sx, j);
             }
@@ -981,11 +999,29 @@ __device__ __forceinline__ void epilogue_pair_tail(const TcParams& p, uint32_t t
                                                    int quad, int lane, int rank, int tn, int row0,
                                                    int row_end, int n0, int group) {
   const int L = quad * 32 + lane;
-  // FP8 operands: scale v[j] (token row0 + c + j) by this lane's weight row and that token
-  auto scale = [&](float (&v)[32], int c, int wrow, bool live) {
+  // FP8 operands: v[j] (token row0 + c + j) is scaled by this lane's weight-row scale and
+  // that token row's scale.  The token-row scales of every chunk and the lane's weight-row
+  // scale are loaded once, before the chunk loop (one dependent load, not one per chunk).
+  constexpr int kMaxChunks = kPairTailMaxN / 32;
+  float sxv[kMaxChunks];
+  if (p.a_scale != nullptr) {
+#pragma unroll
+    for (int k = 0; k < kMaxChunks; ++k) {
+      const int r = row0 + 32 * k + lane;
+      sxv[k] = 32 * k < tn && r < row_end ? __ldg(p.a_scale + r) : 0.f;
+    }
+  }
+  auto weight_scale = [&](int wrow, bool live) {
+    return p.a_scale != nullptr && live
+               ? __ldg(p.b_scale + static_cast<size_t>(group) * p.b_rows + wrow)
+               : 0.f;
+  };
+  auto scale = [&](float (&v)[32], int c, float sw) {
     if (p.a_scale == nullptr) return;
-    const float sw = live ? __ldg(p.b_scale + static_cast<size_t>(group) * p.b_rows + wrow) : 0.f;
-    const float sx = row0 + c + lane < row_end ? __ldg(p.a_scale + row0 + c + lane) : 0.f;
+    float sx = 0.f;
+#pragma unroll
+    for (int k = 0; k < kMaxChunks; ++k)
+      if (32 * k == c) sx = sxv[k];
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] *= sw * __shfl_sync(0xffffffffu, sx, j);
   };
@@ -993,20 +1029,21 @@ __device__ __forceinline__ void epilogue_pair_tail(const TcParams& p, uint32_t t
     float* xchg = reinterpret_cast<float*>(stg);  // [64][32], rotated by row
     __nv_bfloat16* C = static_cast<__nv_bfloat16*>(p.C);
     const int col = n0 + 64 * rank + (L & 63);
+    const float sw = weight_scale(quad >= 2 ? p.up_offset + col : col, col < p.N_out);
 #pragma unroll 1
     for (int c = 0; c < tn; c += 32) {
       float v[32];
       if (quad >= 2) {
         const int r = L - 64;
         tmem_ld_cols<32>(t_row + c, v);
-        scale(v, c, p.up_offset + col, col < p.N_out);
+        scale(v, c, sw);
 #pragma unroll
         for (int j = 0; j < 32; ++j) xchg[r * 32 + ((j + r) & 31)] = v[j];
       }
       epi_bar();
       if (quad < 2) {
         tmem_ld_cols<32>(t_row + c, v);
-        scale(v, c, col, col < p.N_out);
+        scale(v, c, sw);
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const int tok = row0 + c + j;
@@ -1022,11 +1059,12 @@ __device__ __forceinline__ void epilogue_pair_tail(const TcParams& p, uint32_t t
     float* C = static_cast<float*>(p.C);
     const int col = n0 + 128 * rank + L;
     const float b = (p.col_bias != nullptr && col < p.N_out) ? __ldg(p.col_bias + col) : 0.f;
+    const float sw = weight_scale(col, col < p.N_out);
 #pragma unroll 1
     for (int c = 0; c < tn; c += 32) {
       float v[32];
       tmem_ld_cols<32>(t_row + c, v);
-      scale(v, c, col, col < p.N_out);
+      scale(v, c, sw);
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const int tok = row0 + c + j;
