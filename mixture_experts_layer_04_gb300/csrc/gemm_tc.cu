@@ -249,6 +249,14 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, const int* s_off,
   }
 }
 
+// True when tile (g, row0..row_end) is its group's only token tile: each of the group's
+// weight tiles is then read by this one tile and never again in the launch.
+__device__ __forceinline__ bool read_once(const TcParams& p, const int* s_off, int g, int row0,
+                                          int row_end, int tile_rows) {
+  const int first = p.offsets != nullptr ? s_off[g] : 0;
+  return row0 == first && row_end - row0 <= tile_rows;
+}
+
 // This CTA's share of the array to clear (see TcParams::zero_ptr), by the `nthreads`
 // epilogue threads before they wait for the first accumulator; the writes need no ordering
 // with the rest of this launch, only with later launches.
@@ -682,6 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     static_assert(kGatherLanes <= 32, "one gather4 per lane");
     if (gather || elect_one_sync()) {
       const bool leader = !gather || lane == 0;
+      const uint64_t pol_once = l2_policy_evict_first();
       int stage = 0;
       uint32_t phase = 0;
       long long issued = 0;
@@ -690,6 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int g, row0, row_end, n_tile;
         decode_tile(p, s_off, s_mt, s_light, sc, kTileRows, idx, g, row0, row_end, n_tile);
         const int n0 = n_tile * Cfg::kColsOut;  // first weight row of the tile
+        const bool once = read_once(p, s_off, g, row0, row_end, kTileRows);
         // With a row gather only the lanes whose four rows start inside the group load
         // anything: the rest of the tile's rows are never stored, so whatever an earlier
         // stage left in that part of the buffer is harmless.  Within a lane, rows past
@@ -722,9 +732,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (leader) {
             mbar_arrive_expect_tx(fb, stage_tx);
             if constexpr (!GATHER) tma_load_2d(a_dst, &p.tmAct, fb, kb * kKStep, row0);
-            tma_load_3d(w_dst, &p.tmWgt, fb, kb * kKStep, n0, g);
-            if constexpr (MODE == kSwiGLU)
-              tma_load_3d(w_dst + Cfg::kWgtBox * 128, &p.tmWgt, fb, kb * kKStep, p.up_offset + n0, g);
+            if (once) {
+              tma_load_3d_hint(w_dst, &p.tmWgt, fb, kb * kKStep, n0, g, pol_once);
+              if constexpr (MODE == kSwiGLU)
+                tma_load_3d_hint(w_dst + Cfg::kWgtBox * 128, &p.tmWgt, fb, kb * kKStep,
+                                 p.up_offset + n0, g, pol_once);
+            } else {
+              tma_load_3d(w_dst, &p.tmWgt, fb, kb * kKStep, n0, g);
+              if constexpr (MODE == kSwiGLU)
+                tma_load_3d(w_dst + Cfg::kWgtBox * 128, &p.tmWgt, fb, kb * kKStep,
+                            p.up_offset + n0, g);
+            }
           }
           if constexpr (GATHER) {
             __syncwarp();
@@ -1170,6 +1188,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer ----
     if (elect_one_sync()) {
+      const uint64_t pol_once = l2_policy_evict_first();
       int stage = 0;
       uint32_t phase = 0;
       long long issued = 0;
@@ -1184,6 +1203,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // swapped tail: sA takes this CTA's 128 weight rows, sB its N/2 token rows
         const int tn = pair_tail_n(row0, row_end);
         const int t_row = row0 + static_cast<int>(rank) * (tn / 2);
+        const bool once = read_once(p, s_off, g, row0, row_end, kTileRows);
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
             ok = false;
@@ -1195,11 +1215,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (tn > 0) {
             if (rank == 0)
               mbar_arrive_expect_tx(full_bar(stage), 2u * (Cfg::kABytes + tn * 64));
-            if constexpr (MODE == kSwiGLU)  // gate rows w0.. then the matching up rows
-              tma_load_4d_pair(a_dst, &p.tmWgtS, fb_leader, kb * kKStep,
-                               n0 + static_cast<int>(rank) * 64, 0, g);
-            else
+            if constexpr (MODE == kSwiGLU) {  // gate rows w0.. then the matching up rows
+              if (once)
+                tma_load_4d_pair_hint(a_dst, &p.tmWgtS, fb_leader, kb * kKStep,
+                                      n0 + static_cast<int>(rank) * 64, 0, g, pol_once);
+              else
+                tma_load_4d_pair(a_dst, &p.tmWgtS, fb_leader, kb * kKStep,
+                                 n0 + static_cast<int>(rank) * 64, 0, g);
+            } else if (once) {
+              tma_load_3d_pair_hint(a_dst, &p.tmWgt, fb_leader, kb * kKStep, b_row, g, pol_once);
+            } else {
               tma_load_3d_pair(a_dst, &p.tmWgt, fb_leader, kb * kKStep, b_row, g);
+            }
             // this CTA's tn/2 token rows in boxes of 64, 32 and 16 rows
             int rr = 0;
             for (; rr + 64 <= tn / 2; rr += 64)
@@ -1219,7 +1246,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * Cfg::kStageBytes);
           tma_load_2d_pair(a_dst, &p.tmAct, fb_leader, kb * kKStep, a_row);
-          tma_load_3d_pair(b_dst, &p.tmWgt, fb_leader, kb * kKStep, b_row, g);
+          if (once)
+            tma_load_3d_pair_hint(b_dst, &p.tmWgt, fb_leader, kb * kKStep, b_row, g, pol_once);
+          else
+            tma_load_3d_pair(b_dst, &p.tmWgt, fb_leader, kb * kKStep, b_row, g);
           ++issued;
           if (++stage == S) {
             stage = 0;
