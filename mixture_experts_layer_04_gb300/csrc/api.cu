@@ -110,7 +110,7 @@ bool use_tc_router(const moe_config_t* c) {
 struct Plan {
   size_t logits, partial, ids, w, counts, offsets, perm, inv, perm_ws, table, num_mt, x_perm, h,
       out_perm, row_w, y32, x_codes, x_scales, xs_perm, h_codes, h_scales,
-      shared_h, shared_out, total;
+      shared_h, shared_out, tile_counter, total;
 };
 
 inline size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
@@ -158,6 +158,7 @@ Plan make_plan(const moe_config_t* c) {
   p.xs_perm = take(fp8 ? T * K * 4 : 0);
   p.h_codes = take(fp8 ? T * K * I : 0);
   p.h_scales = take(fp8 ? T * K * 4 : 0);
+  p.tile_counter = take(4);
   p.total = o;
   return p;
 }
@@ -269,6 +270,25 @@ constexpr int kSharedSideMinTokens = 1024;
 constexpr int kPairMinRowsSwiGLU = 384;
 constexpr int kPairWideDim = 4096;
 
+// The routed gate/up GEMM of a prefill-sized bf16 batch runs on CTA pairs in the normal
+// operand order, where the pairs draw their tiles from a counter in the workspace (the
+// SwiGLU launch measured faster so on GB300: Qwen3-, Mixtral- and DeepSeek-shaped gate/up
+// 1-4%, FP8 Mixtral-shaped 22%; the down projections and single-CTA launches were not).
+// The layer's permutation kernel zeroes the counter; a standalone call, a memset.
+bool dynamic_tiles(const moe_config_t* c) {
+  return c->dtype == MOE_BF16 && c->T > kSwapMaxTokens;
+}
+
+// The tile counter of a standalone gate/up call (zeroed first), or null.
+int* standalone_counter(const moe_config_t* c, void* ws, const Plan& p, cudaStream_t s,
+                        cudaError_t* e) {
+  *e = cudaSuccess;
+  if (!dynamic_tiles(c)) return nullptr;
+  int* ctr = at<int>(ws, p.tile_counter);
+  *e = cudaMemsetAsync(ctr, 0, sizeof(int), s);
+  return ctr;
+}
+
 // CTA pairs (256-row tiles, 2/3 of the shared-memory traffic per MMA) pay for the padding
 // of each group's last tile when groups are large (>= 768 rows on average), or half that
 // size with a long reduction or a wide output to amortise it; otherwise single CTAs with
@@ -301,9 +321,10 @@ moe_status_t launch_gemm(const moe_config_t* c, const DeviceInfo* d, const Group
 moe_status_t run_gate_up(const moe_config_t* c, const DeviceInfo* d, const void* A,
                          int rows_alloc, const void* w_gate_up, int I, void* h, const Groups& gr,
                          cudaStream_t s, const int32_t* gather_rows = nullptr,
-                         float* clear = nullptr, long long clear_n = 0) {
+                         float* clear = nullptr, long long clear_n = 0, int* ctr = nullptr) {
   if (rows_alloc == 0) return MOE_OK;
   GroupedGemm g{};
+  g.tile_counter = ctr;
   g.zero_ptr = clear;
   g.zero_n = clear_n;
   g.gather_rows = gather_rows;
@@ -654,7 +675,10 @@ moe_status_t moe_grouped_ffn(const moe_config_t* cfg, const void* x_perm, const 
   MOE_TRY(routed_groups(cfg, offsets, ws, p, false, s, &gr));
   void* h = at<void>(ws, p.h);
   const int rows = cfg->T * cfg->K;
-  MOE_TRY(run_gate_up(cfg, d, x_perm, rows, w_gate_up, cfg->I, h, gr, s));
+  cudaError_t e;
+  int* ctr = standalone_counter(cfg, ws, p, s, &e);
+  MOE_CUDA(e);
+  MOE_TRY(run_gate_up(cfg, d, x_perm, rows, w_gate_up, cfg->I, h, gr, s, nullptr, nullptr, 0, ctr));
   return run_down(cfg, d, h, rows, w_down, cfg->I, out_perm, gr, s);
 }
 
@@ -675,7 +699,11 @@ moe_status_t moe_expert_gate_up(const moe_config_t* cfg, const void* x_perm,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Groups gr;
   MOE_TRY(routed_groups(cfg, offsets, ws, p, false, s, &gr));
-  return run_gate_up(cfg, d, x_perm, cfg->T * cfg->K, w_gate_up, cfg->I, h, gr, s);
+  cudaError_t e;
+  int* ctr = standalone_counter(cfg, ws, p, s, &e);
+  MOE_CUDA(e);
+  return run_gate_up(cfg, d, x_perm, cfg->T * cfg->K, w_gate_up, cfg->I, h, gr, s, nullptr,
+                     nullptr, 0, ctr);
 }
 
 moe_status_t moe_quantize_fp8(const void* in, int64_t rows, int32_t cols, uint8_t* codes,
@@ -722,6 +750,9 @@ moe_status_t moe_expert_gate_up_fp8(const moe_config_t* cfg, const uint8_t* x_co
   g.offsets = offsets;
   g.swap_tokens = cfg->T <= kSwapMaxTokens ? cfg->T : 0;
   g.pair = use_pairs(g) ? 1 : 0;
+  cudaError_t e;
+  g.tile_counter = standalone_counter(cfg, ws, p, static_cast<cudaStream_t>(stream), &e);
+  MOE_CUDA(e);
   return cuda_status(launch_gate_up_fp8(g, x_scales, w_scales, d->err, d->num_sms,
                                         static_cast<cudaStream_t>(stream)));
 }
@@ -875,9 +906,11 @@ moe_status_t moe_layer_forward_fp8(const moe_config_t* cfg, const void* x, const
   MOE_CUDA(launch_quantize_fp8(x, T, H, x_codes, x_scales, s));
   const bool fused = (cfg->flags & MOE_FLAG_FUSED_COMBINE) != 0u;
   float* row_w = fused ? at<float>(ws, p.row_w) : nullptr;
+  // the permutation zeroes the routed gate/up GEMM's tile counter
+  int* ctr = dynamic_tiles(cfg) ? at<int>(ws, p.tile_counter) : nullptr;
   MOE_CUDA(launch_permute(MOE_BF16, x_codes, ids, T, H / 2, E, K, counts, offsets, perm, inv,
                           xq_perm, at<int32_t>(ws, p.perm_ws), nullptr, nullptr, kF32TileRows, w,
-                          row_w, s));
+                          row_w, s, ctr));
   MOE_CUDA(launch_gather_scales(x_scales, perm, offsets + E, xs_perm, T * K, s));
   // 3. FP8 gate/up -> bf16 h -> E4M3 h -> FP8 down
   GroupedGemm g{};
@@ -895,6 +928,7 @@ moe_status_t moe_layer_forward_fp8(const moe_config_t* cfg, const void* x, const
   g.offsets = offsets;
   g.swap_tokens = T <= kSwapMaxTokens ? T : 0;
   g.pair = use_pairs(g) ? 1 : 0;
+  g.tile_counter = ctr;
   // the fused combine's fp32 sum is initialised by the shared expert or cleared here
   float* y32 = fused ? (y_f32 != nullptr ? y_f32 : at<float>(ws, p.y32)) : nullptr;
   if (fused && !shared) {
@@ -1040,6 +1074,7 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
     return run_down(cfg, d, hs, cfg->T, w_shared_down, cfg->I_shared, fused ? y32 : shared_out,
                     one, st);
   };
+  int* gu_counter = nullptr;  // set where the permutation zeroes it
   StageRanges nv;
   nv.next("moe_layer_forward.route");
   MOE_TRY(fault_point("moe_layer_forward.route"));
@@ -1072,17 +1107,19 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
     }
     nv.next("moe_layer_forward.permute");
     MOE_TRY(fault_point("moe_layer_forward.permute"));
+    // the permutation zeroes the routed gate/up GEMM's tile counter
+    gu_counter = dynamic_tiles(cfg) ? at<int>(ws, p.tile_counter) : nullptr;
     if (deferred > 0) {
       MOE_CUDA(launch_topk_permute_small(partial, deferred, router_bias, logits, ids, w,
                                          cfg->gate_threshold, cfg->dtype, x, cfg->T, cfg->H,
                                          cfg->E, cfg->K, counts, offsets, perm, inv, x_perm,
                                          f32 ? table : nullptr, f32 ? num_mt : nullptr, kF32TileRows,
-                                         row_w, s));
+                                         row_w, s, gu_counter));
     } else {
       MOE_CUDA(launch_permute(cfg->dtype, x, ids, cfg->T, cfg->H, cfg->E, cfg->K, counts,
                               offsets, perm, inv, x_perm, at<int32_t>(ws, p.perm_ws),
                               f32 ? table : nullptr, f32 ? num_mt : nullptr, kF32TileRows, w, row_w,
-                              s));
+                              s, gu_counter));
     }
   }
   // 3-4. grouped SwiGLU FFN of the routed experts
@@ -1103,7 +1140,7 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
     MOE_TRY(run_gate_up(cfg, d, x, rows, w_gate_up, cfg->I, h, gr, s, perm, clear, clear_n));
   else
     MOE_TRY(run_gate_up(cfg, d, x_perm, rows, w_gate_up, cfg->I, h, gr, s, nullptr, clear,
-                        clear_n));
+                        clear_n, gu_counter));
   if (fused) {
     // 5'. shared expert written straight into the fp32 sum (cleared above otherwise), then
     //     the down projection adds every routed row, scaled by its gate, into its token's

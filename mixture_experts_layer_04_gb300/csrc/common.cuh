@@ -126,16 +126,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with acquire at cluster scope: for a barrier that a peer CTA arrives on
+// (release.cluster) after writing into this CTA's shared memory.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait until the phase of parity `parity` of barrier `bar` has completed.  Gives up
 // when *abort becomes non-zero (another role gave up) or after `limit_ns` (default
 // kWaitLimitNs), in which case it sets *abort and the error word.  Returns true on success.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           unsigned* err,
                                           unsigned long long limit_ns = kWaitLimitNs) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto try_wait = [&] {
+    return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+  };
+  if (try_wait()) return true;
   unsigned long long t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (try_wait()) return true;
     if ((it & 255u) == 0u) {
       if (*abort) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
@@ -360,6 +378,10 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t mask) {
       " [%0], %1;" ::"r"(bar),
       "h"(mask)
       : "memory");
+}
+// 32-bit store into the shared memory of a CTA of the cluster (shared::cluster address)
+__device__ __forceinline__ void st_shared_cluster(uint32_t addr, int v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(

@@ -95,6 +95,9 @@ struct TcParams {
   float* zero_ptr;  // cleared by the epilogue warps before the first tile (n floats), or null
   long long zero_n;
   int a_rows;  // rows of the tensor behind tmAct (the gather's source rows with a row gather)
+  // CTA pairs: tiles are taken in index order from this counter (zero at launch) as pairs
+  // become free (see ring_publish), or null for every npairs-th tile per pair
+  int* tile_counter;
   int c_rows;  // kScatter: rows of C, 0 = unknown (both checked in the debug build only)
 };
 
@@ -255,6 +258,61 @@ __device__ __forceinline__ bool read_once(const TcParams& p, const int* s_off, i
                                           int row_end, int tile_rows) {
   const int first = p.offsets != nullptr ? s_off[g] : 0;
   return row0 == first && row_end - row0 <= tile_rows;
+}
+
+// ------------------------------------------------------- dynamic tile order ----
+// With p.tile_counter, CTA pairs take tiles in index order as they become free instead of
+// every npairs-th tile each: the even CTA's producer thread draws tile indices from the
+// counter and hands them to the pair's other roles (its own MMA thread and epilogue warps,
+// the odd CTA's producer and epilogue warps) through a ring of kTileRing slots in shared
+// memory.  Tiles that share a weight tile then start close together in time whichever
+// pairs run them, and no pair is left running a whole tile after the others have finished.
+// The drawing thread keeps two tiles ahead: it draws the index of tile j + 2 when it starts
+// loading tile j and publishes it once tile j's loads are issued, so the atomic's latency
+// and the odd CTA's wait are off the load path.  Every pair's last two draws are past the
+// end, so the counter ends at total + 2 x pairs.
+constexpr int kTileRing = 6;
+
+struct TileRing {
+  uint32_t full0;   // kTileRing barriers (count 1): the slot holds the next index
+  uint32_t empty0;  // kTileRing barriers of the even CTA: every consumer has read the slot
+  uint32_t slot0;   // kTileRing ints
+};
+
+// Publishes tile index v (-1: stop) as tile number j of this pair, in both CTAs.  The slot
+// is written even when the wait for it fails, so that the consumers stop; returns false then.
+__device__ __forceinline__ bool ring_publish(const TileRing& r, int j, int v,
+                                             volatile int* abort, unsigned* err) {
+  const int s = j % kTileRing;
+  const uint32_t ph = static_cast<uint32_t>(j / kTileRing) & 1u;
+  const bool ok = mbar_wait<true>(r.empty0 + 8u * s, ph ^ 1u, abort, err);
+  if (!ok) v = -1;
+  const uint32_t slot = r.slot0 + 4u * s;
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(slot), "r"(v) : "memory");
+  mbar_arrive(r.full0 + 8u * s);
+  st_shared_cluster(mapa_shared(slot, 1), v);
+  mbar_arrive_cluster(mapa_shared(r.full0 + 8u * s, 1));
+  return ok;
+}
+__device__ __forceinline__ int ring_index(int ticket, int total) {
+  return ticket < total ? ticket : -1;
+}
+
+// A consumer thread: tile number j (-1: stop), after which it releases the slot.  kRemote:
+// the thread is in the odd CTA, whose slot the even CTA wrote.
+template <bool kRemote>
+__device__ __forceinline__ int ring_take(const TileRing& r, int j, volatile int* abort,
+                                         unsigned* err) {
+  const int s = j % kTileRing;
+  const uint32_t ph = static_cast<uint32_t>(j / kTileRing) & 1u;
+  int v = -1;
+  if (mbar_wait<kRemote>(r.full0 + 8u * s, ph, abort, err))
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(r.slot0 + 4u * s) : "memory");
+  if constexpr (kRemote)
+    mbar_arrive_cluster(mapa_shared(r.empty0 + 8u * s, 0));
+  else
+    mbar_arrive(r.empty0 + 8u * s);
+  return v;
 }
 
 // This CTA's share of the array to clear (see TcParams::zero_ptr), by the `nthreads`
@@ -631,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sStg = sWgt + S * Cfg::kWgtBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + Cfg::kStgBytes);
   // bars: full[S], empty[S], tfull[2], tempty[2], mma_done
-  static_assert(8 * (2 * S + 5) + 8 <= 256, "barrier region");
+  static_assert(8 * (2 * S + 5) + 8 <= Cfg::kBarBytes, "barrier region");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_off = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(bars) + Cfg::kBarBytes);
@@ -1111,7 +1169,7 @@ struct TcPairCfg {
   static constexpr int kColsOut = MODE == kSwiGLU ? 128 : 256;
   static constexpr int kTmemCols = 512;
   static constexpr int kStgBytes = kEpiWarps * 32 * (MODE == kSwiGLU ? 64 : 128);
-  static constexpr int kBarBytes = 256;
+  static constexpr int kBarBytes = 384;
   static constexpr int kSchedBytes = 3 * (kMaxGroups + 4) * 4 + 32 * 4;
   static constexpr int kSmem = 1024 + kStages * kStageBytes + kStgBytes + kBarBytes + kSchedBytes;
   static_assert(kSmem <= 232448, "shared memory per CTA");
@@ -1132,7 +1190,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t* sB = sA + S * Cfg::kABytes;
   uint8_t* sStg = sB + S * Cfg::kBBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + Cfg::kStgBytes);
-  // bars: full[S], empty[S], tfull[2], tempty[2], mma_done
+  // bars: full[S], empty[S], tfull[2], tempty[2], mma_done, {tmem slot, abort flag},
+  // tile ring full[kTileRing], empty[kTileRing], slots
+  static_assert(8 * (2 * S + 6 + 2 * kTileRing) + 4 * kTileRing <= Cfg::kBarBytes,
+                "barrier region");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_off = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(bars) + Cfg::kBarBytes);
@@ -1148,6 +1209,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
   const uint32_t mma_done_bar = bar0 + 8u * (2 * S + 4);
+  // dynamic tile order: the even CTA's producer draws; consumers are the even CTA's MMA
+  // thread and epilogue warps and the odd CTA's producer and epilogue warps
+  const bool dyn = p.tile_counter != nullptr;
+  const TileRing ring{bar0 + 8u * (2 * S + 6), bar0 + 8u * (2 * S + 6 + kTileRing),
+                      bar0 + 8u * (2 * S + 6 + 2 * kTileRing)};
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -1159,6 +1225,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(tempty_bar(a), 2 * kEpiWarps);
     }
     mbar_init(mma_done_bar, 1);
+    for (int r = 0; r < kTileRing; ++r) {
+      mbar_init(ring.full0 + 8u * r, 1);
+      mbar_init(ring.empty0 + 8u * r, 2 + 2 * kEpiWarps);
+    }
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&p.tmAct);
@@ -1193,7 +1263,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       long long issued = 0;
       bool ok = true;
-      for (int idx = pair; idx < total && ok; idx += npairs) {
+      const bool draws = dyn && rank == 0;  // the even CTA draws, the odd one takes
+      int cur = -1, nxt = -1;                // (drawing) tiles j and j + 1, already published
+      if (draws) {
+        const int t0 = atomicAdd(p.tile_counter, 1), t1 = atomicAdd(p.tile_counter, 1);
+        cur = ring_index(t0, total);
+        nxt = ring_index(t1, total);
+        ok = ring_publish(ring, 0, cur, abort_flag, p.err) &&
+             ring_publish(ring, 1, nxt, abort_flag, p.err);
+      }
+      for (int j = 0; ok; ++j) {
+        int idx = pair + j * npairs;
+        if (draws) idx = cur;
+        else if (dyn) idx = ring_take<true>(ring, j, abort_flag, p.err);
+        if (idx < 0 || idx >= total) break;
+        const int ticket = draws ? atomicAdd(p.tile_counter, 1) : 0;  // tile j + 2
         int g, row0, row_end, n_tile;
         decode_tile(p, s_off, s_mt, s_light, sc, kTileRows, idx, g, row0, row_end, n_tile);
         const int n0 = n_tile * Cfg::kColsOut;
@@ -1256,6 +1340,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             phase ^= 1u;
           }
         }
+        if (draws && ok) {
+          ok = ring_publish(ring, j + 2, ring_index(ticket, total), abort_flag, p.err);
+          cur = nxt;
+          nxt = ring_index(ticket, total);
+        }
       }
       if (rank == 0) {
         // Drain: both CTAs' loads complete on the even CTA's full barriers.
@@ -1281,7 +1370,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
-      for (int idx = pair; idx < total && ok; idx += npairs, ++local) {
+      for (int j = 0; ok; ++j, ++local) {
+        int idx = pair + j * npairs;
+        if (dyn) idx = ring_take<false>(ring, j, abort_flag, p.err);
+        if (idx < 0 || idx >= total) break;
         const int acc = local & 1;
         const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
         int g, row0, row_end, n_tile;
@@ -1331,7 +1423,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t stg =
         smem_u32(sStg) + static_cast<uint32_t>((warp - 2) * 32 * (MODE == kSwiGLU ? 64 : 128));
     int local = 0;
-    for (int idx = pair; idx < total; idx += npairs, ++local) {
+    for (int j = 0;; ++j, ++local) {
+      int idx = pair + j * npairs;
+      if (dyn) {
+        if (lane == 0)
+          idx = rank == 0 ? ring_take<false>(ring, j, abort_flag, p.err)
+                          : ring_take<true>(ring, j, abort_flag, p.err);
+        idx = __shfl_sync(0xffffffffu, idx, 0);
+        if (epi_bar_any(idx < 0)) break;  // the four warps stop together
+      }
+      if (idx >= total) break;
       int g, row0, row_end, n_tile;
       decode_tile(p, s_off, s_mt, s_light, sc, kTileRows, idx, g, row0, row_end, n_tile);
       const int acc = local & 1;
@@ -1567,6 +1668,7 @@ cudaError_t launch_pair(const GroupedGemm& g, unsigned* err, int num_sms, cudaSt
   p.up_offset = g.up_offset;
   p.swz = kSwz;
   p.interleave = g.offsets != nullptr ? 1 : 0;
+  p.tile_counter = g.tile_counter;
   p.a_rows = g.rows_alloc;
   p.c_rows = g.c_rows;
   p.zero_ptr = g.zero_ptr;

@@ -120,11 +120,13 @@ inline int max_mtiles(int T, int K, int E, int bm) {
 // x_perm[r] = x[perm[r]].  If `mtile_table` is non-null the m-tile table of `bm`
 // rows per tile is written as well (entries {expert, row0, row_end, 0}) with its
 // length in *num_mtiles.  If `row_w` is non-null, row_w[r] = gate_w of row r's slot.
+// If `zero_word` is non-null it is set to 0 (the tile counter of a later grouped GEMM on
+// the same stream, so that no memset sits between the launches).
 cudaError_t launch_permute(int dtype, const void* x, const int32_t* ids, int T, int H, int E,
                            int K, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
                            void* x_perm, int32_t* ws_words, int4* mtile_table,
                            int32_t* num_mtiles, int bm, const float* gate_w, float* row_w,
-                           cudaStream_t s);
+                           cudaStream_t s, int32_t* zero_word = nullptr);
 
 // Routing and the permutation in one launch for small batches: logits = sum of the
 // router's S partial slices + bias (written to `logits`), top-k/softmax/gate drop
@@ -135,7 +137,8 @@ cudaError_t launch_topk_permute_small(const float* partial, int S, const float* 
                                       int dtype, const void* x, int T, int H, int E, int K,
                                       int32_t* counts, int32_t* offsets, int32_t* perm,
                                       int32_t* inv, void* x_perm, int4* mtile_table,
-                                      int32_t* num_mtiles, int bm, float* row_w, cudaStream_t s);
+                                      int32_t* num_mtiles, int bm, float* row_w, cudaStream_t s,
+                                      int32_t* zero_word = nullptr);
 
 // The m-tile table of a grouped GEMM from offsets alone.
 // `rows`: rows of the grouped matrix (offsets[E] must not exceed it).
@@ -195,6 +198,10 @@ struct GroupedGemm {
   // projection, so no separate memset sits between the two launches.
   float* zero_ptr;
   long long zero_n;
+  // Tensor-core engine, normal order: a device int, zero when the launch starts, from
+  // which the CTAs draw tile indices in order as they become free; or null for a fixed
+  // round-robin assignment of the tiles.
+  int* tile_counter;
   // Tensor-core engine, normal order only: run on CTA pairs (cta_group::2, 256-row tiles)
   int pair;
   // Tensor-core engine, single CTAs: row r of the (grouped) A is row gather_rows[r] of the

@@ -74,11 +74,13 @@ __device__ void write_mtiles(int4* table, int e, int base, int count, int first,
 __global__ void __launch_bounds__(kScanThreads)
     permute_scan_kernel(int32_t* __restrict__ block_counts, int nblocks, int E,
                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-                        int4* __restrict__ mtile_table, int32_t* __restrict__ num_mtiles, int bm) {
+                        int4* __restrict__ mtile_table, int32_t* __restrict__ num_mtiles, int bm,
+                        int32_t* __restrict__ zero_word) {
   __shared__ int scratch[32];
   grid_dep_wait();
   grid_dep_trigger();
   const int e = threadIdx.x;
+  if (zero_word != nullptr && e == 0) *zero_word = 0;
   constexpr int kChunk = 16;  // counts loaded at once (independent loads in flight)
   // pass 1: the expert's total over all rank blocks
   int total = 0;
@@ -229,7 +231,7 @@ __global__ void __launch_bounds__(kSmallThreads)
                          uint4* __restrict__ x_perm, int4* __restrict__ mtile_table,
                          int32_t* __restrict__ num_mtiles, int bm,
                          const float* __restrict__ gate_w, float* __restrict__ row_w,
-                         unsigned* __restrict__ err) {
+                         unsigned* __restrict__ err, int32_t* __restrict__ zero_word) {
   extern __shared__ uint32_t smem_u[];
   uint32_t* masks = smem_u;                                        // [E][8]
   int* cnt = reinterpret_cast<int*>(masks + E * kSmallMaskWords);  // [E]
@@ -239,6 +241,7 @@ __global__ void __launch_bounds__(kSmallThreads)
   grid_dep_wait();
   grid_dep_trigger();
   const int tid = threadIdx.x;
+  if (zero_word != nullptr && blockIdx.x == 0 && tid == 0) *zero_word = 0;
   const int TK = T * K;
   const int32_t* ids = ids_in;
   const float* gates = gate_w;
@@ -373,7 +376,7 @@ cudaError_t launch_small_t(int dtype, const void* x, const int32_t* ids, const S
                            int T, int H, int E, int K, int32_t* counts, int32_t* offsets,
                            int32_t* perm, int32_t* inv, void* x_perm, int4* mtile_table,
                            int32_t* num_mtiles, int bm, const float* gate_w, float* row_w,
-                           cudaStream_t s) {
+                           int32_t* zero_word, cudaStream_t s) {
   static int attr_dev = -1;  // opt in to more than 48 KB of dynamic shared memory once
   int dev = 0;
   cudaGetDevice(&dev);
@@ -394,19 +397,19 @@ cudaError_t launch_small_t(int dtype, const void* x, const int32_t* ids, const S
   return launch_pdl(permute_small_kernel<kRoute>, dim3(blocks), dim3(kSmallThreads), smem, s, ids,
                     r, T, E, K, row_units, counts, offsets, perm, inv,
                     static_cast<const uint4*>(x), static_cast<uint4*>(x_perm), mtile_table,
-                    num_mtiles, bm, gate_w, row_w, device_error_word());
+                    num_mtiles, bm, gate_w, row_w, device_error_word(), zero_word);
 }
 
 cudaError_t launch_small(int dtype, const void* x, const int32_t* ids, const SmallRoute* rt,
                          int T, int H, int E, int K, int32_t* counts, int32_t* offsets,
                          int32_t* perm, int32_t* inv, void* x_perm, int4* mtile_table,
                          int32_t* num_mtiles, int bm, const float* gate_w, float* row_w,
-                         cudaStream_t s) {
+                         int32_t* zero_word, cudaStream_t s) {
   if (rt != nullptr)
     return launch_small_t<true>(dtype, x, ids, rt, T, H, E, K, counts, offsets, perm, inv, x_perm,
-                                mtile_table, num_mtiles, bm, gate_w, row_w, s);
+                                mtile_table, num_mtiles, bm, gate_w, row_w, zero_word, s);
   return launch_small_t<false>(dtype, x, ids, rt, T, H, E, K, counts, offsets, perm, inv, x_perm,
-                               mtile_table, num_mtiles, bm, gate_w, row_w, s);
+                               mtile_table, num_mtiles, bm, gate_w, row_w, zero_word, s);
 }
 
 }  // namespace
@@ -420,10 +423,11 @@ cudaError_t launch_topk_permute_small(const float* partial, int S, const float* 
                                       int dtype, const void* x, int T, int H, int E, int K,
                                       int32_t* counts, int32_t* offsets, int32_t* perm,
                                       int32_t* inv, void* x_perm, int4* mtile_table,
-                                      int32_t* num_mtiles, int bm, float* row_w, cudaStream_t s) {
+                                      int32_t* num_mtiles, int bm, float* row_w, cudaStream_t s,
+                                      int32_t* zero_word) {
   SmallRoute rt{partial, S, bias, logits, ids, w, theta};
   return launch_small(dtype, x, nullptr, &rt, T, H, E, K, counts, offsets, perm, inv, x_perm,
-                      mtile_table, num_mtiles, bm, nullptr, row_w, s);
+                      mtile_table, num_mtiles, bm, nullptr, row_w, zero_word, s);
 }
 
 size_t permute_ws_words(int T, int E) {
@@ -435,10 +439,10 @@ cudaError_t launch_permute(int dtype, const void* x, const int32_t* ids, int T, 
                            int K, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
                            void* x_perm, int32_t* ws_words, int4* mtile_table,
                            int32_t* num_mtiles, int bm, const float* gate_w, float* row_w,
-                           cudaStream_t s) {
+                           cudaStream_t s, int32_t* zero_word) {
   if (T > 0 && T <= kSmallMaxT)
     return launch_small(dtype, x, ids, nullptr, T, H, E, K, counts, offsets, perm, inv, x_perm,
-                        mtile_table, num_mtiles, bm, gate_w, row_w, s);
+                        mtile_table, num_mtiles, bm, gate_w, row_w, zero_word, s);
   const int nb = (T + kRankTokens - 1) / kRankTokens;
   if (nb > 0) {
     cudaError_t err = launch_pdl(permute_rank_kernel, dim3(nb), dim3(kRankTokens),
@@ -447,7 +451,7 @@ cudaError_t launch_permute(int dtype, const void* x, const int32_t* ids, int T, 
     if (err != cudaSuccess) return err;
   }
   cudaError_t err = launch_pdl(permute_scan_kernel, dim3(1), dim3(kScanThreads), 0, s, ws_words,
-                               nb, E, counts, offsets, mtile_table, num_mtiles, bm);
+                               nb, E, counts, offsets, mtile_table, num_mtiles, bm, zero_word);
   if (err != cudaSuccess || T == 0) return err;
   const int row_units = static_cast<int>(static_cast<size_t>(H) * act_bytes(dtype) / 16);
   return launch_pdl(permute_scatter_kernel, dim3((T + kScatterWarps - 1) / kScatterWarps),
