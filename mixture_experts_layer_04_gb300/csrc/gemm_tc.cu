@@ -453,9 +453,9 @@ __device__ __forceinline__ void epilogue_rows(const TcParams& p, uint32_t t_row,
       uint32_t pk[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        const float h0 = silu_f(__uint_as_float(gr[2 * j])) * __uint_as_float(ur[2 * j]);
+        const float h0 = silu_bf16out(__uint_as_float(gr[2 * j])) * __uint_as_float(ur[2 * j]);
         const float h1 =
-            silu_f(__uint_as_float(gr[2 * j + 1])) * __uint_as_float(ur[2 * j + 1]);
+            silu_bf16out(__uint_as_float(gr[2 * j + 1])) * __uint_as_float(ur[2 * j + 1]);
         pk[j] = pack_bf16x2(h0, h1);
       }
 #pragma unroll
@@ -479,9 +479,17 @@ __device__ __forceinline__ void epilogue_rows(const TcParams& p, uint32_t t_row,
     // kScatter: this thread's row is scaled by its route weight and added into the
     // output row of its token (the fused combine); other rows are stored as they are
     float rw = 1.f;
+    // kScatter: the destination (token) rows of the rows this lane stores in the passes
+    // below (row 4 pass + lane / 8 of the warp's 32), loaded once per tile
+    int tok[8];
     if constexpr (MODE == kScatter) {
       const int grow = tile_row0 + lane;
       rw = grow < row_end ? __ldg(p.row_w + grow) : 0.f;
+#pragma unroll
+      for (int pass = 0; pass < 8; ++pass) {
+        const int gr = tile_row0 + pass * 4 + (lane >> 3);
+        tok[pass] = gr < row_end ? __ldg(p.row_token + gr) : 0;
+      }
     }
     // FP8 operands: this thread's row scale and the group's output-channel scales, the
     // latter for every chunk at once
@@ -537,9 +545,9 @@ __device__ __forceinline__ void epilogue_rows(const TcParams& p, uint32_t t_row,
         const int col = col0 + c + u * 4;
         if (grow < row_end && col < p.N_out) {
           if constexpr (MODE == kScatter) {
-            const int tok = __ldg(p.row_token + grow);
-            if (dcheck(tok >= 0 && (p.c_rows == 0 || tok < p.c_rows), p.err))
-              red_add_v4(C + static_cast<size_t>(tok) * p.N_out + col, v);
+            const int t = tok[pass];
+            if (dcheck(t >= 0 && (p.c_rows == 0 || t < p.c_rows), p.err))
+              red_add_v4(C + static_cast<size_t>(t) * p.N_out + col, v);
           } else {
             *reinterpret_cast<uint4*>(C + static_cast<size_t>(grow) * p.N_out + col) = v;
           }
@@ -986,7 +994,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (tok < row_end && col < p.N_out) {
                   const float u = xchg[r * BN + ((c + j + r) % BN)];
                   C[static_cast<size_t>(tok) * p.N_out + col] =
-                      __float2bfloat16_rn(silu_f(v[j]) * u);
+                      __float2bfloat16_rn(silu_bf16out(v[j]) * u);
                 }
               }
             }
@@ -1125,7 +1133,7 @@ __device__ __forceinline__ void epilogue_pair_tail(const TcParams& p, uint32_t t
           const int tok = row0 + c + j;
           if (tok < row_end && col < p.N_out) {
             const float u = xchg[L * 32 + ((j + L) & 31)];
-            C[static_cast<size_t>(tok) * p.N_out + col] = __float2bfloat16_rn(silu_f(v[j]) * u);
+            C[static_cast<size_t>(tok) * p.N_out + col] = __float2bfloat16_rn(silu_bf16out(v[j]) * u);
           }
         }
       }
