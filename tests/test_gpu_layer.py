@@ -470,3 +470,55 @@ def test_shared_expert_on_side_stream_matches_in_order_layer(moe, fused):
     L32 = r["logits"][toks]
     amb = H.ambiguous_tokens(L32, shape.K, shape.theta, ref["w"])
     H.assert_close_y(eager.y32.double().cpu().numpy()[toks][~amb], ref["y"][~amb])
+
+
+@pytest.mark.parametrize("fill", [0x00, 0xFF, 0x7F], ids=["zeros", "ones", "large"])
+def test_workspace_contents_do_not_matter(moe, fill):
+    """Every workspace field a call reads is written by that call first.  In particular the
+    tile counter of the routed gate/up GEMM on CTA pairs (tiles drawn in index order) is
+    zeroed by the call's permutation kernel (the layer) or a memset (the standalone call):
+    a stale or garbage counter would make the pairs skip tiles.  The layer's shape puts the
+    gate/up on CTA pairs (512 rows per expert)."""
+    shape = synth.MoEShape("wsfill", T=2048, H=512, E=32, K=8, I=256, I_shared=128, theta=0.0,
+                           bias="normal", seed=21)
+    inp = synth.make_inputs(shape, device="cuda")
+    clean = H.LayerRun(moe, shape, inp)
+    clean.ws.zero_()
+    clean.run()
+    run = H.LayerRun(moe, shape, inp)
+    run.ws.fill_(fill)
+    run.run()
+    run.run()  # and again on the workspace the first call left behind
+    moe.sync_check()
+    assert torch.equal(run.y, clean.y) and torch.equal(run.y32, clean.y32)
+    # the standalone gate/up on the same routing, with a filled workspace
+    r = clean.routing()
+    T, K = shape.T, shape.K
+    x_perm = clean.view("x_perm", (T * K, shape.H), torch.bfloat16).clone()
+    offsets = torch.from_numpy(r["offsets"]).cuda()
+    h_clean = torch.empty(T * K, shape.I, dtype=torch.bfloat16, device="cuda")
+    h_fill = torch.empty_like(h_clean)
+    ws2 = torch.full_like(run.ws, fill)
+    moe.expert_gate_up(clean.cfg, x_perm, offsets, inp["w_gate_up"], h_clean, clean.ws)
+    moe.expert_gate_up(clean.cfg, x_perm, offsets, inp["w_gate_up"], h_fill, ws2)
+    moe.sync_check()
+    M = int(r["offsets"][-1])
+    assert torch.equal(h_fill[:M], h_clean[:M])
+    # the FP8 layer, whose permutation zeroes the same counter
+    E, I, Hd = shape.E, shape.I, shape.H
+    wq = torch.empty(E, 2 * I, Hd, dtype=torch.uint8, device="cuda")
+    wsc = torch.empty(E, 2 * I, device="cuda")
+    moe.quantize_fp8(inp["w_gate_up"].reshape(E * 2 * I, Hd), wq, wsc)
+    wdq = torch.empty(E, Hd, I, dtype=torch.uint8, device="cuda")
+    wds = torch.empty(E, Hd, device="cuda")
+    moe.quantize_fp8(inp["w_down"].reshape(E * Hd, I), wdq, wds)
+    cfg8 = moe.MoEConfig.make(T, Hd, E, K, I, shape.I_shared, shape.theta, moe.BF16, moe.FLAG_FP8)
+    outs = []
+    for f in (0x00, fill):
+        ws8 = torch.full((moe.workspace_size(cfg8),), f, dtype=torch.uint8, device="cuda")
+        y8 = torch.empty(T, Hd, dtype=torch.bfloat16, device="cuda")
+        moe.layer_forward_fp8(cfg8, inp["x"], inp["w_router"], inp["router_bias"], wq, wsc, wdq,
+                              wds, inp["w_shared_gate_up"], inp["w_shared_down"], y8, None, ws8)
+        outs.append(y8)
+    moe.sync_check()
+    assert torch.equal(outs[0], outs[1])
