@@ -476,73 +476,89 @@ __device__ __forceinline__ void epilogue_rows(const TcParams& p, uint32_t t_row,
     }
   } else {
     float* C = static_cast<float*>(p.C);
-    // kScatter: this thread's row is scaled by its route weight and added into the
-    // output row of its token (the fused combine); other rows are stored as they are
-    float rw = 1.f;
-    // kScatter: the destination (token) rows of the rows this lane stores in the passes
-    // below (row 4 pass + lane / 8 of the warp's 32), loaded once per tile
+    // The scaling is applied after the transpose through shared memory, where each lane
+    // holds 4 consecutive columns of one row per pass: row r = 4 pass + lane / 8 of the
+    // warp's 32, columns 4 (lane % 8) .. + 3 of the chunk.  A lane then needs one factor per
+    // pass (loaded once per tile) and four column factors per chunk, and no shuffles.
+    //   kScatter: the row is scaled by its route weight and added into the output row of
+    //             its token (the fused combine);
+    //   FP8:      the row's token-row scale and the columns' weight-row scales;
+    //   bias:     added per column after the scaling.
+    const bool f8 = p.a_scale != nullptr;
+    const bool row_scaled = MODE == kScatter || f8;
+    const float* sb = f8 ? p.b_scale + static_cast<size_t>(group) * p.b_rows : nullptr;
+    float rsc[8];
     int tok[8];
-    if constexpr (MODE == kScatter) {
-      const int grow = tile_row0 + lane;
-      rw = grow < row_end ? __ldg(p.row_w + grow) : 0.f;
 #pragma unroll
-      for (int pass = 0; pass < 8; ++pass) {
-        const int gr = tile_row0 + pass * 4 + (lane >> 3);
-        tok[pass] = gr < row_end ? __ldg(p.row_token + gr) : 0;
+    for (int pass = 0; pass < 8; ++pass) {
+      const int gr = tile_row0 + pass * 4 + (lane >> 3);
+      const bool live = gr < row_end;
+      float f = 1.f;
+      tok[pass] = 0;
+      if constexpr (MODE == kScatter) {
+        f = live ? __ldg(p.row_w + gr) : 0.f;
+        tok[pass] = live ? __ldg(p.row_token + gr) : 0;
       }
+      if (f8) f *= live ? __ldg(p.a_scale + gr) : 0.f;
+      rsc[pass] = f;
     }
-    // FP8 operands: this thread's row scale and the group's output-channel scales, the
-    // latter for every chunk at once
-    const float* sb = nullptr;
+    const int u = lane & 7;
+    // FP8: this lane's four columns' weight-row scales for every chunk, loaded once per
+    // tile (their latency is then paid once, not once per chunk)
     constexpr int kChunks = BN / 32;
-    float scv[kChunks];
-    if (p.a_scale != nullptr) {
-      rw *= tile_row0 + lane < row_end ? __ldg(p.a_scale + tile_row0 + lane) : 0.f;
-      sb = p.b_scale + static_cast<size_t>(group) * p.b_rows;
+    float csv[kChunks][4];
+    if (f8) {
 #pragma unroll
-      for (int k = 0; k < kChunks; ++k) {
-        const int cl = col0 + 32 * k + lane;
-        scv[k] = cl < p.N_out ? __ldg(sb + cl) : 0.f;
-      }
+      for (int k = 0; k < kChunks; ++k)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int cl = col0 + 32 * k + u * 4 + q;
+          csv[k][q] = cl < p.N_out ? __ldg(sb + cl) : 0.f;
+        }
     }
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       uint32_t r[32];
       tmem_ld_32x32b_x32(t_row + c, r);
-      tmem_ld_wait();
-      if (sb != nullptr) {
-        float sc = 0.f;
+      // this lane's four columns' weight-row scales and biases for the chunk
+      const int col = col0 + c + u * 4;
+      float cs[4] = {1.f, 1.f, 1.f, 1.f}, bs[4] = {0.f, 0.f, 0.f, 0.f};
+      if (f8) {
 #pragma unroll
         for (int k = 0; k < kChunks; ++k)
-          if (32 * k == c) sc = scv[k];
-        const float rs = MODE == kScatter ? 1.f : rw;  // kScatter applies rw below
+          if (32 * k == c) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          r[j] = __float_as_uint(__uint_as_float(r[j]) * (rs * __shfl_sync(0xffffffffu, sc, j)));
-      }
-      if constexpr (MODE == kScatter) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * rw);
+            for (int q = 0; q < 4; ++q) cs[q] = csv[k][q];
+          }
       }
       if (p.col_bias != nullptr) {
-        // one coalesced load of the chunk's 32 biases, then broadcast by shuffles
-        const int bc = col0 + c + lane;
-        const float bl = bc < p.N_out ? __ldg(p.col_bias + bc) : 0.f;
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          r[j] = __float_as_uint(__uint_as_float(r[j]) + __shfl_sync(0xffffffffu, bl, j));
+        for (int q = 0; q < 4; ++q) bs[q] = col + q < p.N_out ? __ldg(p.col_bias + col + q) : 0.f;
       }
+      tmem_ld_wait();
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        st_shared_v4(stg + stg_off<128>(lane, u), r[4 * u], r[4 * u + 1], r[4 * u + 2],
-                     r[4 * u + 3]);
+      for (int w = 0; w < 8; ++w)
+        st_shared_v4(stg + stg_off<128>(lane, w), r[4 * w], r[4 * w + 1], r[4 * w + 2],
+                     r[4 * w + 3]);
       __syncwarp();
 #pragma unroll
       for (int pass = 0; pass < 8; ++pass) {
-        const int rr = pass * 4 + (lane >> 3), u = lane & 7;
-        const uint4 v = ld_shared_v4(stg + stg_off<128>(rr, u));
+        const int rr = pass * 4 + (lane >> 3);
+        uint4 v = ld_shared_v4(stg + stg_off<128>(rr, u));
+        if (row_scaled) {
+          const float f = rsc[pass];
+          v.x = __float_as_uint(__uint_as_float(v.x) * (f * cs[0]));
+          v.y = __float_as_uint(__uint_as_float(v.y) * (f * cs[1]));
+          v.z = __float_as_uint(__uint_as_float(v.z) * (f * cs[2]));
+          v.w = __float_as_uint(__uint_as_float(v.w) * (f * cs[3]));
+        }
+        if (p.col_bias != nullptr) {
+          v.x = __float_as_uint(__uint_as_float(v.x) + bs[0]);
+          v.y = __float_as_uint(__uint_as_float(v.y) + bs[1]);
+          v.z = __float_as_uint(__uint_as_float(v.z) + bs[2]);
+          v.w = __float_as_uint(__uint_as_float(v.w) + bs[3]);
+        }
         const int grow = tile_row0 + rr;
-        const int col = col0 + c + u * 4;
         if (grow < row_end && col < p.N_out) {
           if constexpr (MODE == kScatter) {
             const int t = tok[pass];
