@@ -101,7 +101,19 @@ struct TcParams {
   int c_rows;  // kScatter: rows of C, 0 = unknown (both checked in the debug build only)
 };
 
-template <int BN, int MODE, bool SWAP>
+// Epilogue warps of a single-CTA launch: FP8 plain / scatter tiles in the normal order
+// take eight (two per TMEM lane quarter, each draining every other 32-column chunk): their
+// MMAs take half the time of bf16 ones, and with four warps the fp32 epilogue set the pace
+// (a per-tile timeline at the Qwen3 shape: MMA 1.9 us, epilogue 3.8-4.9 us per tile; the
+// FP8 layer went from 530 to 508 us with eight).
+__host__ __device__ constexpr int tc_epi_warps(int MODE, bool SWAP, bool F8) {
+  return (F8 && !SWAP && (MODE == kPlain || MODE == kScatter)) ? 8 : kEpiWarps;
+}
+__host__ __device__ constexpr int tc_threads(int MODE, bool SWAP, bool GATHER, bool F8) {
+  return 64 + 32 * tc_epi_warps(MODE, SWAP, F8) + (GATHER ? 32 : 0);
+}
+
+template <int BN, int MODE, bool SWAP, int EPI = kEpiWarps>
 struct TcCfg {
   static constexpr int kActRows = SWAP ? BN : 128;   // token rows per tile
   static constexpr int kWgtRows = SWAP ? 128 : BN;   // weight rows per tile
@@ -112,7 +124,7 @@ struct TcCfg {
   static constexpr int kColsOut = MODE == kSwiGLU ? kWgtRows / 2 : kWgtRows; // outputs per tile
   static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
   static constexpr int kStgBytes =
-      SWAP ? (MODE == kSwiGLU ? 64 * BN * 4 : 0) : kEpiWarps * 32 * (MODE == kSwiGLU ? 64 : 128);
+      SWAP ? (MODE == kSwiGLU ? 64 * BN * 4 : 0) : EPI * 32 * (MODE == kSwiGLU ? 64 : 128);
   static constexpr int kBarBytes = 256;
   static constexpr int kSchedBytes = 3 * (kMaxGroups + 4) * 4 + 32 * 4;
   // as many stages as shared memory holds (up to 12): the bytes a CTA keeps in flight set
@@ -410,7 +422,7 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[32]) {
 template <int BN, int MODE>
 __device__ __forceinline__ void epilogue_rows(const TcParams& p, uint32_t t_row, uint32_t stg,
                                               int lane, int tile_row0, int row_end, int col0,
-                                              int group = 0) {
+                                              int group = 0, int c_first = 0, int c_step = 32) {
   if constexpr (MODE == kSwiGLU) {
     __nv_bfloat16* C = static_cast<__nv_bfloat16*>(p.C);
     // FP8 operands: this thread's token-row scale, and the group's weight-row scales
@@ -517,7 +529,7 @@ __device__ __forceinline__ void epilogue_rows(const TcParams& p, uint32_t t_row,
         }
     }
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
+    for (int c = c_first; c < BN; c += c_step) {
       uint32_t r[32];
       tmem_ld_32x32b_x32(t_row + c, r);
       // this lane's four columns' weight-row scales and biases for the chunk
@@ -698,13 +710,14 @@ __device__ __forceinline__ void epilogue_topk(const TcParams& p, uint32_t t_row,
 }
 
 template <int BN, int MODE, bool SWAP, bool GATHER, bool F8 = false>
-__global__ void __launch_bounds__(kThreads + 32, 1)
+__global__ void __launch_bounds__(tc_threads(MODE, SWAP, GATHER, F8), 1)
     tc_grouped_gemm_kernel(const __grid_constant__ TcParams p) {
+  constexpr int kEpi = tc_epi_warps(MODE, SWAP, F8);
   // With a row gather two producer warps (0 and 2 + kEpiWarps) take alternate k-steps: the
   // gather's many small requests then come from two warps (decode at one token: layer
   // 41.5 -> 39.6 us on GB300; without a gather a second producer measured no faster).
   constexpr int kProducers = GATHER ? 2 : 1;
-  using Cfg = TcCfg<BN, MODE, SWAP>;
+  using Cfg = TcCfg<BN, MODE, SWAP, kEpi>;
   constexpr int S = Cfg::kStages;
   constexpr int kKStep = F8 ? 128 : BK;  // elements per 128-byte k-step
   constexpr int kTileRows = Cfg::kActRows;
@@ -740,7 +753,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), kEpiWarps);
+      mbar_init(tempty_bar(a), kEpi);
     }
     mbar_init(mma_done_bar, 1);
     *abort_flag = 0;
@@ -765,7 +778,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
   const Sched sc = build_schedule(p, s_off, s_mt, s_light, s_scan, kTileRows);
   const int total = sc.total;
 
-  if (warp == 0 || (kProducers == 2 && warp == 2 + kEpiWarps)) {
+  if (warp == 0 || (kProducers == 2 && warp == 2 + kEpi)) {
     const int pid = warp == 0 ? 0 : 1;
     // ------------------------------------------------------------ producer ----
     // One elected lane waits for a free stage, arms its barrier and loads the weight and
@@ -923,7 +936,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     // ------------------------------------------------------------ epilogue ----
     const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
     clear_share(p, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x),
-                static_cast<int>(threadIdx.x) - 64, 32 * kEpiWarps);
+                static_cast<int>(threadIdx.x) - 64, 32 * kEpi);
     int local = 0;
     for (int idx = blockIdx.x; idx < total; idx += gridDim.x, ++local) {
       int g, row0, row_end, n_tile;
@@ -955,7 +968,8 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
           else
             epilogue_topk<BN, 16>(p, t_row, stg, lane, tile_row0, row_end);
         } else
-          epilogue_rows<BN, MODE>(p, t_row, stg, lane, tile_row0, row_end, col0, g);
+          epilogue_rows<BN, MODE>(p, t_row, stg, lane, tile_row0, row_end, col0, g,
+                                  32 * ((warp - 2) / 4), 32 * (kEpi / 4));
       } else {
         // swapped: lane = weight row of the tile, column j = token row0 + j
         // FP8 operands: the token-row scales of every chunk, loaded before the chunk loops
@@ -1590,7 +1604,7 @@ bool make_map_4d_halves(CUtensorMap* m, const void* base, uint64_t G, uint64_t h
 template <int BN, int MODE, bool SWAP, bool GATHER = false, bool F8 = false>
 cudaError_t launch_one(const GroupedGemm& g, unsigned* err, int num_sms, cudaStream_t s,
                        const float* a_scale = nullptr, const float* b_scale = nullptr) {
-  using Cfg = TcCfg<BN, MODE, SWAP>;
+  using Cfg = TcCfg<BN, MODE, SWAP, tc_epi_warps(MODE, SWAP, F8)>;  // the kernel's own layout
   auto kernel = tc_grouped_gemm_kernel<BN, MODE, SWAP, GATHER, F8>;
   if (GATHER != (g.gather_rows != nullptr)) return cudaErrorInvalidValue;
   static int attr_set_dev = -1;  // the attribute is per function and device
@@ -1650,7 +1664,7 @@ cudaError_t launch_one(const GroupedGemm& g, unsigned* err, int num_sms, cudaStr
   const long long max_tiles = max_mt * p.n_tiles;
   if (max_tiles == 0) return cudaSuccess;
   return launch_pdl(kernel, dim3(static_cast<unsigned>(max_tiles < num_sms ? max_tiles : num_sms)),
-                    dim3(GATHER ? kThreads + 32 : kThreads), Cfg::kSmem, s, p);
+                    dim3(tc_threads(MODE, SWAP, GATHER, F8)), Cfg::kSmem, s, p);
 }
 
 
