@@ -238,8 +238,8 @@ moe_status_t moe_layer_forward_fp8(const moe_config_t* cfg, const void* x, const
  * bits to save memory).  Reading: E4M3, the 8-bit format the tensor cores run at full rate,
  * one float32 scale per row.  For every row r:
  *   scales[r] = max_c |in[r,c]| / 448 (1 for an all-zero row), float32;
- *   codes[r,c] = E4M3(in[r,c] / scales[r]) (float32 division, round to nearest even,
- *   saturating at +-448), one byte each.
+ *   codes[r,c] = E4M3(in[r,c] * (1 / scales[r])) (the reciprocal and the product each
+ *   rounded to float32, then round to nearest even, saturating at +-448), one byte each.
  *   in [rows, cols] bf16 (device); codes [rows, cols] uint8 out; scales [rows] float out.
  *   cols % 8 == 0; rows >= 0.  Expert weights quantise as rows = E*2I (gate/up, per output
  *   channel); token rows as rows = T*K (the permuted x). */

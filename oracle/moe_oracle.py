@@ -286,13 +286,15 @@ def quantize_e4m3(v32):
 
 def quantize_rows_fp8(a):
     """Per-row E4M3 quantisation of a [rows, cols] matrix: scale = amax(|row|) / 448 in
-    float32 (1 for an all-zero row) and codes = E4M3(row / scale), the division in float32
-    (the precision the kernels take this decision in).  Returns (codes as float64 values,
-    scales as float32), with row ~= codes * scale."""
+    float32 (1 for an all-zero row) and codes = E4M3(row * (1 / scale)): the reciprocal of
+    the scale and the product, each rounded to float32, which is the precision the kernels
+    take this decision in (the page fixes none).  Returns (codes as float64 values, scales
+    as float32), with row ~= codes * scale."""
     a32 = np.asarray(a, dtype=np.float32)
     amax = np.abs(a32).max(axis=1)
     scale = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
-    codes = quantize_e4m3((a32 / scale[:, None]).astype(np.float32))
+    inv = (np.float32(1.0) / scale).astype(np.float32)
+    codes = quantize_e4m3((a32 * inv[:, None]).astype(np.float32))
     return codes, scale
 
 
