@@ -63,6 +63,62 @@ __global__ void __launch_bounds__(kQThreads)
   }
 }
 
+// The same for rows of up to 32 * 8 * U values, read once: each lane keeps its U 16-byte
+// units of the row in registers (all loads issued before the first use) for the amax and
+// the conversion, instead of reading the row a second time.
+template <int U>
+__global__ void __launch_bounds__(kQThreads)
+    quantize_rows_fp8_reg_kernel(const __nv_bfloat16* __restrict__ in, long long rows, int cols,
+                                 uint8_t* __restrict__ codes, float* __restrict__ scales) {
+  grid_dep_wait();
+  grid_dep_trigger();
+  const int lane = threadIdx.x & 31;
+  const int units = cols / 8;
+  const long long warps = static_cast<long long>(gridDim.x) * (kQThreads / 32);
+  for (long long r = blockIdx.x * (kQThreads / 32) + (threadIdx.x >> 5); r < rows; r += warps) {
+    const uint4* src = reinterpret_cast<const uint4*>(in + r * cols);
+    uint4 v[U];
+#pragma unroll
+    for (int i = 0; i < U; ++i) {
+      const int u = lane + 32 * i;
+      v[i] = u < units ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < U; ++i) {
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v[i]);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = __bfloat1622float2(h[q]);
+        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float scale = amax > 0.f ? amax / 448.f : 1.f;
+    const float inv = 1.f / scale;  // correctly rounded: an IEEE division, once per row
+    if (lane == 0) scales[r] = scale;
+    uint2* dst = reinterpret_cast<uint2*>(codes + r * cols);
+#pragma unroll
+    for (int i = 0; i < U; ++i) {
+      const int u = lane + 32 * i;
+      if (u < units) {
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v[i]);
+        auto four = [&](int k) {  // values 4k .. 4k+3 of the unit as four codes
+          const float2 a = __bfloat1622float2(h[2 * k]);
+          const float2 b = __bfloat1622float2(h[2 * k + 1]);
+          const uint32_t lo = __nv_cvt_float2_to_fp8x2(
+              make_float2(__fmul_rn(a.x, inv), __fmul_rn(a.y, inv)), __NV_SATFINITE, __NV_E4M3);
+          const uint32_t hi = __nv_cvt_float2_to_fp8x2(
+              make_float2(__fmul_rn(b.x, inv), __fmul_rn(b.y, inv)), __NV_SATFINITE, __NV_E4M3);
+          return lo | (hi << 16);
+        };
+        dst[u] = make_uint2(four(0), four(1));
+      }
+    }
+  }
+}
+
 // dst[r] = src[perm[r]] for the dispatched rows r < offsets_end[0], 0 for the rest: the
 // token-row scales in the permuted row order.
 __global__ void __launch_bounds__(kQThreads)
@@ -92,8 +148,20 @@ cudaError_t launch_quantize_fp8(const void* in, long long rows, int cols, uint8_
   if (cols % 8 != 0) return cudaErrorInvalidValue;
   const long long want = (rows + kQThreads / 32 - 1) / (kQThreads / 32);
   const unsigned blocks = static_cast<unsigned>(want < 8192 ? want : 8192);
-  return launch_pdl(quantize_rows_fp8_kernel, dim3(blocks), dim3(kQThreads), 0, s,
-                    static_cast<const __nv_bfloat16*>(in), rows, cols, codes, scales);
+  const auto* src = static_cast<const __nv_bfloat16*>(in);
+  const int per_lane = (cols / 8 + 31) / 32;  // 16-byte units per lane
+  if (per_lane <= 4)
+    return launch_pdl(quantize_rows_fp8_reg_kernel<4>, dim3(blocks), dim3(kQThreads), 0, s, src,
+                      rows, cols, codes, scales);
+  if (per_lane <= 8)
+    return launch_pdl(quantize_rows_fp8_reg_kernel<8>, dim3(blocks), dim3(kQThreads), 0, s, src,
+                      rows, cols, codes, scales);
+  // (9-16 units per lane, e.g. H = 4096, measured about 8% slower read once than twice)
+  if (per_lane > 16 && per_lane <= 28)  // H = 7168: 896 units, 2.82 GB in 541 us against 640
+    return launch_pdl(quantize_rows_fp8_reg_kernel<28>, dim3(blocks), dim3(kQThreads), 0, s, src,
+                      rows, cols, codes, scales);
+  return launch_pdl(quantize_rows_fp8_kernel, dim3(blocks), dim3(kQThreads), 0, s, src, rows,
+                    cols, codes, scales);
 }
 
 }  // namespace moe
