@@ -1056,6 +1056,17 @@ __global__ void __launch_bounds__(tc_threads(MODE, SWAP, GATHER, F8), 1)
           for (int c = 0; c < BN; c += kNC) {
             float v[32];
             tmem_ld_cols<kNC>(t_row + c, v);
+            // kScatter: lane j loads row c + j's token and route weight; shuffles hand
+            // them out
+            int tok_l = 0;
+            float w_l = 0.f;
+            if constexpr (MODE == kScatter) {
+              const int rl = row0 + c + lane;
+              if (lane < kNC && rl < row_end) {
+                tok_l = __ldg(p.row_token + rl);
+                w_l = __ldg(p.row_w + rl);
+              }
+            }
             if (p.a_scale != nullptr) {
               const float sx = chunk_sx(c);
 #pragma unroll
@@ -1064,12 +1075,16 @@ __global__ void __launch_bounds__(tc_threads(MODE, SWAP, GATHER, F8), 1)
 #pragma unroll
             for (int j = 0; j < kNC; ++j) {
               const int row = row0 + c + j;
+              int tok = 0;
+              float wj = 0.f;
+              if constexpr (MODE == kScatter) {
+                tok = __shfl_sync(0xffffffffu, tok_l, j);
+                wj = __shfl_sync(0xffffffffu, w_l, j);
+              }
               if (row < row_end && col < p.N_out) {
                 if constexpr (MODE == kScatter) {
-                  const int tok = __ldg(p.row_token + row);
                   if (dcheck(tok >= 0 && (p.c_rows == 0 || tok < p.c_rows), p.err))
-                    red_add_f32(C + static_cast<size_t>(tok) * p.N_out + col,
-                                __ldg(p.row_w + row) * v[j]);
+                    red_add_f32(C + static_cast<size_t>(tok) * p.N_out + col, wj * v[j]);
                 } else {
                   C[static_cast<size_t>(row) * p.N_out + col] = v[j] + b;
                 }
@@ -1192,16 +1207,30 @@ __device__ __forceinline__ void epilogue_pair_tail(const TcParams& p, uint32_t t
     for (int c = 0; c < tn; c += 32) {
       float v[32];
       tmem_ld_cols<32>(t_row + c, v);
+      // kScatter: lane j loads row c + j's token and route weight; shuffles hand them out
+      int dst_l = 0;
+      float w_l = 0.f;
+      if constexpr (MODE == kScatter) {
+        const int tk = row0 + c + lane;
+        if (tk < row_end) {
+          dst_l = __ldg(p.row_token + tk);
+          w_l = __ldg(p.row_w + tk);
+        }
+      }
       scale(v, c, sw);
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const int tok = row0 + c + j;
+        int dst = 0;
+        float wj = 0.f;
+        if constexpr (MODE == kScatter) {
+          dst = __shfl_sync(0xffffffffu, dst_l, j);
+          wj = __shfl_sync(0xffffffffu, w_l, j);
+        }
         if (tok < row_end && col < p.N_out) {
           if constexpr (MODE == kScatter) {
-            const int dst = __ldg(p.row_token + tok);
             if (dcheck(dst >= 0 && (p.c_rows == 0 || dst < p.c_rows), p.err))
-              red_add_f32(C + static_cast<size_t>(dst) * p.N_out + col,
-                          __ldg(p.row_w + tok) * v[j]);
+              red_add_f32(C + static_cast<size_t>(dst) * p.N_out + col, wj * v[j]);
           } else {
             C[static_cast<size_t>(tok) * p.N_out + col] = v[j] + b;
           }

@@ -359,15 +359,19 @@ def _e4m3_bytes(values):
         torch.uint8).numpy()
 
 
-def test_quantize_fp8_bit_exact(moe):
+# row lengths that take each of the quantiser's paths: rows held in registers (up to 4 or
+# 8 16-byte units per lane, or 17-28 as at H = 7168) and rows read twice (4096, 14336)
+@pytest.mark.parametrize("cols", [384, 2048, 4096, 7168, 14336, 72])
+def test_quantize_fp8_bit_exact(moe, cols):
     gen = torch.Generator().manual_seed(31)
-    a = torch.randn(300, 384, generator=gen) * torch.rand(300, 1, generator=gen) * 20
+    rows = 300 if cols <= 4096 else 64
+    a = torch.randn(rows, cols, generator=gen) * torch.rand(rows, 1, generator=gen) * 20
     a[7] = 0.0                      # an all-zero row: scale 1
     a[11, 5] = 1e4                  # one large value: the rest of the row goes subnormal
-    a[13] = 1e-6 * torch.randn(384, generator=gen)
+    a[13] = 1e-6 * torch.randn(cols, generator=gen)
     x = a.to(torch.bfloat16).cuda()
-    codes = torch.full((300, 384), 0x55, dtype=torch.uint8, device="cuda")
-    scales = torch.full((300,), -1.0, dtype=torch.float32, device="cuda")
+    codes = torch.full((rows, cols), 0x55, dtype=torch.uint8, device="cuda")
+    scales = torch.full((rows,), -1.0, dtype=torch.float32, device="cuda")
     moe.quantize_fp8(x, codes, scales)
     torch.cuda.synchronize()
     ref_codes, ref_scales = oracle.quantize_rows_fp8(x.float().cpu().numpy())
