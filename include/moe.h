@@ -103,7 +103,11 @@ typedef void* moe_stream_t; /* a cudaStream_t */
 /* Bytes of device workspace that moe_layer_forward, moe_permute and moe_grouped_ffn
  * need for `cfg` (the largest of the three).  The workspace is scratch: its contents
  * are undefined between calls, and it must not be shared by calls that may run
- * concurrently.  Returns MOE_ERR_INVALID_ARG for an unsupported config. */
+ * concurrently.  Among the intermediates, a call with more than 128 tokens keeps in it
+ * the counter from which the gate/up GEMM's CTA pairs draw their tiles; the call zeroes
+ * it first (in the permutation's launch, or with a memset in the standalone GEMM calls),
+ * so no state carries from one call to the next.  Returns MOE_ERR_INVALID_ARG for an
+ * unsupported config. */
 moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes);
 
 /* Router scores and routing.
