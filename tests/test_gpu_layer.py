@@ -522,3 +522,60 @@ def test_workspace_contents_do_not_matter(moe, fill):
         outs.append(y8)
     moe.sync_check()
     assert torch.equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("name", ["qwen_prefill"])
+def test_layer_fp8_full_size_sampled(moe, name):
+    """moe_layer_forward_fp8 at the full Qwen3 shape (T=8192: the FP8 gate/up on CTA pairs
+    with the dynamic tile order, the FP8 scatter-add down projection with eight epilogue
+    warps) against the oracle's FP8 expert chain on a few sampled tokens (the oracle
+    quantises the weights of every expert they use itself, about a second per expert, so
+    the sample is small; the tails of every group are covered by the bf16 full-size test).
+    The oracle routes from the layer's own fp32 logits (as the small FP8 test does)."""
+    shape = synth.WORKLOADS[name]
+    T, H_, E, K, I = shape.T, shape.H, shape.E, shape.K, shape.I
+    inp = synth.make_inputs(shape, device="cuda")
+    cfg = moe.MoEConfig.make(T, H_, E, K, I, shape.I_shared, shape.theta, moe.BF16,
+                             moe.FLAG_FP8 | moe.FLAG_FUSED_COMBINE)
+    ws = torch.empty(moe.workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    wgq = torch.empty(E, 2 * I, H_, dtype=torch.uint8, device="cuda")
+    wgs = torch.empty(E, 2 * I, dtype=torch.float32, device="cuda")
+    moe.quantize_fp8(inp["w_gate_up"].reshape(E * 2 * I, H_), wgq, wgs)
+    wdq = torch.empty(E, H_, I, dtype=torch.uint8, device="cuda")
+    wds = torch.empty(E, H_, dtype=torch.float32, device="cuda")
+    moe.quantize_fp8(inp["w_down"].reshape(E * H_, I), wdq, wds)
+    y = torch.empty(T, H_, dtype=torch.bfloat16, device="cuda")
+    y32 = torch.empty(T, H_, dtype=torch.float32, device="cuda")
+    moe.layer_forward_fp8(cfg, inp["x"], inp["w_router"], inp["router_bias"], wgq, wgs, wdq, wds,
+                          inp.get("w_shared_gate_up"), inp.get("w_shared_down"), y, y32, ws)
+    torch.cuda.synchronize()
+    moe.sync_check()
+    run = H.LayerRun(moe, shape, inp)  # only for its workspace views
+    run.cfg, run.ws = cfg, ws
+    r = run.routing()
+    _check_dispatch_properties(r, T, K, E)
+    ids_ref, w_ref = oracle.route(r["logits"].astype(np.float32), K, shape.theta)
+    np.testing.assert_array_equal(r["ids"], ids_ref)
+    toks = _sample_tokens(r, T, 2)
+    xc, xs = oracle.quantize_rows_fp8(inp["x"][toks].float().cpu().numpy())
+    wg_cache, wd_cache = {}, {}
+
+    def expert(e):
+        if e not in wg_cache:
+            wg_cache[e] = oracle.quantize_rows_fp8(inp["w_gate_up"][e].float().cpu().numpy())
+            wd_cache[e] = oracle.quantize_rows_fp8(inp["w_down"][e].float().cpu().numpy())
+        return wg_cache[e], wd_cache[e]
+
+    y_ref = np.zeros((len(toks), H_))
+    for i, t in enumerate(toks):
+        for k in range(K):
+            e = int(ids_ref[t, k])
+            if e < 0:
+                continue
+            (wgc, wgsr), (wdc, wdsr) = expert(e)
+            h = oracle.expert_gate_up_fp8(xc[i:i + 1], xs[i:i + 1], wgc, wgsr)
+            h = torch.from_numpy(h).to(torch.bfloat16).float().numpy()  # rounded once to bf16
+            hc, hsc = oracle.quantize_rows_fp8(h)
+            y_ref[i] += w_ref[t, k] * oracle.expert_down_fp8(hc, hsc, wdc, wdsr)[0]
+    H.assert_close_y(y32.double().cpu().numpy()[toks], y_ref, **_tol(shape))
+    assert torch.equal(y, y32.to(torch.bfloat16))
