@@ -524,14 +524,13 @@ def test_workspace_contents_do_not_matter(moe, fill):
     assert torch.equal(outs[0], outs[1])
 
 
-@pytest.mark.parametrize("name", ["qwen_prefill"])
+@pytest.mark.parametrize("name", ["qwen_prefill", "mixtral"])
 def test_layer_fp8_full_size_sampled(moe, name):
-    """moe_layer_forward_fp8 at the full Qwen3 shape (T=8192: the FP8 gate/up on CTA pairs
+    """moe_layer_forward_fp8 at full size (Qwen3 shape, T=8192: the FP8 gate/up on CTA pairs
     with the dynamic tile order, the FP8 scatter-add down projection with eight epilogue
-    warps) against the oracle's FP8 expert chain on a few sampled tokens (the oracle
-    quantises the weights of every expert they use itself, about a second per expert, so
-    the sample is small; the tails of every group are covered by the bf16 full-size test).
-    The oracle routes from the layer's own fp32 logits (as the small FP8 test does)."""
+    warps; Mixtral shape: both FP8 GEMMs on CTA pairs) against the oracle's FP8 expert chain on sampled tokens, every touched expert's
+    last row among them.  The oracle quantises the weights of every expert they use itself,
+    and routes from the layer's own fp32 logits (as the small FP8 test does)."""
     shape = synth.WORKLOADS[name]
     T, H_, E, K, I = shape.T, shape.H, shape.E, shape.K, shape.I
     inp = synth.make_inputs(shape, device="cuda")
@@ -556,7 +555,7 @@ def test_layer_fp8_full_size_sampled(moe, name):
     _check_dispatch_properties(r, T, K, E)
     ids_ref, w_ref = oracle.route(r["logits"].astype(np.float32), K, shape.theta)
     np.testing.assert_array_equal(r["ids"], ids_ref)
-    toks = _sample_tokens(r, T, 2)
+    toks = _sample_tokens(r, T, 8, tails=True)
     xc, xs = oracle.quantize_rows_fp8(inp["x"][toks].float().cpu().numpy())
     wg_cache, wd_cache = {}, {}
 
