@@ -53,7 +53,7 @@ namespace {
 constexpr int BK = 64;  // bf16 elements = 128 bytes = one swizzle row
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
-constexpr int kSwz = 16;  // token tiles per raster chunk
+constexpr int kSwz = 8;  // token tiles per raster chunk
 constexpr int kMaxGroups = 1024;
 
 struct TcParams {
