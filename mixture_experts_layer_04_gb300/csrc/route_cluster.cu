@@ -8,7 +8,19 @@
 // With a handful of tokens every step is latency-bound, and separate launches (router,
 // top-k, counting sort, row copy) cost more than their work.  Here a cluster of nc CTAs
 // (16 when the device allows it, else 8) does all of it, synchronised by cluster
-// barriers and distributed shared memory instead of global counters:
+// barriers and distributed shared memory instead of global counters.
+//
+// Up to kRdMaxT tokens (route_dispatch_dot_kernel), the logits are split by expert:
+//   1. CTA c takes experts [c*E/nc, (c+1)*E/nc); warp w of it computes an expert's full-H
+//      dot products with every token on the CUDA cores (the tokens staged in shared
+//      memory, the router row read straight into registers), adds the bias and stores the
+//      logit into every CTA's logit table through distributed shared memory.
+//   2. One cluster barrier: every CTA now holds all T x E logits, takes every token's
+//      top-k itself and runs step 3 below with no further exchange.
+//   At one token this saves two of the three cluster barriers and the 16-way partial
+//   sums (the routing of the Qwen3-shaped decode layer 12.5 -> 9.1 us); from 8 tokens on,
+//   the dot products on the CUDA cores cost more than that.
+// With more tokens (route_dispatch_cluster_kernel), the H dimension is split instead:
 //   1. CTA c computes the partial logits of its share of the H dimension on the tensor
 //      core: D[e][t] = sum over its k-blocks of W_r[e, k] x[t, k] (tcgen05.mma, experts
 //      on the 128-row side, tokens zero-padded to npad columns), TMA-fed, and parks
@@ -21,6 +33,9 @@
 //      counting sort (per-expert token bit masks, a block scan for the offsets, ranks by
 //      popcount), identically; CTA 0 stores counts, offsets, perm and inv; and, unless the
 //      caller gathers rows itself, every CTA copies some token rows into x_perm.
+// (Pushing the partials and the ids into the owners' shared memory with remote stores
+// instead, one barrier fewer, measured slower: 4-byte remote stores from the TMEM
+// read-out cost more than the loads they replace, 5 us more per layer at 64 tokens.)
 #include <cstring>
 
 #include "common.cuh"
@@ -37,6 +52,8 @@ constexpr int kRcMaxE = 256;
 constexpr int kRcMaxK = 16;
 constexpr int kRcMaxStages = 4;
 constexpr int kRcSmemBudget = 200 * 1024;
+constexpr int kRdMaxT = 4;    // tokens up to which the logits are CUDA-core dot products
+constexpr int kRdChunk = 8;   // 16-byte units of a router row each lane holds at a time
 
 struct RcParams {
   CUtensorMap tmX;  // x [T, H] bf16, box 64 columns x npad rows (rows >= T read as zero)
@@ -51,6 +68,7 @@ struct RcParams {
   int32_t* inv;     // [T*K]
   float* row_w;     // [T*K] gate of every row, or null
   const uint4* x;   // token rows (H*2/16 units each)
+  const uint4* wr;  // router rows (H*2/16 units each)
   uint4* x_perm;    // x_perm[r] = x[perm[r]], or null: rows not copied
   unsigned* err;
   int T, H, E, K;
@@ -103,6 +121,36 @@ __host__ __device__ inline RcLayout rc_layout(int npad, int nmt, int E, int K, i
   return L;
 }
 
+// Shared memory of the expert-split kernel: the tokens, the logit table, the top-k of every
+// token and the counting-sort scratch.
+struct RdLayout {
+  int x_off, ls_off, sid_off, sw_off, rows_off, masks_off, cnt_off, off_off, scratch_off, total;
+};
+
+__host__ __device__ inline RdLayout rd_layout(int T, int H, int E, int K) {
+  RdLayout L;
+  int o = 0;
+  L.x_off = o;
+  o = rc_align(o + T * H * 2, 16);
+  L.ls_off = o;
+  o = rc_align(o + T * E * 4, 16);
+  L.sid_off = o;
+  o = rc_align(o + T * K * 4, 16);
+  L.sw_off = o;
+  o = rc_align(o + T * K * 4, 16);
+  L.rows_off = o;
+  o = rc_align(o + T * K * 4, 16);
+  L.masks_off = o;
+  o = rc_align(o + E * 2 * 4, 16);
+  L.cnt_off = o;
+  o = rc_align(o + E * 4, 16);
+  L.off_off = o;
+  o = rc_align(o + (E + 1) * 4, 16);
+  L.scratch_off = o;
+  L.total = o + 32 * 4;
+  return L;
+}
+
 __device__ __forceinline__ float ld_dsmem_f32(uint32_t cluster_addr) {
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
@@ -113,10 +161,117 @@ __device__ __forceinline__ int ld_dsmem_s32(uint32_t cluster_addr) {
   asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
   return v;
 }
+// Bulk prefetch of `bytes` (a multiple of 16) at `src` (16-byte aligned) into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Split cluster barrier: arrive now, wait later (no memory ordering: it only tells a CTA
+// that every CTA of the cluster is running, before the first write into their shared memory).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
+// bf16 pair -> two floats (exact)
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t v) {
+  return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+}
+
 __device__ __forceinline__ uint32_t cluster_nctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
   return r;
+}
+
+// Step 3 of both kernels, once every CTA holds all T*K expert ids `aid` (-1: dropped)
+// and gates `agate` and has zeroed `masks`: the stable counting sort (redundantly in every
+// CTA), CTA 0's stores of counts, offsets, perm, inv and row_w, and the row copies, dealt
+// over the warps of the whole cluster.  No remote shared memory access.
+__device__ __forceinline__ void rc_sort_and_dispatch(const RcParams& p, int c, int nc,
+                                                     const int32_t* aid, const float* agate,
+                                                     uint32_t* masks, int* cnt, int* off,
+                                                     int32_t* rows, int* scratch) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int TK = p.T * p.K;
+  for (int a = tid; a < TK; a += kRcThreads) {
+    const int e = aid[a];
+    if (e >= 0) {
+      const int t = a / p.K;
+      atomicOr(&masks[2 * e + (t >> 5)], 1u << (t & 31));
+    }
+  }
+  __syncthreads();
+  int cnt_e = 0;
+  if (tid < p.E) cnt_e = __popc(masks[2 * tid]) + __popc(masks[2 * tid + 1]);
+  int M = 0;
+  const int base = block_exclusive_scan(cnt_e, scratch, &M);
+  if (tid < p.E) {
+    cnt[tid] = cnt_e;
+    off[tid] = base;
+  }
+  if (tid == 0) off[p.E] = M;
+  __syncthreads();
+  for (int a = tid; a < TK; a += kRcThreads) {
+    const int e = aid[a];
+    int row = -1;
+    if (e >= 0) {
+      const int t = a / p.K;
+      const uint32_t* m = masks + 2 * e;
+      int r = __popc(m[t >> 5] & ((1u << (t & 31)) - 1u));
+      if (t >= 32) r += __popc(m[0]);
+      row = off[e] + r;
+    }
+    rows[a] = row;
+  }
+  __syncthreads();
+  if (c == 0) {
+    for (int e = tid; e < p.E; e += kRcThreads) p.counts[e] = cnt[e];
+    for (int e = tid; e <= p.E; e += kRcThreads) p.offsets[e] = off[e];
+    for (int a = tid; a < TK; a += kRcThreads) {
+      const int r = rows[a];
+      p.inv[a] = r;
+      if (r >= 0) {
+        p.perm[r] = a / p.K;
+        if (p.row_w != nullptr) p.row_w[r] = agate[a];
+      }
+    }
+  }
+  // row copies: the T*K kept assignments are dealt to all warps of the cluster, two at a
+  // time per warp (both rows' loads in flight, then both rows' stores), so every SM of the
+  // cluster shares the stores; each lane moves 16-byte units in bursts of 4 per row
+  if (p.x_perm != nullptr) {
+    const int row_units = p.H / 8;
+    constexpr int kBurst = 4;
+    const int nw = nc * kRcWarps;
+    for (int a0 = c * kRcWarps + warp; a0 < TK; a0 += 2 * nw) {
+      const int a1 = a0 + nw;
+      const int r0 = rows[a0], r1 = a1 < TK ? rows[a1] : -1;
+      const uint4* s0 = p.x + static_cast<size_t>(a0 / p.K) * row_units;
+      const uint4* s1 = p.x + static_cast<size_t>((a1 < TK ? a1 : a0) / p.K) * row_units;
+      for (int i0 = 0; i0 < row_units; i0 += 32 * kBurst) {
+        uint4 v0[kBurst], v1[kBurst];
+#pragma unroll
+        for (int b = 0; b < kBurst; ++b) {
+          const int i = i0 + b * 32 + lane;
+          if (i < row_units) {
+            if (r0 >= 0) v0[b] = __ldg(s0 + i);
+            if (r1 >= 0) v1[b] = __ldg(s1 + i);
+          }
+        }
+#pragma unroll
+        for (int b = 0; b < kBurst; ++b) {
+          const int i = i0 + b * 32 + lane;
+          if (i < row_units) {
+            if (r0 >= 0) p.x_perm[static_cast<size_t>(r0) * row_units + i] = v0[b];
+            if (r1 >= 0) p.x_perm[static_cast<size_t>(r1) * row_units + i] = v1[b];
+          }
+        }
+      }
+    }
+  }
 }
 
 __global__ void __launch_bounds__(kRcThreads, 1)
@@ -321,88 +476,162 @@ __global__ void __launch_bounds__(kRcThreads, 1)
   }
   if (!dispatch) return;
 
-  for (int a = tid; a < TK; a += kRcThreads) {
-    const int e = aid[a];
-    if (e >= 0) {
-      const int t = a / p.K;
-      atomicOr(&masks[2 * e + (t >> 5)], 1u << (t & 31));
-    }
-  }
-  __syncthreads();
-  int cnt_e = 0;
-  if (tid < p.E) cnt_e = __popc(masks[2 * tid]) + __popc(masks[2 * tid + 1]);
-  int M = 0;
-  const int base = block_exclusive_scan(cnt_e, scratch, &M);
-  if (tid < p.E) {
-    cnt[tid] = cnt_e;
-    off[tid] = base;
-  }
-  if (tid == 0) off[p.E] = M;
-  __syncthreads();
-  for (int a = tid; a < TK; a += kRcThreads) {
-    const int e = aid[a];
-    int row = -1;
-    if (e >= 0) {
-      const int t = a / p.K;
-      const uint32_t* m = masks + 2 * e;
-      int r = __popc(m[t >> 5] & ((1u << (t & 31)) - 1u));
-      if (t >= 32) r += __popc(m[0]);
-      row = off[e] + r;
-    }
-    rows[a] = row;
-  }
-  __syncthreads();
-  if (c == 0) {
-    for (int e = tid; e < p.E; e += kRcThreads) p.counts[e] = cnt[e];
-    for (int e = tid; e <= p.E; e += kRcThreads) p.offsets[e] = off[e];
-    for (int a = tid; a < TK; a += kRcThreads) {
-      const int r = rows[a];
-      p.inv[a] = r;
-      if (r >= 0) {
-        p.perm[r] = a / p.K;
-        if (p.row_w != nullptr) p.row_w[r] = agate[a];
-      }
-    }
-  }
-  // row copies: the T*K kept assignments are dealt to all warps of the cluster, two at a
-  // time per warp (both rows' loads in flight, then both rows' stores), so every SM of the
-  // cluster shares the stores; each lane moves 16-byte units in bursts of 4 per row
-  if (p.x_perm != nullptr) {
-    const int row_units = p.H / 8;
-    constexpr int kBurst = 4;
-    const int nw = nc * kRcWarps;
-    for (int a0 = c * kRcWarps + warp; a0 < TK; a0 += 2 * nw) {
-      const int a1 = a0 + nw;
-      const int r0 = rows[a0], r1 = a1 < TK ? rows[a1] : -1;
-      const uint4* s0 = p.x + static_cast<size_t>(a0 / p.K) * row_units;
-      const uint4* s1 = p.x + static_cast<size_t>((a1 < TK ? a1 : a0) / p.K) * row_units;
-      for (int i0 = 0; i0 < row_units; i0 += 32 * kBurst) {
-        uint4 v0[kBurst], v1[kBurst];
+  rc_sort_and_dispatch(p, c, nc, aid, agate, masks, cnt, off, rows, scratch);
+}
+
+// Sums a[t] over the warp for NT (a power of two up to 32) values at once: at each of the
+// first log2(NT) butterfly steps a lane keeps half of its values and adds its partner's
+// copy of them, so the shuffles halve with the values (NT - 1 + 5 - log2(NT) in all).
+// Returns the full sum of value t_out, which the lane's bits 4, 3, ... select; the 32 / NT
+// lanes of a block of consecutive lanes share t_out and the same sum.
+template <int NT>
+__device__ __forceinline__ float warp_sum_scatter(float (&a)[NT], int lane, int& t_out) {
+  int t = 0;
 #pragma unroll
-        for (int b = 0; b < kBurst; ++b) {
-          const int i = i0 + b * 32 + lane;
-          if (i < row_units) {
-            if (r0 >= 0) v0[b] = __ldg(s0 + i);
-            if (r1 >= 0) v1[b] = __ldg(s1 + i);
+  for (int n = NT, o = 16; n > 1; n >>= 1, o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float keep = upper ? a[i + n / 2] : a[i];
+      const float send = upper ? a[i] : a[i + n / 2];
+      a[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+    if (upper) t += n / 2;
+  }
+  float v = a[0];
+#pragma unroll
+  for (int o = 16 / NT; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  t_out = t;
+  return v;
+}
+
+// NT: the token count rounded up to a power of two (the tokens from T on are zero rows).
+template <int NT>
+__global__ void __launch_bounds__(kRcThreads, 1)
+    route_dispatch_dot_kernel(const __grid_constant__ RcParams p) {
+  extern __shared__ __align__(16) uint8_t smem_rd[];
+  const RdLayout L = rd_layout(NT, p.H, p.E, p.K);
+  uint4* xs = reinterpret_cast<uint4*>(smem_rd + L.x_off);
+  float* Ls = reinterpret_cast<float*>(smem_rd + L.ls_off);
+  int32_t* sid = reinterpret_cast<int32_t*>(smem_rd + L.sid_off);
+  float* sw = reinterpret_cast<float*>(smem_rd + L.sw_off);
+  int32_t* rows = reinterpret_cast<int32_t*>(smem_rd + L.rows_off);
+  uint32_t* masks = reinterpret_cast<uint32_t*>(smem_rd + L.masks_off);
+  int* cnt = reinterpret_cast<int*>(smem_rd + L.cnt_off);
+  int* off = reinterpret_cast<int*>(smem_rd + L.off_off);
+  int* scratch = reinterpret_cast<int*>(smem_rd + L.scratch_off);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c = static_cast<int>(cluster_ctarank());
+  const int nc = static_cast<int>(cluster_nctarank());
+  const int e0 = c * p.E / nc, e1 = (c + 1) * p.E / nc;
+  const int units = p.H / 8;  // 16-byte units per row
+  for (int i = tid; i < 2 * p.E; i += kRcThreads) masks[i] = 0u;
+  cluster_arrive_relaxed();  // waited on after the tokens are staged
+  // Warp w takes experts e0 + w, e0 + w + 8, ... Their router rows are fetched into L2
+  // while the previous kernel on the stream may still run (a prefetch reads nothing into
+  // the SM, so a row written by that kernel is still read afresh below).
+  if (lane == 0)
+    for (int e = e0 + warp; e < e1; e += kRcWarps)
+      bulk_prefetch_l2(p.wr + static_cast<size_t>(e) * units, static_cast<uint32_t>(units * 16));
+
+  grid_dep_wait();  // x may come from the previous kernel on the stream
+  grid_dep_trigger();
+
+  // the first chunk of this warp's first router row, in flight while the tokens are staged
+  uint4 wv[kRdChunk];
+  auto load_chunk = [&](int e, int u0) {
+    const uint4* row = p.wr + static_cast<size_t>(e) * units;
+#pragma unroll
+    for (int j = 0; j < kRdChunk; ++j) {
+      const int u = u0 + 32 * j + lane;
+      wv[j] = u < units ? __ldg(row + u) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  if (e0 + warp < e1) load_chunk(e0 + warp, 0);
+
+  // ---- 1. the tokens into shared memory (all of a thread's loads in flight at once) ----
+  {
+    const int n = p.T * units;
+#pragma unroll 8
+    for (int i = tid; i < n; i += kRcThreads) xs[i] = __ldg(p.x + i);
+    for (int i = n + tid; i < NT * units; i += kRcThreads) xs[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  __syncthreads();
+  cluster_wait();  // every CTA of the cluster is running: its shared memory may be written
+
+  // ---- 2. logits of this CTA's experts: warp per expert, lanes over H ------------------
+  // Each lane adds its units in order and the warp sums the lanes by a fixed butterfly, so
+  // a logit is the same on every run; the lanes holding it store it into every CTA's table.
+  const uint32_t ls_addr = smem_u32(Ls);
+  for (int e = e0 + warp; e < e1; e += kRcWarps) {
+    const float be = p.bias != nullptr ? __ldg(p.bias + e) : 0.f;
+    float acc[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc[t] = 0.f;
+    for (int u0 = 0; u0 < units; u0 += 32 * kRdChunk) {
+      if (u0 != 0 || e != e0 + warp) load_chunk(e, u0);
+#pragma unroll
+      for (int j = 0; j < kRdChunk; ++j) {
+        const int u = u0 + 32 * j + lane;
+        if (u < units) {
+          const float2 w0 = bf2_to_f2(wv[j].x), w1 = bf2_to_f2(wv[j].y);
+          const float2 w2 = bf2_to_f2(wv[j].z), w3 = bf2_to_f2(wv[j].w);
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            const uint4 xv = xs[t * units + u];
+            const float2 x0 = bf2_to_f2(xv.x), x1 = bf2_to_f2(xv.y);
+            const float2 x2 = bf2_to_f2(xv.z), x3 = bf2_to_f2(xv.w);
+            float a = acc[t];
+            a = fmaf(w0.x, x0.x, a);
+            a = fmaf(w0.y, x0.y, a);
+            a = fmaf(w1.x, x1.x, a);
+            a = fmaf(w1.y, x1.y, a);
+            a = fmaf(w2.x, x2.x, a);
+            a = fmaf(w2.y, x2.y, a);
+            a = fmaf(w3.x, x3.x, a);
+            a = fmaf(w3.y, x3.y, a);
+            acc[t] = a;
           }
         }
-#pragma unroll
-        for (int b = 0; b < kBurst; ++b) {
-          const int i = i0 + b * 32 + lane;
-          if (i < row_units) {
-            if (r0 >= 0) p.x_perm[static_cast<size_t>(r0) * row_units + i] = v0[b];
-            if (r1 >= 0) p.x_perm[static_cast<size_t>(r1) * row_units + i] = v1[b];
-          }
-        }
       }
     }
+    int t = 0;
+    const float v = warp_sum_scatter<NT>(acc, lane, t) + be;
+    if (t < p.T) {
+      constexpr int kGroup = 32 / NT;  // lanes holding token t
+      const uint32_t a = ls_addr + static_cast<uint32_t>((t * p.E + e) * 4);
+      for (int r = lane & (kGroup - 1); r < nc; r += kGroup)
+        st_shared_cluster(mapa_shared(a, static_cast<uint32_t>(r)), __float_as_int(v));
+    }
   }
+  cluster_sync_all();  // every CTA holds all logits; the last remote access
+
+  // ---- 3. top-k of every token, in every CTA ---------------------------------------------
+  if (warp < p.T) {
+    warp_topk_softmax(Ls + warp * p.E, p.E, p.K, p.theta, sid + warp * p.K, sw + warp * p.K);
+    __syncwarp();
+  }
+  __syncthreads();
+  // CTA c stores the routing results of tokens c, c + nc, ...
+  for (int t = c; t < p.T; t += nc) {
+    for (int e = tid; e < p.E; e += kRcThreads)
+      p.logits[static_cast<size_t>(t) * p.E + e] = Ls[t * p.E + e];
+    if (tid < p.K) {
+      p.ids[static_cast<size_t>(t) * p.K + tid] = sid[t * p.K + tid];
+      p.w[static_cast<size_t>(t) * p.K + tid] = sw[t * p.K + tid];
+    }
+  }
+  if (p.counts == nullptr) return;
+  rc_sort_and_dispatch(p, c, nc, sid, sw, masks, cnt, off, rows, scratch);
 }
 
 struct RcDevice {
   bool ready = false;
+  bool dot_ready = false;
   int nc = 0;  // cluster size that fits (16 or 8), 0 if none
 };
+
 RcDevice g_rc[64];
 
 int rc_stages(int npad, int nmt, int E, int K, int T, int kb_total, int nc) {
@@ -466,12 +695,33 @@ cudaError_t launch_route_cluster(const void* x, const void* w_router, const floa
     d.ready = true;
   }
   if (d.nc == 0) return cudaErrorNotSupported;
+  // up to kRdMaxT tokens, when the tokens fit in shared memory: the expert-split kernel
+  int nt = 1;
+  while (nt < T) nt <<= 1;
+  const bool dot = T <= kRdMaxT && rd_layout(nt, H, E, K).total <= kRcSmemBudget;
+  if (dot && !d.dot_ready) {
+    for (const void* f : {reinterpret_cast<const void*>(route_dispatch_dot_kernel<1>),
+                          reinterpret_cast<const void*>(route_dispatch_dot_kernel<2>),
+                          reinterpret_cast<const void*>(route_dispatch_dot_kernel<4>)}) {
+      e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kRcSmemBudget);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
+    d.dot_ready = true;
+  }
   RcParams p;
   std::memset(&p, 0, sizeof(p));
-  if (!make_tma_2d_bf16(&p.tmX, x, static_cast<uint64_t>(T), static_cast<uint64_t>(H),
-                        static_cast<uint32_t>(npad)) ||
-      !make_tma_2d_bf16(&p.tmW, w_router, static_cast<uint64_t>(E), static_cast<uint64_t>(H), 128))
+  if (dot) {
+    // the rows are read in 16-byte units
+    if (((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w_router)) & 15u) != 0u)
+      return cudaErrorInvalidValue;
+  } else if (!make_tma_2d_bf16(&p.tmX, x, static_cast<uint64_t>(T), static_cast<uint64_t>(H),
+                               static_cast<uint32_t>(npad)) ||
+             !make_tma_2d_bf16(&p.tmW, w_router, static_cast<uint64_t>(E),
+                               static_cast<uint64_t>(H), 128)) {
     return cudaErrorInvalidValue;
+  }
   p.bias = bias;
   p.logits = logits;
   p.ids = ids;
@@ -482,6 +732,7 @@ cudaError_t launch_route_cluster(const void* x, const void* w_router, const floa
   p.inv = inv;
   p.row_w = row_w;
   p.x = static_cast<const uint4*>(x);
+  p.wr = static_cast<const uint4*>(w_router);
   p.x_perm = static_cast<uint4*>(x_perm);
   p.err = err;
   p.T = T;
@@ -496,7 +747,7 @@ cudaError_t launch_route_cluster(const void* x, const void* w_router, const floa
   while (cols < nmt * npad) cols <<= 1;
   p.tmem_cols = cols;
   p.theta = theta;
-  const int smem = rc_layout(npad, nmt, E, K, T, p.stages).total;
+  const int smem = dot ? rd_layout(nt, H, E, K).total : rc_layout(npad, nmt, E, K, T, p.stages).total;
 
   cudaLaunchConfig_t lc;
   std::memset(&lc, 0, sizeof(lc));
@@ -513,7 +764,12 @@ cudaError_t launch_route_cluster(const void* x, const void* w_router, const floa
   at[1].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = at;
   lc.numAttrs = 2;
-  return count_launch(cudaLaunchKernelEx(&lc, route_dispatch_cluster_kernel, p));
+  if (!dot) return count_launch(cudaLaunchKernelEx(&lc, route_dispatch_cluster_kernel, p));
+  switch (nt) {
+    case 1: return count_launch(cudaLaunchKernelEx(&lc, route_dispatch_dot_kernel<1>, p));
+    case 2: return count_launch(cudaLaunchKernelEx(&lc, route_dispatch_dot_kernel<2>, p));
+    default: return count_launch(cudaLaunchKernelEx(&lc, route_dispatch_dot_kernel<4>, p));
+  }
 }
 
 }  // namespace moe

@@ -585,6 +585,14 @@ CLUSTER_CASES = [
     (64, 7168, 256, 8, 0.05, "zipf", False),   # 7 k-blocks per CTA through the stage ring
     (8, 64, 8, 2, 0.0, "none", False),         # one k-block for the whole cluster
     (48, 512, 96, 8, 0.0, "none", True),       # exact ties between duplicated experts
+    # up to 4 tokens the logits are split by expert over the cluster's CTAs
+    (4, 7168, 256, 8, 0.05, "zipf", False),    # 16 experts per CTA, 28 row units per lane
+    (4, 320, 40, 6, 0.1, "normal", False),     # ragged units per lane; 2-3 experts per CTA
+    (4, 512, 96, 8, 0.0, "none", True),        # exact ties between duplicated experts
+    (2, 2048, 128, 8, 0.0, "normal", False),
+    (3, 1024, 64, 4, 0.0, "zipf", False),      # padded to 4 tokens; 4 experts per CTA
+    (2, 64, 8, 2, 0.0, "none", False),         # fewer experts than CTAs: some have none
+    (5, 2048, 128, 8, 0.0, "normal", False),   # the first H-split size
 ]
 
 
