@@ -161,11 +161,6 @@ __device__ __forceinline__ int ld_dsmem_s32(uint32_t cluster_addr) {
   asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
   return v;
 }
-// Bulk prefetch of `bytes` (a multiple of 16) at `src` (16-byte aligned) into L2.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 // Split cluster barrier: arrive now, wait later (no memory ordering: it only tells a CTA
 // that every CTA of the cluster is running, before the first write into their shared memory).
 __device__ __forceinline__ void cluster_arrive_relaxed() {
@@ -528,17 +523,13 @@ __global__ void __launch_bounds__(kRcThreads, 1)
   const int units = p.H / 8;  // 16-byte units per row
   for (int i = tid; i < 2 * p.E; i += kRcThreads) masks[i] = 0u;
   cluster_arrive_relaxed();  // waited on after the tokens are staged
-  // Warp w takes experts e0 + w, e0 + w + 8, ... Their router rows are fetched into L2
-  // while the previous kernel on the stream may still run (a prefetch reads nothing into
-  // the SM, so a row written by that kernel is still read afresh below).
-  if (lane == 0)
-    for (int e = e0 + warp; e < e1; e += kRcWarps)
-      bulk_prefetch_l2(p.wr + static_cast<size_t>(e) * units, static_cast<uint32_t>(units * 16));
 
   grid_dep_wait();  // x may come from the previous kernel on the stream
   grid_dep_trigger();
 
-  // the first chunk of this warp's first router row, in flight while the tokens are staged
+  // Warp w takes experts e0 + w, e0 + w + 8, ...: the first chunk of its first router row
+  // is in flight while the tokens are staged.  (An L2 bulk prefetch of the rows before
+  // griddepcontrol.wait measured no faster.)
   uint4 wv[kRdChunk];
   auto load_chunk = [&](int e, int u0) {
     const uint4* row = p.wr + static_cast<size_t>(e) * units;
