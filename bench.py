@@ -24,8 +24,8 @@ host buffers: every step's H2D of x and D2H of y inside the timed region; for pr
 layers whose weights exceed L2 the copies of neighbouring steps run on copy streams while a
 step computes, and the serial figure is kept beside it), "stages_us" (route /
 permute / gate_up / down / shared / combine, timed one by one), "gpu_launches" (the
-library's own launch counter over the timed region), "clocks" (nvidia-smi samples taken
-during the timed region).
+library's own launch counter over the timed region), "clocks" (SM clock and clock-event
+reasons sampled during the timed region: NVML every 10 ms, else nvidia-smi every 200 ms).
 """
 
 from __future__ import annotations
@@ -121,36 +121,97 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
+    """SM clock and clock-event reasons sampled while the timed region runs. Through NVML
+    (ctypes on the driver's libnvidia-ml) every 10 ms where it loads, else from nvidia-smi
+    every 200 ms. Only samples taken between entering and leaving the region count; if the
+    region is shorter than one nvidia-smi period, the first sample after it stands in."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # clock-event reason bits of the NVML API
+    NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                    0x40: "hw_thermal_slowdown"}
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.lines = []
+        self.nvml = None
+        self.samples = []  # (monotonic time, sm MHz, max MHz, reason names)
+        self.source = None
+        self.t0 = self.t1 = None
+        self.stop = threading.Event()
+
+    def _nvml_open(self):
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return False
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.gpu), ctypes.byref(h)) != 0:
+                lib.nvmlShutdown()
+                return False
+            reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        except (OSError, AttributeError):
+            return False
+        self.nvml = (lib, h, reasons, ctypes)
+        return True
+
+    def _nvml_loop(self):
+        lib, h, reasons, ctypes = self.nvml
+        sm, mx, bits = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop.is_set():
+            ok = (lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) == 0 and
+                  lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 and
+                  reasons(h, ctypes.byref(bits)) == 0)
+            if ok:
+                names = [n for b, n in self.NVML_REASONS.items() if bits.value & b]
+                self.samples.append((time.monotonic(), float(sm.value), float(mx.value), names))
+            self.stop.wait(0.01)
+
+    def _smi_loop(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.strip().split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm, mx = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            active = [n for n, v in zip(names, parts[5:9]) if v.lower() == "active"]
+            self.samples.append((time.monotonic(), sm, mx, active))
 
     def __enter__(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
+        if self._nvml_open():
+            self.source = "nvml, every 10 ms"
+            self.thread = threading.Thread(target=self._nvml_loop, daemon=True)
             self.thread.start()
-        except (OSError, FileNotFoundError):
-            self.proc = None
+        else:
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                     "--format=csv,noheader,nounits", "-lms", "200"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                self.source = "nvidia-smi, every 200 ms"
+                self.thread = threading.Thread(target=self._smi_loop, daemon=True)
+                self.thread.start()
+            except (OSError, FileNotFoundError):
+                self.proc = None
+        self.t0 = time.monotonic()
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
     def __exit__(self, *a):
-        if self.proc is not None:
-            time.sleep(0.25)
+        self.t1 = time.monotonic()
+        if self.nvml is not None:
+            self.stop.set()
+            self.thread.join(timeout=1)
+            self.nvml[0].nvmlShutdown()
+        elif self.proc is not None:
+            if not any(self.t0 <= t <= self.t1 for t, *_ in self.samples):
+                time.sleep(0.25)  # the region was shorter than one period: take the next
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -158,22 +219,14 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx = float(parts[2])
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        inside = [x for x in self.samples if self.t0 <= x[0] <= self.t1]
+        if not inside:
+            inside = [x for x in self.samples if x[0] > self.t1][:1]
+        sm = [x[1] for x in inside]
+        reasons = sorted({n for x in inside for n in x[3]})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": inside[-1][2] if inside else None,
+                "reasons": reasons, "samples": len(sm), "source": self.source}
 
 
 def gate_up_kernel(shape, T):
